@@ -1,0 +1,123 @@
+"""Exact decoding of one expert's pageable bytes into float64 weight matrices.
+
+Source: "Running an MoE Model Larger Than Your VRAM", section "What does Paged
+Experts actually do?" (PR #42557 adds bf16, block-FP8 and GPTQ experts) and
+section "Can paging change the model's outputs?" (every per-expert tensor,
+including scales and zero points, is paged with the expert).
+
+An expert is one contiguous byte string that holds all of its tensors. The
+layout is this library's own (the pages fix none); it is restated here from the
+layout contract, independently of the CUDA code:
+
+  bf16  (format 0)
+      W_gu  bf16 [2I][H]   rows 0..I-1 gate_proj, rows I..2I-1 up_proj
+      W_d   bf16 [H][I]    down_proj
+  block-FP8 (format 1), H and I multiples of 128
+      Q_gu  e4m3 [2I][H]
+      Q_d   e4m3 [H][I]
+      S_gu  fp32 [2I/128][H/128]   one scale per 128x128 block: w = e4m3(q) * s
+      S_d   fp32 [H/128][I/128]
+  GPTQ int4, group 128 (format 2), H and I multiples of 128
+      Q_gu  u8 [2I][H/2]   element c of a row: byte c//2, low nibble if c even
+      Q_d   u8 [H][I/2]
+      SZ_gu fp16 [2I][H/128][2]   (scale, zero) per output row and input group
+      SZ_d  fp16 [H][I/128][2]
+      w[n, c] = (q[n, c] - z[n, c//128]) * s[n, c//128]
+
+All sections are packed back to back in the order listed, with no padding.
+TEST INFRASTRUCTURE ONLY (see the package docstring).
+"""
+
+import numpy as np
+
+BF16, FP8_BLOCK128, INT4_GPTQ_G128 = 0, 1, 2
+
+
+def expert_nbytes(fmt, H, I):
+    """Bytes of one expert in the given format (sum of the sections above)."""
+    n_w = 3 * H * I
+    if fmt == BF16:
+        return 2 * n_w
+    if fmt == FP8_BLOCK128:
+        return n_w + 4 * ((2 * I // 128) * (H // 128) + (H // 128) * (I // 128))
+    if fmt == INT4_GPTQ_G128:
+        return n_w // 2 + 4 * ((2 * I) * (H // 128) + H * (I // 128))
+    raise ValueError("unknown format")
+
+
+def bf16_bits_to_f64(u16):
+    """bf16 bit patterns -> float64 (exact: bf16 is the top half of an fp32)."""
+    u32 = np.asarray(u16, dtype=np.uint16).astype(np.uint32) << 16
+    return u32.view(np.float32).astype(np.float64)
+
+
+def e4m3_value(code):
+    """Value of one OCP FP8 E4M3 ("e4m3fn") code, from the format's definition.
+
+    1 sign bit, 4 exponent bits with bias 7, 3 mantissa bits; exponent 0 is
+    subnormal (m/8 * 2^-6); S.1111.111 is NaN; there is no infinity.
+    """
+    s = -1.0 if code & 0x80 else 1.0
+    e = (code >> 3) & 0xF
+    m = code & 0x7
+    if e == 0xF and m == 0x7:
+        return float("nan")
+    if e == 0:
+        return s * (m / 8.0) * 2.0 ** -6
+    return s * (1.0 + m / 8.0) * 2.0 ** (e - 7)
+
+
+E4M3_TABLE = np.array([e4m3_value(c) for c in range(256)], dtype=np.float64)
+
+
+def _take(buf, off, nbytes):
+    return buf[off:off + nbytes], off + nbytes
+
+
+def decode_expert(buf, fmt, H, I):
+    """Decode one expert's bytes -> (W_g [I,H], W_u [I,H], W_d [H,I]) float64."""
+    buf = np.frombuffer(bytes(buf), dtype=np.uint8) if not isinstance(buf, np.ndarray) else buf.view(np.uint8).reshape(-1)
+    if buf.size != expert_nbytes(fmt, H, I):
+        raise ValueError("expert byte size does not match the format")
+    off = 0
+    if fmt == BF16:
+        raw, off = _take(buf, off, 2 * 2 * I * H)
+        Wgu = bf16_bits_to_f64(raw.view(np.uint16)).reshape(2 * I, H)
+        raw, off = _take(buf, off, 2 * H * I)
+        Wd = bf16_bits_to_f64(raw.view(np.uint16)).reshape(H, I)
+    elif fmt == FP8_BLOCK128:
+        qgu, off = _take(buf, off, 2 * I * H)
+        qd, off = _take(buf, off, H * I)
+        sgu, off = _take(buf, off, 4 * (2 * I // 128) * (H // 128))
+        sd, off = _take(buf, off, 4 * (H // 128) * (I // 128))
+        Sgu = sgu.view(np.float32).astype(np.float64).reshape(2 * I // 128, H // 128)
+        Sd = sd.view(np.float32).astype(np.float64).reshape(H // 128, I // 128)
+        Wgu = E4M3_TABLE[qgu].reshape(2 * I, H)
+        Wd = E4M3_TABLE[qd].reshape(H, I)
+        # block (n // 128, c // 128) carries one scale
+        Wgu = Wgu * np.repeat(np.repeat(Sgu, 128, axis=0), 128, axis=1)
+        Wd = Wd * np.repeat(np.repeat(Sd, 128, axis=0), 128, axis=1)
+    elif fmt == INT4_GPTQ_G128:
+        qgu, off = _take(buf, off, I * H)
+        qd, off = _take(buf, off, H * I // 2)
+        szgu, off = _take(buf, off, 4 * 2 * I * (H // 128))
+        szd, off = _take(buf, off, 4 * H * (I // 128))
+        Wgu = _int4_rows(qgu, szgu, 2 * I, H)
+        Wd = _int4_rows(qd, szd, H, I)
+    else:
+        raise ValueError("unknown format")
+    if off != buf.size:
+        raise AssertionError("layout sections do not cover the expert")
+    return Wgu[:I], Wgu[I:], Wd
+
+
+def _int4_rows(qbytes, szbytes, n_rows, n_cols):
+    """GPTQ int4 rows: q nibbles (low first), per-(row, group of 128) fp16 (s, z)."""
+    q = qbytes.reshape(n_rows, n_cols // 2)
+    nib = np.empty((n_rows, n_cols), dtype=np.float64)
+    nib[:, 0::2] = (q & 0x0F).astype(np.float64)
+    nib[:, 1::2] = (q >> 4).astype(np.float64)
+    sz = szbytes.view(np.float16).astype(np.float64).reshape(n_rows, n_cols // 128, 2)
+    s = np.repeat(sz[:, :, 0], 128, axis=1)
+    z = np.repeat(sz[:, :, 1], 128, axis=1)
+    return (nib - z) * s
