@@ -1,0 +1,408 @@
+"""Benchmark of the paged-expert MoE layer on one GB300 (or N independent replicas).
+
+Default workload: one Qwen3-30B-A3B-shaped MoE layer (E=128, top_k=8, H=2048,
+I=768), bf16 experts, K=40 slots, single-stream decode (B=1) over a 256-step routing
+trace in which every expert of a stream's previous step is kept with p=0.8. A step is
+one pass of the whole path over one batch: router -> residency step (dedup, LRU,
+waves) -> page-in of the misses -> grouping -> gate/up + SiLU*mul -> down ->
+weighted combine. B=2 and B=4 are reported alongside under "batches".
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Timing: W untimed warm-up steps, then K timed steps; L2 is flushed (256 MB write)
+before every timed step, outside the events; each step is bracketed by CUDA events
+on the stream it runs on; a barrier and torch.cuda.synchronize() bracket the timed
+loop; the max over ranks is reported. The reference arm times the oracle (plain
+CPU float64) on the host cores on the same workload.
+"""
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from workloads import generators as gen  # noqa: E402
+
+METRIC = "MoE layer tokens/s and expert-weight HBM GB/s (% of 8 TB/s); paged decode tok/s"
+E, TOPK, H, I = 128, 8, 2048, 768
+K_SLOTS = 40
+TRACE_STEPS = 256
+SEED = 0
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            return float(d.get("hbm_gbs", FALLBACK_HBM_GBS)), float(d.get("bf16_tflops", FALLBACK_BF16_TFLOPS)), \
+                "measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+# --------------------------------------------------------------------------- inputs
+
+def make_inputs(B, seed=SEED):
+    rng = np.random.default_rng([seed, B])
+    trace = gen.reuse_routing_trace(rng, E, TOPK, B, TRACE_STEPS, p=0.8)
+    xs, logits = [], []
+    for sets in trace:
+        logits.append(gen.logits_for_sets(rng, sets, E))
+        xs.append(gen.activations_bf16(rng, B, H))
+    distinct = [len({e for st in sets for e in st}) for sets in trace]
+    return trace, xs, logits, distinct
+
+
+def make_store(fmt=0, seed=SEED):
+    return gen.layer_store(fmt, H, I, E, seed, 0)
+
+
+# --------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self, t0, t1):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = [l for t, l in self.lines if t0 - 0.15 <= t <= t1 + 0.15] or [l for _, l in self.lines[-3:]]
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            f = [x.strip() for x in r.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(smax)), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- distributed (replicas only)
+
+def dist_init():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if os.environ.get("PMOE_BENCH_BACKEND", "nccl") == "nccl" else "gloo"
+        dist.init_process_group(backend=backend)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def reduce_max(v, ws, device):
+    """Max of a float over ranks (the slowest replica sets the job time)."""
+    if ws == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(units_per_rank, time_s_per_rank):
+    """Whole-job throughput of independent replicas: all units over the slowest rank's time."""
+    return float(sum(units_per_rank)) / float(max(time_s_per_rank))
+
+
+# --------------------------------------------------------------------------- our arm
+
+def run_decode(pm, torch, store, B, steps, warmup, device, timed_clock=None, e2e=True):
+    trace, xs, logits, distinct = make_inputs(B)
+    cache = pm.ExpertCache(E, TOPK, H, I, K_SLOTS, fmt=pm.PMOE_BF16, max_tokens=B, device=device)
+    cache.load_layer(0, store)
+    dev = torch.device("cuda", device)
+    x_dev = [torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(dev) for x in xs]
+    l_dev = [torch.from_numpy(l).to(dev) for l in logits]
+    ids = torch.empty((B, TOPK), dtype=torch.int32, device=dev)
+    w = torch.empty((B, TOPK), dtype=torch.float32, device=dev)
+    y = torch.empty((B, H), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def one(s):
+        pm.moe_router_topk(l_dev[s], TOPK, ids_out=ids, w_out=w)
+        cache.moe_paged_forward(0, x_dev[s], ids, w, y=y)
+
+    for i in range(warmup):
+        one(i % TRACE_STEPS)
+    torch.cuda.synchronize(dev)
+    stats0 = cache.expert_cache_stats(0)
+    cache.expert_cache_set_timing(True)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    step_ids = [(warmup + i) % TRACE_STEPS for i in range(steps)]
+    torch.cuda.synchronize(dev)
+    t0 = time.time()
+    for i, s in enumerate(step_ids):
+        flush.zero_()
+        evs[i][0].record(stream)
+        one(s)
+        evs[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    t1 = time.time()
+    ms = [a.elapsed_time(b) for a, b in evs]
+    kt = cache.expert_cache_kernel_times()
+    stats1 = cache.expert_cache_stats(0)
+    total_ms = float(sum(ms))
+    d_steps = [distinct[s] for s in step_ids]
+    res = {
+        "B": B, "steps": steps, "total_ms": total_ms, "ms_per_step": total_ms / steps,
+        "tokens_per_s": B * steps / (total_ms / 1e3), "t_wall": (t0, t1),
+        "kernel_times": kt, "distinct_per_step": float(np.mean(d_steps)),
+        "misses_per_step": (stats1["misses"] - stats0["misses"]) / steps,
+        "hit_rate": (stats1["hits"] - stats0["hits"]) / max(1, (stats1["hits"] - stats0["hits"]) +
+                                                            (stats1["misses"] - stats0["misses"])),
+        "waves_per_step": (stats1["waves"] - stats0["waves"]) / steps,
+        "bytes_paged_per_step": (stats1["bytes_paged"] - stats0["bytes_paged"]) / steps,
+        "gateup_weight_bytes": sum(d * 2 * I * H * 2 for d in d_steps),
+        "down_weight_bytes": sum(d * H * I * 2 for d in d_steps),
+        "launches": sum(v["launches"] for k_, v in kt.items() if k_ != "copies") + steps,  # + router
+    }
+    cache.expert_cache_set_timing(False)
+    if e2e:
+        # end to end: pinned host inputs -> device, the layer, result -> pinned host, every step
+        x_h = [torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory() for x in xs]
+        l_h = [torch.from_numpy(l).pin_memory() for l in logits]
+        y_h = torch.empty((B, H), dtype=torch.bfloat16).pin_memory()
+        x_d = torch.empty((B, H), dtype=torch.bfloat16, device=dev)
+        l_d = torch.empty((B, E), dtype=torch.float32, device=dev)
+        evs2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for i, s in enumerate(step_ids):
+            flush.zero_()
+            evs2[i][0].record(stream)
+            x_d.copy_(x_h[s], non_blocking=True)
+            l_d.copy_(l_h[s], non_blocking=True)
+            pm.moe_router_topk(l_d, TOPK, ids_out=ids, w_out=w)
+            cache.moe_paged_forward(0, x_d, ids, w, y=y)
+            y_h.copy_(y, non_blocking=True)
+            evs2[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = float(sum(a.elapsed_time(b) for a, b in evs2))
+        res["e2e"] = {"value": B * steps / (e2e_ms / 1e3), "unit": "tokens/s",
+                      "h2d_bytes_per_step": B * H * 2 + B * E * 4, "d2h_bytes_per_step": B * H * 2}
+    cache.close()
+    return res
+
+
+def cpu_baseline_decode(B=1, budget_s=15.0, max_steps=400, store=None):
+    """The oracle as it stands (float64 NumPy + the pure-Python LRU simulator) on the host
+    cores, on the first steps of the same trace until the time budget is spent."""
+    from oracle import lru as olru
+    from oracle import moe as omoe
+    from oracle import router as orouter
+    trace, xs, logits, _ = make_inputs(B)
+    store = make_store() if store is None else store
+    experts = omoe.ExpertSource(lambda e: store[e], 0, H, I, cache=48)
+    sim = olru.LayerLRU(E, K_SLOTS)
+    t0 = time.time()
+    n = 0
+    while n < min(max_steps, TRACE_STEPS) and time.time() - t0 < budget_s:
+        ids, w = orouter.router_topk(logits[n], TOPK)
+        sim.step(ids.ravel().tolist())
+        omoe.moe_layer(gen.bf16_bits_to_float(xs[n]).astype(np.float64), ids, w, experts)
+        n += 1
+    dt = time.time() - t0
+    cores = len(os.sched_getaffinity(0))
+    return {"value": B * n / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"first {n} decode steps (B={B}) of the same 256-step trace: float64 NumPy router + "
+                      f"SwiGLU experts decoded from the same bytes + LRU simulator, {dt:.1f} s"}
+
+
+def run_ours(args):
+    import torch
+    ws, rank, local = dist_init()
+    torch.cuda.set_device(local)
+    import paged_expert_moe_gb300 as pm
+    pm.load()
+    store = make_store()
+    hbm_peak, _, peak_kind = _peaks()
+    barrier(ws)
+    torch.cuda.synchronize()
+    clock = ClockSampler(local).start() if rank == 0 else None
+    time.sleep(0.3)
+    head = run_decode(pm, torch, store, 1, args.steps, args.warmup, local)
+    torch.cuda.synchronize()
+    barrier(ws)
+    clocks = clock.stop(*head["t_wall"]) if clock else None
+    others = {}
+    if not args.headline_only:
+        for B in (2, 4):
+            others[B] = run_decode(pm, torch, store, B, args.steps, args.warmup, local, e2e=False)
+    job_ms = reduce_max(head["total_ms"], ws, torch.device("cuda", local))
+    value = ws * 1 * args.steps / (job_ms / 1e3)
+    if rank != 0:
+        return
+    kt = head["kernel_times"]
+    gu_ms = kt["gateup"]["ms"]
+    gu_launch = max(1, kt["gateup"]["launches"])
+    achieved = head["gateup_weight_bytes"] / (gu_ms / 1e3) / 1e9
+    layer_ms = gu_ms + kt["down"]["ms"]
+    layer_gbs = (head["gateup_weight_bytes"] + head["down_weight_bytes"]) / (layer_ms / 1e3) / 1e9
+    traffic = None
+    tp = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tp):
+        try:
+            traffic = json.load(open(tp)).get("decode_gateup_bf16_B1")
+        except Exception:
+            traffic = None
+    out = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": job_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "Qwen3-30B-A3B-shaped MoE layer, bf16 experts, decode B=1, K=40 slots, "
+                               "256-step p=0.8 reuse routing trace",
+                   "E": E, "top_k": TOPK, "hidden": H, "intermediate": I, "K": K_SLOTS, "batch": 1,
+                   "pagein": "copy engine (cudaMemcpyAsync from pinned host store)",
+                   "l2": "flushed before every timed step (256 MB write, outside the events)",
+                   "parallelism": f"replicas x{ws}"},
+        "expert_weight_hbm_gbs": layer_gbs,
+        "expert_weight_hbm_frac": layer_gbs / hbm_peak,
+        "roofline": {"kernel": "gemv_gateup (decode gate/up + SiLU*mul)", "bound": "hbm", "achieved": achieved,
+                     "peak": hbm_peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / hbm_peak,
+                     "traffic": traffic,
+                     "avg_launch_us": gu_ms / gu_launch * 1e3,
+                     "algorithmic_bytes_per_launch": head["gateup_weight_bytes"] / gu_launch},
+        "layer": {"misses_per_step": head["misses_per_step"], "hit_rate": head["hit_rate"],
+                  "waves_per_step": head["waves_per_step"], "distinct_experts_per_step": head["distinct_per_step"],
+                  "bytes_paged_per_step": head["bytes_paged_per_step"],
+                  "kernel_ms_per_step": {k_: v["ms"] / args.steps for k_, v in kt.items() if k_ != "copies"},
+                  "copies_per_step": kt["copies"] / args.steps},
+        "batches": {f"B{B}": {"tokens_per_s": r["tokens_per_s"], "ms_per_step": r["ms_per_step"],
+                              "misses_per_step": r["misses_per_step"], "waves_per_step": r["waves_per_step"],
+                              "gateup_gbs": r["gateup_weight_bytes"] / (r["kernel_times"]["gateup"]["ms"] / 1e3) / 1e9,
+                              "down_gbs": r["down_weight_bytes"] / (r["kernel_times"]["down"]["ms"] / 1e3) / 1e9}
+                    for B, r in others.items()},
+        "e2e": head.get("e2e"),
+        "gpu_launches": head["launches"],
+        "clocks": clocks,
+        "impl": "ours",
+    }
+    if not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline_decode(1, budget_s=args.cpu_budget, store=store)
+    print(json.dumps(out))
+
+
+# --------------------------------------------------------------------------- reference arm (the oracle)
+
+def run_reference(args):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from oracle import lru as olru
+    from oracle import moe as omoe
+    from oracle import router as orouter
+    B = 1
+    trace, xs, logits, _ = make_inputs(B)
+    store = make_store()
+    experts = omoe.ExpertSource(lambda e: store[e], 0, H, I, cache=48)
+    sim = olru.LayerLRU(E, K_SLOTS)
+
+    def one(s):
+        ids, w = orouter.router_topk(logits[s], TOPK)
+        sim.step(ids.ravel().tolist())
+        omoe.moe_layer(gen.bf16_bits_to_float(xs[s]).astype(np.float64), ids, w, experts)
+
+    # each step is one decode step of the trace; the run is capped so it ends within minutes
+    budget = args.cpu_budget * 6
+    t_start = time.time()
+    for i in range(args.warmup):
+        one(i % TRACE_STEPS)
+    n = 0
+    t0 = time.time()
+    while n < args.steps and time.time() - t0 < budget:
+        one((args.warmup + n) % TRACE_STEPS)
+        n += 1
+    dt = time.time() - t0
+    cores = len(os.sched_getaffinity(0))
+    v = B * n / dt
+    out = {
+        "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": ws, "steps": n, "warmup": args.warmup,
+        "ms_per_step": dt / max(n, 1) * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic", "impl": "reference",
+        "config": {"workload": "Qwen3-30B-A3B-shaped MoE layer, bf16 experts, decode B=1, K=40 slots, "
+                               "256-step p=0.8 reuse routing trace", "E": E, "top_k": TOPK, "hidden": H,
+                   "intermediate": I, "K": K_SLOTS, "batch": 1},
+        "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{n} decode steps after {args.warmup} warm-up steps, "
+                                   f"{time.time() - t_start:.1f} s in all"},
+        "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--headline-only", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

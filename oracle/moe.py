@@ -41,16 +41,22 @@ def expert_hidden(x, Wg, Wu):
 class ExpertSource:
     """Maps an expert id to its float64 matrices, decoding bytes on demand."""
 
-    def __init__(self, get_bytes, fmt, H, I, cache=True):
+    def __init__(self, get_bytes, fmt, H, I, cache=64):
         self._get = get_bytes
         self.fmt, self.H, self.I = fmt, H, I
-        self._cache = {} if cache else None
+        self._limit = cache
+        self._cache = {}
 
     def __call__(self, e):
-        if self._cache is not None and e in self._cache:
-            return self._cache[e]
-        m = decode_expert(self._get(int(e)), self.fmt, self.H, self.I)
-        if self._cache is not None:
+        e = int(e)
+        if e in self._cache:
+            m = self._cache.pop(e)
+            self._cache[e] = m  # most recent last
+            return m
+        m = decode_expert(self._get(e), self.fmt, self.H, self.I)
+        if self._limit:
+            if len(self._cache) >= self._limit:
+                self._cache.pop(next(iter(self._cache)))
             self._cache[e] = m
         return m
 
@@ -90,18 +96,21 @@ def moe_layer(x, ids, w, experts):
     return y, n_act
 
 
-def moe_stack(x, layers):
-    """A stack of MoE layers with attention omitted: x_{l+1} = moe_layer_l(x_l).
+def moe_stack(x, layers, residual=False):
+    """A stack of MoE layers with attention omitted.
 
-    layers: list of (ids, w, experts), one per layer, routing given per layer
-    (the reading for a stack with attention omitted: synthetic per-layer routing
-    that does not depend on the layer's input). Returns the final activations and
-    the total number of expert activations; for one token that is layers x top_k
-    ("Why is it fast when experts keep crossing PCIe?": 48 x 8 = 384).
+    layers: list of (ids, w, experts), one per layer, routing given per layer (the
+    reading for a stack with attention omitted: synthetic per-layer routing that
+    does not depend on the layer's input). Without `residual` each layer feeds the
+    next, x_{l+1} = moe_l(x_l); with it the layers add to a residual stream,
+    x_{l+1} = x_l + moe_l(x_l), as a decoder block does. Returns the final
+    activations and the total number of expert activations; for one token that is
+    layers x top_k ("Why is it fast when experts keep crossing PCIe?": 48 x 8 = 384).
     """
     h = np.asarray(x, dtype=np.float64)
     n_total = 0
     for ids, w, experts in layers:
-        h, n = moe_layer(h, ids, w, experts)
+        y, n = moe_layer(h, ids, w, experts)
+        h = h + y if residual else y
         n_total += n
     return h, n_total

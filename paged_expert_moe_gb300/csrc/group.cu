@@ -1,0 +1,189 @@
+// Token -> expert grouping: histogram, exclusive scan, stable permutation, the
+// per-wave tile list of the tensor-core path, and the row gather of activations.
+//
+// Article "Running an MoE Model Larger Than Your VRAM", section "What does Paged
+// Experts actually do?": once the routed experts are resident the fused MoE runs
+// over them, i.e. the (token, rank) pairs are grouped by expert. Pair p = t*top_k + r.
+//   counts[e]  pairs routed to e;   offs = exclusive scan of counts (offs[E] = P)
+//   perm[j]    pairs grouped by expert ascending, ascending pair index inside one
+//              expert (stable), so the grouping is deterministic;   pos = perm^-1
+// A pair whose id is outside [0, E) is left out (pos = -1) and flagged.
+#include "pmoe_internal.h"
+
+namespace pmoe {
+namespace {
+
+// Warp w counts (pass 0) or places (pass 1) the pairs of expert w.
+__global__ void __launch_bounds__(256) group_expert_pass(const int32_t* __restrict__ ids, int P, int E, int pass,
+                                                          Workspace ws, int32_t* __restrict__ err) {
+  const int lane = threadIdx.x & 31;
+  const int e = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (e >= E) return;
+  int base = pass ? ws.offs[e] : 0;
+  int n = 0;
+  for (int p0 = 0; p0 < P; p0 += 32) {
+    const int p = p0 + lane;
+    const int id = (p < P) ? ids[p] : -1;
+    const unsigned m = __ballot_sync(0xffffffffu, id == e);
+    if (pass && id == e) {
+      const int j = base + n + __popc(m & ((1u << lane) - 1u));
+      ws.perm[j] = p;
+      ws.pos[p] = j;
+    }
+    if (pass && e == 0 && p < P && (id < 0 || id >= E)) {
+      ws.pos[p] = -1;
+      atomicOr(err, kErrBadExpertId);
+    }
+    n += __popc(m);
+  }
+  if (!pass && lane == 0) ws.counts[e] = n;
+}
+
+// Single CTA: offs = scan(counts); per-wave tiles of at most tile_n pairs.
+__global__ void __launch_bounds__(1024) group_scan_tiles(int E, const int32_t* __restrict__ plan, Workspace ws,
+                                                         int tile_n, int32_t* __restrict__ err) {
+  __shared__ int s_v[kMaxExperts + 1];
+  __shared__ int s_t[kMaxExperts + 1];
+  const int tid = threadIdx.x;
+  const PlanLayout L{E};
+  // offs: inclusive Hillis-Steele scan (E <= 1024, fixed order -> deterministic)
+  s_v[tid] = (tid < E) ? ws.counts[tid] : 0;
+  __syncthreads();
+  for (int off = 1; off < 1024; off <<= 1) {
+    const int add = (tid >= off) ? s_v[tid - off] : 0;
+    __syncthreads();
+    s_v[tid] += add;
+    __syncthreads();
+  }
+  if (tid < E) ws.offs[tid + 1] = s_v[tid];
+  if (tid == 0) ws.offs[0] = 0;
+  if (plan == nullptr || tile_n <= 0) return;
+  // tiles, in the plan's wave order (ascending expert id within a wave)
+  const int n_waves = plan[kPlanWaves];
+  const int n_wexp = plan[L.wave_start() + n_waves];
+  int my_tiles = 0, e = -1, cnt = 0;
+  if (tid < n_wexp) {
+    e = plan[L.wave_exp() + tid];
+    cnt = ws.counts[e];
+    my_tiles = (cnt + tile_n - 1) / tile_n;
+  }
+  s_t[tid] = my_tiles;
+  __syncthreads();
+  for (int off = 1; off < 1024; off <<= 1) {
+    const int add = (tid >= off) ? s_t[tid - off] : 0;
+    __syncthreads();
+    s_t[tid] += add;
+    __syncthreads();
+  }
+  const int first = s_t[tid] - my_tiles;
+  if (tid < n_wexp && my_tiles > 0) {
+    const int slot = plan[L.wave_slot() + tid];
+    const int e_off = (e == 0) ? 0 : s_v[e - 1];  // offs[e]
+    // even split, chunk rounded up to a multiple of 16 pairs
+    int chunk = (cnt + my_tiles - 1) / my_tiles;
+    chunk = (chunk + 15) & ~15;
+    for (int i = 0; i < my_tiles; ++i) {
+      const int idx = first + i;
+      if (idx >= ws.max_tiles) {
+        atomicOr(err, kErrPlanOverflow);
+        break;
+      }
+      const int start = i * chunk;
+      const int n = (cnt - start < chunk) ? (cnt - start) : chunk;
+      ws.tiles[3 * idx + 0] = slot;
+      ws.tiles[3 * idx + 1] = e_off + start;
+      ws.tiles[3 * idx + 2] = n > 0 ? n : 0;
+    }
+  }
+  __syncthreads();
+  if (tid <= n_waves) {
+    const int j = plan[L.wave_start() + tid];  // first wave-list index of wave tid
+    int t = (j == 0) ? 0 : s_t[j - 1];
+    if (t > ws.max_tiles) t = ws.max_tiles;
+    ws.tile_wave[tid] = t;
+  }
+}
+
+// Single CTA for small P: everything in one launch (decode). Thread e owns expert e.
+__global__ void __launch_bounds__(1024) group_small(const int32_t* __restrict__ ids, int P, int E,
+                                                    const int32_t* __restrict__ plan, Workspace ws,
+                                                    int32_t* __restrict__ err) {
+  __shared__ int s_ids[1024];
+  __shared__ int s_v[kMaxExperts];
+  const int tid = threadIdx.x;
+  for (int p = tid; p < P; p += blockDim.x) {
+    const int id = ids[p];
+    s_ids[p] = id;
+    if (id < 0 || id >= E) {
+      ws.pos[p] = -1;
+      atomicOr(err, kErrBadExpertId);
+    }
+  }
+  __syncthreads();
+  int cnt = 0;
+  if (tid < E)
+    for (int p = 0; p < P; ++p) cnt += (s_ids[p] == tid);
+  s_v[tid] = cnt;
+  __syncthreads();
+  for (int off = 1; off < 1024; off <<= 1) {
+    const int add = (tid >= off) ? s_v[tid - off] : 0;
+    __syncthreads();
+    s_v[tid] += add;
+    __syncthreads();
+  }
+  if (tid < E) {
+    const int base = s_v[tid] - cnt;
+    ws.counts[tid] = cnt;
+    ws.offs[tid] = base;
+    if (tid == E - 1) ws.offs[E] = s_v[tid];
+    int j = base;
+    for (int p = 0; p < P; ++p)
+      if (s_ids[p] == tid) {
+        ws.perm[j] = p;
+        ws.pos[p] = j;
+        ++j;
+      }
+  }
+}
+
+// x_perm[j] = x[perm[j] / top_k]; one warp per row, 16-byte vectors.
+__global__ void __launch_bounds__(256) gather_rows_kernel(const __nv_bfloat16* __restrict__ x,
+                                                          const int32_t* __restrict__ perm, int P, int top_k,
+                                                          int H, __nv_bfloat16* __restrict__ x_perm) {
+  const int lane = threadIdx.x & 31;
+  const int nwarps = gridDim.x * (blockDim.x >> 5);
+  const int nvec = H / 8;
+  for (int j = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); j < P; j += nwarps) {
+    const int t = perm[j] / top_k;
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H);
+    uint4* dst = reinterpret_cast<uint4*>(x_perm + (size_t)j * H);
+    for (int c = lane; c < nvec; c += 32) dst[c] = __ldg(src + c);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_group(const int32_t* ids, int P, int E, const int32_t* plan, Workspace ws, int tile_n,
+                         int32_t* err, cudaStream_t s) {
+  if (P <= 1024 && tile_n <= 0) {
+    group_small<<<1, 1024, 0, s>>>(ids, P, E, plan, ws, err);
+    return cudaGetLastError();
+  }
+  const int wpb = 8;
+  const int blocks = (E + wpb - 1) / wpb;
+  group_expert_pass<<<blocks, wpb * 32, 0, s>>>(ids, P, E, 0, ws, err);
+  group_scan_tiles<<<1, 1024, 0, s>>>(E, plan, ws, tile_n, err);
+  group_expert_pass<<<blocks, wpb * 32, 0, s>>>(ids, P, E, 1, ws, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_rows(const __nv_bfloat16* x, const int32_t* perm, int P, int top_k, int H,
+                               __nv_bfloat16* x_perm, cudaStream_t s) {
+  if (P == 0) return cudaSuccess;
+  int blocks = (P + 7) / 8;
+  if (blocks > 4096) blocks = 4096;
+  gather_rows_kernel<<<blocks, 256, 0, s>>>(x, perm, P, top_k, H, x_perm);
+  return cudaGetLastError();
+}
+
+}  // namespace pmoe

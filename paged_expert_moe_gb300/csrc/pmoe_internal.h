@@ -1,0 +1,87 @@
+// Internal declarations shared by the library's translation units (host + device).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+#include <stddef.h>
+
+#include "../../include/pagedmoe.h"
+
+namespace pmoe {
+
+constexpr int kMaxExperts = 1024;
+constexpr int kMaxTopK = 32;
+constexpr int kGemvMaxTokens = 8;  // decode (weight-streaming) path for T <= this
+
+// Device error word bits.
+enum : int32_t { kErrBadExpertId = 1, kErrPlanOverflow = 2, kErrBadSlot = 4, kErrPullTimeout = 8 };
+
+// Layout of a layer's residency plan (int32 words), written by the residency kernel
+// and mirrored to pinned host memory in copy-engine mode.
+struct PlanLayout {
+  int E;
+  __host__ __device__ int header() const { return 0; }                 // 8 words
+  __host__ __device__ int wave_start() const { return 8; }             // E + 1
+  __host__ __device__ int wave_exp() const { return 8 + (E + 1); }     // E
+  __host__ __device__ int wave_slot() const { return 8 + 2 * E + 1; }  // E
+  __host__ __device__ int miss_start() const { return 8 + 3 * E + 1; } // E + 1
+  __host__ __device__ int miss_exp() const { return 8 + 4 * E + 2; }   // E
+  __host__ __device__ int miss_slot() const { return 8 + 5 * E + 2; }  // E
+  __host__ __device__ int wave_of() const { return 8 + 6 * E + 2; }    // E
+  __host__ __device__ int words() const { return 8 + 7 * E + 2; }
+};
+// header words
+enum { kPlanUnique = 0, kPlanWaves = 1, kPlanMisses = 2, kPlanError = 3, kPlanStep = 4 };
+
+// One layer's device LRU state.
+struct LayerState {
+  int32_t* slot_of;     // [E]  slot holding expert e, -1 if absent
+  int32_t* expert_in;   // [K]  expert in slot s, -1 if empty
+  int32_t* last_use;    // [K]  step of last use, -1 if never
+  int32_t* step;        // [1]  the layer's step counter
+  unsigned long long* counters;  // [4] hits, misses, waves, steps
+};
+
+// Forward workspace (device), shared by all layers of a cache.
+struct Workspace {
+  int32_t* counts;      // [E]
+  int32_t* offs;        // [E + 1]
+  int32_t* perm;        // [P]  grouped position -> pair
+  int32_t* pos;         // [P]  pair -> grouped position
+  int32_t* tiles;       // [3 * max_tiles] (slot, pair start, pair count) per tile, grouped by wave
+  int32_t* tile_wave;   // [E + 2] tile range of each wave
+  __nv_bfloat16* h;     // [P][I] intermediate activations, grouped order
+  float* o_part;        // [P][H] per-pair down-projection outputs, grouped order
+  __nv_bfloat16* x_perm;  // [P][H] tokens gathered in grouped order (tensor-core path)
+  int max_tiles;
+};
+
+// Kernel launchers (each returns cudaError_t of the launch).
+cudaError_t launch_router_topk(const float* logits, int T, int E, int top_k, int renorm,
+                               int32_t* ids, float* w, cudaStream_t s);
+cudaError_t launch_residency(const int32_t* ids, int n_ids, int E, int K, LayerState st,
+                             int32_t* plan, int32_t* err, cudaStream_t s);
+cudaError_t launch_group(const int32_t* ids, int P, int E, const int32_t* plan, Workspace ws,
+                         int tile_n, int32_t* err, cudaStream_t s);
+cudaError_t launch_gather_rows(const __nv_bfloat16* x, const int32_t* perm, int P, int top_k, int H,
+                               __nv_bfloat16* x_perm, cudaStream_t s);
+cudaError_t launch_gemv_gateup(int fmt, const __nv_bfloat16* x, int T, int top_k, int H, int I,
+                               const int32_t* plan, int E, int wave, const Workspace& ws,
+                               const uint8_t* arena, size_t stride, int num_sms, cudaStream_t s);
+cudaError_t launch_gemv_down(int fmt, int H, int I, const int32_t* plan, int E, int wave,
+                             const Workspace& ws, const uint8_t* arena, size_t stride, int num_sms,
+                             cudaStream_t s);
+cudaError_t launch_combine(const Workspace& ws, const float* w, const __nv_bfloat16* residual,
+                           __nv_bfloat16* y, int T, int top_k, int H, cudaStream_t s);
+cudaError_t launch_pull_pages(const int32_t* plan, int E, int wave, const uint8_t* host_store_dev,
+                              size_t stride, size_t expert_bytes, uint8_t* arena, int32_t* err,
+                              cudaStream_t s);
+
+// Expert section offsets within an expert's bytes.
+struct ExpertLayout {
+  size_t gu_w, d_w, gu_s, d_s, bytes;
+};
+ExpertLayout expert_layout(int fmt, int H, int I);
+
+}  // namespace pmoe

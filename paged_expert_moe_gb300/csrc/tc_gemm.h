@@ -1,0 +1,27 @@
+// Tensor-core (tcgen05 / TMEM / TMA) grouped GEMMs of the prefill path.
+#pragma once
+
+#include <cuda.h>
+
+#include "pmoe_internal.h"
+
+namespace pmoe {
+
+constexpr int kTcMaxN = 256;  // pairs per tile (MMA N)
+
+struct TcMaps {
+  CUtensorMap gu;  // gate/up rows of every slot: dims {H, 2I, K} bf16
+  CUtensorMap d;   // down rows of every slot: dims {I, H, K} bf16
+  CUtensorMap x;   // gathered activations x_perm: dims {H, P} bf16
+  CUtensorMap h;   // intermediate h: dims {I, P} bf16
+};
+
+bool tc_supported(int H, int I);
+int tc_make_weight_maps(uint8_t* arena, size_t stride, int K, int H, int I, TcMaps* out);
+int tc_make_act_maps(__nv_bfloat16* x_perm, __nv_bfloat16* h, size_t P, int H, int I, TcMaps* out);
+cudaError_t tc_gateup(const TcMaps& wm, const TcMaps& am, const int32_t* plan, int E, int wave, const Workspace& ws,
+                      int I, int num_sms, cudaStream_t s);
+cudaError_t tc_down(const TcMaps& wm, const TcMaps& am, const int32_t* plan, int E, int wave, const Workspace& ws,
+                    int H, int I, int num_sms, cudaStream_t s);
+
+}  // namespace pmoe

@@ -23,8 +23,8 @@ GAP = 1e-3
 def bf16_bits(a):
     """float32 array -> bf16 bit patterns (uint16), round to nearest even."""
     a = np.ascontiguousarray(a, dtype=np.float32)
-    u = a.view(np.uint32).astype(np.uint64)
-    rounded = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    u = a.view(np.uint32)
+    rounded = (u + np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1))) >> np.uint32(16)
     return rounded.astype(np.uint16)
 
 
@@ -185,13 +185,25 @@ def fast_int4_expert_bytes(H, I, seed, layer=0, expert=0):
     return out
 
 
-def layer_store(fmt, H, I, E, seed, layer=0, fast=False):
-    """All E experts of one layer, [E, expert_nbytes] uint8."""
+def layer_store(fmt, H, I, E, seed, layer=0, fast=False, threads=None):
+    """All E experts of one layer, [E, expert_nbytes] uint8 (experts drawn in parallel
+    threads; each expert's bytes depend only on its own seed)."""
+    import concurrent.futures
+    import os
     nb = expert_nbytes(fmt, H, I)
     out = np.empty((E, nb), dtype=np.uint8)
-    for e in range(E):
+
+    def fill(e):
         if fast and fmt == 2:
             out[e] = fast_int4_expert_bytes(H, I, seed, layer, e)
         else:
             out[e] = expert_bytes(fmt, H, I, seed, layer, e)
+
+    n = threads or min(16, len(os.sched_getaffinity(0)))
+    if E * nb < (8 << 20) or n <= 1:
+        for e in range(E):
+            fill(e)
+    else:
+        with concurrent.futures.ThreadPoolExecutor(max_workers=n) as ex:
+            list(ex.map(fill, range(E)))
     return out
