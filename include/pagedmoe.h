@@ -250,6 +250,32 @@ PMOE_API int expert_cache_set_timing(pmoe_cache* cache, int enable);
  * Synchronises the cache's streams. */
 PMOE_API int expert_cache_kernel_times(pmoe_cache* cache, pmoe_kernel_times* out);
 
+/*
+ * moe_decode_forward_noalloc — the decode MoE (T <= 8 tokens) over experts that are
+ * already in device memory, using no device allocation of any kind. The paper has
+ * no counterpart of this call; it exists for callers that cannot call cudaMalloc:
+ * code running inside another framework's memory pool or allocator hooks, real-time
+ * loops that must never enter the driver's allocator, and embedders whose device
+ * memory is budgeted up front. It computes what moe_paged_forward computes for the
+ * same tokens when every routed expert is resident, with the same kernels.
+ *   experts   device: expert slots of pmoe_expert_bytes(format, H, I) bytes each,
+ *             `stride` bytes apart (stride a multiple of 16)
+ *   slot_of   device int32 [E]: slot of each expert in `experts`, or NULL when
+ *             expert e sits in slot e; an expert with slot -1 contributes nothing
+ *   x, residual, y, ids, w: as in moe_paged_forward (residual may be NULL)
+ * Limits: E <= 1024, T <= 8, T * top_k <= 64, and the intermediates must fit the
+ * library's fixed 2 MiB static device scratch ((P*(2I + 4H)) bytes plus small
+ * tables, P = T * top_k); larger requests return PMOE_EINVAL with nothing enqueued.
+ * The first call on each device (with that device current) looks up the scratch
+ * address once; make it before any stream capture. All calls share the one scratch
+ * array: calls that overlap on the GPU race on it, so serialise them (one stream).
+ * Invalid expert ids are skipped on the device. Nothing is synchronised.
+ */
+PMOE_API int moe_decode_forward_noalloc(const void* experts, size_t stride, const int32_t* slot_of, int E,
+                                        int top_k, int H, int I, int format, const void* x, int T,
+                                        const int32_t* ids, const float* w, const void* residual, void* y,
+                                        void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -67,6 +67,7 @@ _SIGS = {
     "expert_cache_read_slot": ([_P, _I, _I, _P, ctypes.c_size_t], _I),
     "expert_cache_set_timing": ([_P, _I], _I),
     "expert_cache_kernel_times": ([_P, ctypes.POINTER(pmoe_kernel_times)], _I),
+    "moe_decode_forward_noalloc": ([_P, ctypes.c_size_t, _P, _I, _I, _I, _I, _I, _P, _I, _P, _P, _P, _P, _P], _I),
 }
 EXPORTED = tuple(_SIGS)
 
@@ -122,6 +123,20 @@ def moe_router_topk(logits, top_k, renormalize=True, ids_out=None, w_out=None, s
     _check(lib.moe_router_topk(_ptr(logits), T, E, top_k, 1 if renormalize else 0, _ptr(ids_out), _ptr(w_out),
                                _stream_handle(stream)), "moe_router_topk")
     return ids_out, w_out
+
+
+def moe_decode_forward_noalloc(experts, stride, E, top_k, H, I, fmt, x, ids, w, y=None, slot_of=None,
+                               residual=None, stream=None):
+    """Decode MoE over experts already in device memory; allocates no device memory
+    (the library uses a fixed static scratch). experts: CUDA uint8 tensor holding the
+    expert slots `stride` bytes apart; x: bf16 [T, H]; returns y."""
+    import torch
+    if y is None:
+        y = torch.empty_like(x)
+    _check(load().moe_decode_forward_noalloc(_ptr(experts), stride, _ptr(slot_of), E, top_k, H, I, fmt, _ptr(x),
+                                             x.shape[0], _ptr(ids), _ptr(w), _ptr(residual), _ptr(y),
+                                             _stream_handle(stream)), "moe_decode_forward_noalloc")
+    return y
 
 
 class ExpertCache:
