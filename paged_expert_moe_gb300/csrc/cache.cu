@@ -593,10 +593,10 @@ int moe_paged_forward(pmoe_cache* c, int layer, const void* x, int T, const int3
     if (tc) {
       {
         KernelMark km(c, PMOE_K_GATEUP, s);
-        PMOE_CUDA(tc_gateup(c->maps[layer], c->ws_maps, c->plan_dev[layer], E, wv, c->ws, I, c->num_sms, s));
+        PMOE_CUDA(tc_gateup(c->maps[layer], c->ws_maps, c->plan_dev[layer], E, wv, c->ws, I, H, c->num_sms, c->err_dev, s));
       }
       KernelMark km(c, PMOE_K_DOWN, s);
-      PMOE_CUDA(tc_down(c->maps[layer], c->ws_maps, c->plan_dev[layer], E, wv, c->ws, H, I, c->num_sms, s));
+      PMOE_CUDA(tc_down(c->maps[layer], c->ws_maps, c->plan_dev[layer], E, wv, c->ws, I, H, c->num_sms, c->err_dev, s));
     } else {
       {
         KernelMark km(c, PMOE_K_GATEUP, s);

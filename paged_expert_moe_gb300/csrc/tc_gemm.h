@@ -20,8 +20,8 @@ bool tc_supported(int H, int I);
 int tc_make_weight_maps(uint8_t* arena, size_t stride, int K, int H, int I, TcMaps* out);
 int tc_make_act_maps(__nv_bfloat16* x_perm, __nv_bfloat16* h, size_t P, int H, int I, TcMaps* out);
 cudaError_t tc_gateup(const TcMaps& wm, const TcMaps& am, const int32_t* plan, int E, int wave, const Workspace& ws,
-                      int I, int num_sms, cudaStream_t s);
+                      int I, int H, int num_sms, int32_t* err, cudaStream_t s);
 cudaError_t tc_down(const TcMaps& wm, const TcMaps& am, const int32_t* plan, int E, int wave, const Workspace& ws,
-                    int H, int I, int num_sms, cudaStream_t s);
+                    int I, int H, int num_sms, int32_t* err, cudaStream_t s);
 
 }  // namespace pmoe
