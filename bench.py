@@ -162,9 +162,9 @@ def aggregate(units_per_rank, time_s_per_rank):
 
 # --------------------------------------------------------------------------- our arm
 
-def run_decode(pm, torch, store, B, steps, warmup, device, timed_clock=None, e2e=True):
+def run_decode(pm, torch, store, B, steps, warmup, device, timed_clock=None, e2e=True, mode=0):
     trace, xs, logits, distinct = make_inputs(B)
-    cache = pm.ExpertCache(E, TOPK, H, I, K_SLOTS, fmt=pm.PMOE_BF16, max_tokens=B, device=device)
+    cache = pm.ExpertCache(E, TOPK, H, I, K_SLOTS, fmt=pm.PMOE_BF16, max_tokens=B, device=device, pagein_mode=mode)
     cache.load_layer(0, store)
     dev = torch.device("cuda", device)
     x_dev = [torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(dev) for x in xs]
@@ -211,7 +211,8 @@ def run_decode(pm, torch, store, B, steps, warmup, device, timed_clock=None, e2e
         "bytes_paged_per_step": (stats1["bytes_paged"] - stats0["bytes_paged"]) / steps,
         "gateup_weight_bytes": sum(d * 2 * I * H * 2 for d in d_steps),
         "down_weight_bytes": sum(d * H * I * 2 for d in d_steps),
-        "launches": sum(v["launches"] for k_, v in kt.items() if k_ != "copies") + steps,  # + router
+        "expert_weight_bytes": sum(d * 3 * I * H * 2 for d in d_steps),
+        "launches": sum(v["launches"] for k_, v in kt.items() if k_ not in ("copies", "pagein_copy")) + steps,
     }
     cache.expert_cache_set_timing(False)
     if e2e:
@@ -237,6 +238,85 @@ def run_decode(pm, torch, store, B, steps, warmup, device, timed_clock=None, e2e
                       "h2d_bytes_per_step": B * H * 2 + B * E * 4, "d2h_bytes_per_step": B * H * 2}
     cache.close()
     return res
+
+
+def measure_h2d(torch, dev, nbytes=9_437_184, reps=40):
+    """Pinned host -> device copy bandwidth (cudaMemcpyAsync via torch), GB/s."""
+    src = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    dst = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    for _ in range(3):
+        dst.copy_(src, non_blocking=True)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        dst.copy_(src, non_blocking=True)
+    b.record()
+    torch.cuda.synchronize(dev)
+    return nbytes * reps / (a.elapsed_time(b) / 1e3) / 1e9
+
+
+PREFILL_T, PREFILL_K = 2048, 92
+
+
+def run_prefill(pm, torch, store, steps, warmup, device, K=PREFILL_K, cold=True, n_inputs=3, mode=0):
+    """Config: 2048-token prefill, uniform routing; cold = the table is emptied before every step."""
+    dev = torch.device("cuda", device)
+    rng = np.random.default_rng([SEED, 2048])
+    inputs = []
+    for _ in range(n_inputs):
+        sets = gen.uniform_routing_sets(rng, PREFILL_T, E, TOPK)
+        inputs.append((torch.from_numpy(gen.activations_bf16(rng, PREFILL_T, H).view(np.int16)).view(torch.bfloat16).to(dev),
+                       torch.from_numpy(gen.logits_for_sets(rng, sets, E)).to(dev)))
+    cache = pm.ExpertCache(E, TOPK, H, I, K, fmt=pm.PMOE_BF16, max_tokens=PREFILL_T, device=device, pagein_mode=mode)
+    cache.load_layer(0, store)
+    ids = torch.empty((PREFILL_T, TOPK), dtype=torch.int32, device=dev)
+    w = torch.empty((PREFILL_T, TOPK), dtype=torch.float32, device=dev)
+    y = torch.empty((PREFILL_T, H), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def one(i):
+        x_d, l_d = inputs[i % n_inputs]
+        pm.moe_router_topk(l_d, TOPK, ids_out=ids, w_out=w)
+        cache.moe_paged_forward(0, x_d, ids, w, y=y)
+
+    for i in range(warmup):
+        if cold:
+            cache.expert_cache_reset(0)
+        one(i)
+    torch.cuda.synchronize(dev)
+    s0 = cache.expert_cache_stats(0)
+    cache.expert_cache_set_timing(True)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for i in range(steps):
+        if cold:
+            cache.expert_cache_reset(0)
+        flush.zero_()
+        evs[i][0].record(stream)
+        one(warmup + i)
+        evs[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    total_ms = float(sum(a.elapsed_time(b) for a, b in evs))
+    kt = cache.expert_cache_kernel_times()
+    s1 = cache.expert_cache_stats(0)
+    cache.close()
+    P = PREFILL_T * TOPK
+    flops_gu = 2.0 * P * 2 * I * H * steps
+    flops_d = 2.0 * P * H * I * steps
+    return {"ms_per_step": total_ms / steps, "tokens_per_s": PREFILL_T * steps / (total_ms / 1e3),
+            "misses_per_step": (s1["misses"] - s0["misses"]) / steps,
+            "waves_per_step": (s1["waves"] - s0["waves"]) / steps,
+            "bytes_paged_per_step": (s1["bytes_paged"] - s0["bytes_paged"]) / steps,
+            "kernel_ms_per_step": {k_: v["ms"] / steps for k_, v in kt.items() if k_ != "copies"},
+            "gateup_tflops": flops_gu / (kt["gateup"]["ms"] / 1e3) / 1e12,
+            "down_tflops": flops_d / (kt["down"]["ms"] / 1e3) / 1e12,
+            "gemm_tflops": (flops_gu + flops_d) / ((kt["gateup"]["ms"] + kt["down"]["ms"]) / 1e3) / 1e12,
+            "gemm_ms_per_step": (kt["gateup"]["ms"] + kt["down"]["ms"]) / steps,
+            "pagein_gbs": ((s1["bytes_paged"] - s0["bytes_paged"]) /
+                           ((kt["pagein_copy"]["ms"] + kt["pull"]["ms"]) / 1e3) / 1e9
+                           if kt["pagein_copy"]["ms"] + kt["pull"]["ms"] > 0 else None),
+            "launches_per_step": sum(v["launches"] for k_, v in kt.items()
+                                     if k_ not in ("copies", "pagein_copy")) / steps + 1}
 
 
 def cpu_baseline_decode(B=1, budget_s=15.0, max_steps=400, store=None):
@@ -280,24 +360,29 @@ def run_ours(args):
     barrier(ws)
     clocks = clock.stop(*head["t_wall"]) if clock else None
     others = {}
+    prefill = {}
+    h2d = measure_h2d(torch, torch.device("cuda", local))
     if not args.headline_only:
         for B in (2, 4):
             others[B] = run_decode(pm, torch, store, B, args.steps, args.warmup, local, e2e=False)
+        others["B1_sm_pull"] = run_decode(pm, torch, store, 1, args.steps, args.warmup, local, e2e=False, mode=1)
+        prefill["cold"] = run_prefill(pm, torch, store, args.prefill_steps, 2, local, cold=True)
+        prefill["cold_sm_pull"] = run_prefill(pm, torch, store, args.prefill_steps, 2, local, cold=True, mode=1)
+        prefill["warm_all_resident"] = run_prefill(pm, torch, store, args.prefill_steps, 2, local, K=E, cold=False)
     job_ms = reduce_max(head["total_ms"], ws, torch.device("cuda", local))
     value = ws * 1 * args.steps / (job_ms / 1e3)
     if rank != 0:
         return
     kt = head["kernel_times"]
-    gu_ms = kt["gateup"]["ms"]
-    gu_launch = max(1, kt["gateup"]["launches"])
-    achieved = head["gateup_weight_bytes"] / (gu_ms / 1e3) / 1e9
-    layer_ms = gu_ms + kt["down"]["ms"]
-    layer_gbs = (head["gateup_weight_bytes"] + head["down_weight_bytes"]) / (layer_ms / 1e3) / 1e9
+    dec_ms = kt["decode"]["ms"]
+    dec_launch = max(1, kt["decode"]["launches"])
+    achieved = head["expert_weight_bytes"] / (dec_ms / 1e3) / 1e9
+    layer_gbs = achieved
     traffic = None
     tp = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(tp):
         try:
-            traffic = json.load(open(tp)).get("decode_gateup_bf16_B1")
+            traffic = json.load(open(tp)).get("decode_fused_bf16_B1")
         except Exception:
             traffic = None
     out = {
@@ -312,21 +397,29 @@ def run_ours(args):
                    "parallelism": f"replicas x{ws}"},
         "expert_weight_hbm_gbs": layer_gbs,
         "expert_weight_hbm_frac": layer_gbs / hbm_peak,
-        "roofline": {"kernel": "gemv_gateup (decode gate/up + SiLU*mul)", "bound": "hbm", "achieved": achieved,
+        "roofline": {"kernel": "decode_fused_kernel (gate/up + SiLU*mul + down + combine, one launch per wave)",
+                     "bound": "hbm", "achieved": achieved,
                      "peak": hbm_peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / hbm_peak,
                      "traffic": traffic,
-                     "avg_launch_us": gu_ms / gu_launch * 1e3,
-                     "algorithmic_bytes_per_launch": head["gateup_weight_bytes"] / gu_launch},
+                     "avg_launch_us": dec_ms / dec_launch * 1e3,
+                     "algorithmic_bytes_per_launch": head["expert_weight_bytes"] / dec_launch,
+                     "algorithmic_bytes_note": "distinct routed experts x 3*H*I*2 bytes (gate, up, down weights)"},
         "layer": {"misses_per_step": head["misses_per_step"], "hit_rate": head["hit_rate"],
                   "waves_per_step": head["waves_per_step"], "distinct_experts_per_step": head["distinct_per_step"],
                   "bytes_paged_per_step": head["bytes_paged_per_step"],
                   "kernel_ms_per_step": {k_: v["ms"] / args.steps for k_, v in kt.items() if k_ != "copies"},
                   "copies_per_step": kt["copies"] / args.steps},
-        "batches": {f"B{B}": {"tokens_per_s": r["tokens_per_s"], "ms_per_step": r["ms_per_step"],
+        "batches": {(f"B{B}" if isinstance(B, int) else B): {"tokens_per_s": r["tokens_per_s"], "ms_per_step": r["ms_per_step"],
                               "misses_per_step": r["misses_per_step"], "waves_per_step": r["waves_per_step"],
-                              "gateup_gbs": r["gateup_weight_bytes"] / (r["kernel_times"]["gateup"]["ms"] / 1e3) / 1e9,
-                              "down_gbs": r["down_weight_bytes"] / (r["kernel_times"]["down"]["ms"] / 1e3) / 1e9}
+                              "decode_kernel_gbs": r["expert_weight_bytes"] /
+                              (r["kernel_times"]["decode"]["ms"] / 1e3) / 1e9 if r["kernel_times"]["decode"]["ms"] else None,
+                              "kernel_ms_per_step": {k_: v["ms"] / r["steps"] for k_, v in r["kernel_times"].items()
+                                                     if k_ != "copies" and v["ms"]}}
                     for B, r in others.items()},
+        "host_link": {"pinned_h2d_gbs": h2d, "chunk_bytes": 9_437_184,
+                      "decode_pagein_gbs": (head["bytes_paged_per_step"] * args.steps /
+                                            (kt["pagein_copy"]["ms"] / 1e3) / 1e9) if kt["pagein_copy"]["ms"] else None},
+        "prefill": _prefill_summary(prefill, hbm_peak, _peaks()[1]) if prefill else None,
         "e2e": head.get("e2e"),
         "gpu_launches": head["launches"],
         "clocks": clocks,
@@ -335,6 +428,20 @@ def run_ours(args):
     if not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline_decode(1, budget_s=args.cpu_budget, store=store)
     print(json.dumps(out))
+
+
+def _prefill_summary(prefill, hbm_peak, tc_peak):
+    out = {"workload": f"Qwen3-30B-A3B-shaped MoE layer, bf16, prefill {PREFILL_T} tokens, uniform routing",
+           "FLOP_per_step": 2.0 * PREFILL_T * TOPK * 3 * H * I, "weight_bytes_per_step": E * 3 * H * I * 2}
+    for name, r in prefill.items():
+        d = dict(r)
+        d["tensor_frac"] = r["gemm_tflops"] / tc_peak
+        d["weight_stream_frac"] = (E * 3 * H * I * 2) / (r["gemm_ms_per_step"] / 1e3) / 1e9 / hbm_peak
+        out[name] = d
+    out["tensor_peak_tflops"] = tc_peak
+    out["roofline_note"] = ("AI = 128 FLOP/B for this layer, below the bf16 ridge, so the GEMMs are bounded by "
+                            "min(tensor peak, AI x HBM); both fractions are reported")
+    return out
 
 
 # --------------------------------------------------------------------------- reference arm (the oracle)
@@ -395,6 +502,7 @@ def main():
     ap.add_argument("--headline-only", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--prefill-steps", type=int, default=6)
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

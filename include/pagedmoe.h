@@ -120,7 +120,9 @@ enum {
   PMOE_K_DOWN = 4,       /* down projection                                      */
   PMOE_K_COMBINE = 5,    /* top_k-weighted combine                               */
   PMOE_K_PULL = 6,       /* SM-pull page-in (copy stream)                        */
-  PMOE_K_CLASSES = 8
+  PMOE_K_COPY = 7,       /* copy-engine page-in: first to last copy of a wave    */
+  PMOE_K_DECODE = 8,     /* fused decode kernel: gate/up, SiLU*mul, down (+combine) */
+  PMOE_K_CLASSES = 12
 };
 
 typedef struct {

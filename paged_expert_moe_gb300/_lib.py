@@ -40,10 +40,10 @@ class pmoe_stats(ctypes.Structure):
 
 
 class pmoe_kernel_times(ctypes.Structure):
-    _fields_ = [("ms", ctypes.c_double * 8), ("launches", ctypes.c_uint64 * 8), ("copies", ctypes.c_uint64)]
+    _fields_ = [("ms", ctypes.c_double * 12), ("launches", ctypes.c_uint64 * 12), ("copies", ctypes.c_uint64)]
 
 
-KERNEL_CLASSES = ("residency", "group", "gather", "gateup", "down", "combine", "pull", "spare")
+KERNEL_CLASSES = ("residency", "group", "gather", "gateup", "down", "combine", "pull", "pagein_copy", "decode")
 
 _LIB = None
 
@@ -229,5 +229,5 @@ class ExpertCache:
     def expert_cache_kernel_times(self):
         kt = pmoe_kernel_times()
         _check(load().expert_cache_kernel_times(self.handle, ctypes.byref(kt)), "expert_cache_kernel_times")
-        return {name: {"ms": kt.ms[i], "launches": int(kt.launches[i])} for i, name in enumerate(KERNEL_CLASSES)
-                if name != "spare"} | {"copies": int(kt.copies)}
+        return {name: {"ms": kt.ms[i], "launches": int(kt.launches[i])} for i, name in enumerate(KERNEL_CLASSES)} | \
+            {"copies": int(kt.copies)}

@@ -217,6 +217,8 @@ int issue_copies(pmoe_cache* c, int layer, int wave) {
     snprintf(g_last_error, sizeof(g_last_error), "injected page-in copy failure");
     return PMOE_ECUDA;
   }
+  if (m1 == m0) return PMOE_OK;
+  KernelMark km(c, PMOE_K_COPY, c->copy_stream);
   for (int m = m0; m < m1; ++m) {
     const int e = plan[L.miss_exp() + m], s = plan[L.miss_slot() + m];
     PMOE_CUDA(cudaMemcpyAsync(c->arena[layer] + (size_t)s * c->stride, c->host_store[layer] + (size_t)e * c->stride,
@@ -414,8 +416,13 @@ int expert_cache_create(const pmoe_cache_desc* desc, pmoe_cache** out) {
     };
     const size_t o_counts = carve(4 * (size_t)E), o_offs = carve(4 * (size_t)(E + 1)), o_perm = carve(4 * P),
                  o_pos = carve(4 * P), o_tiles = carve(12 * (size_t)c->ws.max_tiles),
-                 o_tw = carve(4 * (size_t)(E + 2)), o_h = carve(2 * P * d.intermediate),
+                 o_tw = carve(4 * (size_t)(E + 2)), o_ts = carve(4 * (size_t)(E + 2)),
+                 o_h = carve(2 * P * d.intermediate),
                  o_o = carve(4 * P * d.hidden), o_x = c->use_tc ? carve(2 * P * d.hidden) : 0;
+    const size_t chunk_cap = ((P + 255) / 256) * (size_t)E;
+    const size_t o_ch = carve(4 * chunk_cap);
+    const size_t o_gb = carve(8);
+    const size_t o_dn = carve(4 * (size_t)E);
     const cudaError_t e = cudaMalloc(&c->ws_buf, off);
     if (e != cudaSuccess) {
       set_cuda_error(e, "cudaMalloc (workspace)");
@@ -430,9 +437,16 @@ int expert_cache_create(const pmoe_cache_desc* desc, pmoe_cache** out) {
     c->ws.pos = (int32_t*)(b + o_pos);
     c->ws.tiles = (int32_t*)(b + o_tiles);
     c->ws.tile_wave = (int32_t*)(b + o_tw);
+    c->ws.tile_split = (int32_t*)(b + o_ts);
     c->ws.h = (__nv_bfloat16*)(b + o_h);
     c->ws.o_part = (float*)(b + o_o);
     c->ws.x_perm = c->use_tc ? (__nv_bfloat16*)(b + o_x) : nullptr;
+    c->ws.chunk_cnt = (int32_t*)(b + o_ch);
+    c->ws.chunk_cap = (int)chunk_cap;
+    c->ws.gbar = (unsigned*)(b + o_gb);
+    PMOE_TRY(cudaMemset(c->ws.gbar, 0, 8));
+    c->ws.done = (unsigned*)(b + o_dn);
+    PMOE_TRY(cudaMemset(c->ws.done, 0, 4 * (size_t)E));
   }
   if (c->use_tc) {
     c->maps.resize(Lr);
@@ -566,8 +580,54 @@ int moe_paged_forward(pmoe_cache* c, int layer, const void* x, int T, const int3
   c->staged[layer] = 0;
   const int nw = c->staged_waves[layer];
   const bool tc = c->use_tc && T > kGemvMaxTokens;
-  PMOE_CUDA(cudaStreamWaitEvent(s, c->ev_ready[layer], 0));
-  {
+  const bool fused = !tc && decode_fused_supported(c->d.format, T, k, H, I, c->num_sms);
+  const bool ce = c->d.pagein_mode == PMOE_PAGEIN_COPY_ENGINE;
+  // Copy-engine steps whose first wave has both resident and paged-in experts compute
+  // the resident ones while the copies are still in flight (the plan lists them first).
+  bool split0 = false;
+  if (ce && (tc || fused) && nw > 0) {
+    const int32_t* plan = c->plan_h(layer);
+    const PlanLayout L{E};
+    const int hits0 = plan[L.wave_hits() + 0];
+    const int size0 = plan[L.wave_start() + 1] - plan[L.wave_start() + 0];
+    split0 = hits0 > 0 && hits0 < size0;
+  }
+  // the fused decode kernel forms y itself when the step has a single unsplit wave
+  const int fuse_combine = fused ? (ce ? ((nw == 1 && !split0) ? 1 : 0) : 1) : 0;
+  const bool need_combine = !fused || nw > 1 || split0;
+
+  auto compute = [&](int wv, int sub) -> int {
+    if (tc) {
+      {
+        KernelMark km(c, PMOE_K_GATEUP, s);
+        PMOE_CUDA(tc_gateup(c->maps[layer], c->ws_maps, c->plan_dev[layer], E, wv, sub, c->ws, I, H, c->num_sms,
+                            c->err_dev, s));
+      }
+      KernelMark km(c, PMOE_K_DOWN, s);
+      PMOE_CUDA(tc_down(c->maps[layer], c->ws_maps, c->plan_dev[layer], E, wv, sub, c->ws, I, H, c->num_sms,
+                        c->err_dev, s));
+    } else if (fused) {
+      KernelMark km(c, PMOE_K_DECODE, s);
+      PMOE_CUDA(launch_decode_fused(c->d.format, (const __nv_bfloat16*)x, ids, w, (const __nv_bfloat16*)residual,
+                                    (__nv_bfloat16*)y, T, k, H, I, c->plan_dev[layer], E, wv, sub, fuse_combine,
+                                    c->ws, c->arena[layer], c->stride, c->err_dev, c->num_sms, s));
+    } else {
+      {
+        KernelMark km(c, PMOE_K_GATEUP, s);
+        PMOE_CUDA(launch_gemv_gateup(c->d.format, (const __nv_bfloat16*)x, T, k, H, I, c->plan_dev[layer], E, wv,
+                                     c->ws, c->arena[layer], c->stride, c->num_sms, s));
+      }
+      KernelMark km(c, PMOE_K_DOWN, s);
+      PMOE_CUDA(launch_gemv_down(c->d.format, H, I, c->plan_dev[layer], E, wv, c->ws, c->arena[layer], c->stride,
+                                 c->num_sms, s));
+    }
+    return PMOE_OK;
+  };
+
+  // grouping needs only the ids and the plan; in copy-engine mode the plan is ready
+  // once the host has read it, before the copies land
+  PMOE_CUDA(cudaStreamWaitEvent(s, split0 ? c->ev_plan[layer] : c->ev_ready[layer], 0));
+  if (!fused) {  // the fused decode kernel groups the pairs itself
     KernelMark km(c, PMOE_K_GROUP, s);
     PMOE_CUDA(launch_group(ids, P, E, c->plan_dev[layer], c->ws, tc ? kTcMaxN : 0, c->err_dev, s));
   }
@@ -579,7 +639,7 @@ int moe_paged_forward(pmoe_cache* c, int layer, const void* x, int T, const int3
     if (wv > 0) {
       PMOE_CUDA(cudaEventRecord(c->ev_wave_done, s));
       PMOE_CUDA(cudaStreamWaitEvent(c->copy_stream, c->ev_wave_done, 0));
-      if (c->d.pagein_mode == PMOE_PAGEIN_COPY_ENGINE) {
+      if (ce) {
         const int r = issue_copies(c, layer, wv);
         if (r != PMOE_OK) return r;
       } else {
@@ -590,27 +650,23 @@ int moe_paged_forward(pmoe_cache* c, int layer, const void* x, int T, const int3
       PMOE_CUDA(cudaEventRecord(c->ev_ready[layer], c->copy_stream));
       PMOE_CUDA(cudaStreamWaitEvent(s, c->ev_ready[layer], 0));
     }
-    if (tc) {
-      {
-        KernelMark km(c, PMOE_K_GATEUP, s);
-        PMOE_CUDA(tc_gateup(c->maps[layer], c->ws_maps, c->plan_dev[layer], E, wv, c->ws, I, H, c->num_sms, c->err_dev, s));
-      }
-      KernelMark km(c, PMOE_K_DOWN, s);
-      PMOE_CUDA(tc_down(c->maps[layer], c->ws_maps, c->plan_dev[layer], E, wv, c->ws, I, H, c->num_sms, c->err_dev, s));
+    if (wv == 0 && split0) {
+      int r = compute(0, 1);  // resident experts, overlapping the page-in
+      if (r != PMOE_OK) return r;
+      PMOE_CUDA(cudaStreamWaitEvent(s, c->ev_ready[layer], 0));
+      r = compute(0, 2);  // the experts just paged in
+      if (r != PMOE_OK) return r;
     } else {
-      {
-        KernelMark km(c, PMOE_K_GATEUP, s);
-        PMOE_CUDA(launch_gemv_gateup(c->d.format, (const __nv_bfloat16*)x, T, k, H, I, c->plan_dev[layer], E, wv,
-                                     c->ws, c->arena[layer], c->stride, c->num_sms, s));
-      }
-      KernelMark km(c, PMOE_K_DOWN, s);
-      PMOE_CUDA(launch_gemv_down(c->d.format, H, I, c->plan_dev[layer], E, wv, c->ws, c->arena[layer], c->stride,
-                                 c->num_sms, s));
+      const int r = compute(wv, 0);
+      if (r != PMOE_OK) return r;
     }
   }
-  {
+  if (need_combine) {
+    // SM-pull steps that may have several waves: the combine skips itself if the step
+    // turned out to have one wave (the fused kernel then already wrote y)
     KernelMark km(c, PMOE_K_COMBINE, s);
-    PMOE_CUDA(launch_combine(c->ws, w, (const __nv_bfloat16*)residual, (__nv_bfloat16*)y, T, k, H, s));
+    PMOE_CUDA(launch_combine(c->ws, w, (const __nv_bfloat16*)residual, (__nv_bfloat16*)y, T, k, H, s,
+                             (fused && !ce) ? c->plan_dev[layer] : nullptr));
   }
   PMOE_CUDA(cudaEventRecord(c->ev_layer_done[layer], s));
   return status;

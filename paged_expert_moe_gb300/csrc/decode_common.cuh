@@ -1,0 +1,118 @@
+// Device helpers shared by the decode kernels: streaming loads, bf16 unpacking, the
+// per-format dequantisation of one 16-byte weight chunk (bf16 / block-FP8 e4m3 with
+// fp32 128x128 scales / GPTQ int4 g128 with fp16 scale and zero), warp reductions.
+#pragma once
+
+#include "pmoe_internal.h"
+
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
+namespace pmoe {
+namespace dec {
+
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
+
+__device__ __forceinline__ float dot_bf16x8(uint32_t w, uint32_t x, float acc) {
+  acc = fmaf(bf_lo(w), bf_lo(x), acc);
+  return fmaf(bf_hi(w), bf_hi(x), acc);
+}
+
+// Format traits: elements per 16-byte weight chunk, weight bytes per element (x2).
+template <int FMT> struct Fmt;
+template <> struct Fmt<PMOE_BF16> { static constexpr int EPC = 8; static constexpr int BPE2 = 4; };
+template <> struct Fmt<PMOE_FP8_BLOCK128> { static constexpr int EPC = 16; static constexpr int BPE2 = 2; };
+template <> struct Fmt<PMOE_INT4_GPTQ_G128> { static constexpr int EPC = 32; static constexpr int BPE2 = 1; };
+
+// Per-chunk dequantisation parameters of row `row` (of a [rows][cols] matrix), chunk `c`.
+struct ChunkQ {
+  float s, z;
+};
+
+template <int FMT>
+__device__ __forceinline__ ChunkQ chunk_q(const uint8_t* scales, int row, int c, int cols) {
+  ChunkQ q{1.f, 0.f};
+  if constexpr (FMT == PMOE_FP8_BLOCK128) {
+    const float* S = reinterpret_cast<const float*>(scales);
+    q.s = __ldg(S + (size_t)(row >> 7) * (cols >> 7) + ((c * 16) >> 7));
+  } else if constexpr (FMT == PMOE_INT4_GPTQ_G128) {
+    const __half2* SZ = reinterpret_cast<const __half2*>(scales);
+    const float2 sz = __half22float2(SZ[(size_t)row * (cols >> 7) + ((c * 32) >> 7)]);
+    q.s = sz.x;
+    q.z = sz.y;
+  }
+  return q;
+}
+
+// sum over the chunk's elements of w_i * a_i, with a (bf16) read from `av` (EPC/8 uint4).
+template <int FMT, bool SHARED>
+__device__ __forceinline__ float chunk_dot(uint4 w, const uint4* av, ChunkQ q) {
+  if constexpr (FMT == PMOE_BF16) {
+    const uint4 a = SHARED ? av[0] : __ldg(av);
+    float acc = 0.f;
+    acc = dot_bf16x8(w.x, a.x, acc);
+    acc = dot_bf16x8(w.y, a.y, acc);
+    acc = dot_bf16x8(w.z, a.z, acc);
+    acc = dot_bf16x8(w.w, a.w, acc);
+    return acc;
+  } else if constexpr (FMT == PMOE_FP8_BLOCK128) {
+    const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+    float acc = 0.f;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint4 a = SHARED ? av[h] : __ldg(av + h);
+      const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const uint32_t word = wv[2 * h + k];
+        const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(word & 0xffffu), __NV_E4M3);
+        const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(word >> 16), __NV_E4M3);
+        const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&lo));
+        const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+        const uint32_t a0 = aw[2 * k], a1 = aw[2 * k + 1];
+        acc = fmaf(f0.x, bf_lo(a0), acc);
+        acc = fmaf(f0.y, bf_hi(a0), acc);
+        acc = fmaf(f1.x, bf_lo(a1), acc);
+        acc = fmaf(f1.y, bf_hi(a1), acc);
+      }
+    }
+    return acc * q.s;
+  } else {
+    const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+    float acc = 0.f;
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      const uint4 a = SHARED ? av[h] : __ldg(av + h);
+      const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
+      const uint32_t word = wv[h];  // 8 nibbles = elements 8h .. 8h+7
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float q0 = (float)((word >> (8 * k)) & 0xFu) - q.z;
+        const float q1 = (float)((word >> (8 * k + 4)) & 0xFu) - q.z;
+        acc = fmaf(q0, bf_lo(aw[k]), acc);
+        acc = fmaf(q1, bf_hi(aw[k]), acc);
+      }
+    }
+    return acc * q.s;
+  }
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  return v;
+}
+
+__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.f + expf(-g)) * u; }
+
+}  // namespace dec
+}  // namespace pmoe

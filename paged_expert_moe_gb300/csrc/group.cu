@@ -7,36 +7,66 @@
 //   counts[e]  pairs routed to e;   offs = exclusive scan of counts (offs[E] = P)
 //   perm[j]    pairs grouped by expert ascending, ascending pair index inside one
 //              expert (stable), so the grouping is deterministic;   pos = perm^-1
+// Large P: per-chunk histograms, a per-expert scan over chunks, then each pair's
+// stable position from its chunk's prefix and its rank among equal ids before it.
 // A pair whose id is outside [0, E) is left out (pos = -1) and flagged.
 #include "pmoe_internal.h"
 
 namespace pmoe {
 namespace {
 
-// Warp w counts (pass 0) or places (pass 1) the pairs of expert w.
-__global__ void __launch_bounds__(256) group_expert_pass(const int32_t* __restrict__ ids, int P, int E, int pass,
-                                                          Workspace ws, int32_t* __restrict__ err) {
-  const int lane = threadIdx.x & 31;
-  const int e = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (e >= E) return;
-  int base = pass ? ws.offs[e] : 0;
-  int n = 0;
-  for (int p0 = 0; p0 < P; p0 += 32) {
-    const int p = p0 + lane;
-    const int id = (p < P) ? ids[p] : -1;
-    const unsigned m = __ballot_sync(0xffffffffu, id == e);
-    if (pass && id == e) {
-      const int j = base + n + __popc(m & ((1u << lane) - 1u));
-      ws.perm[j] = p;
-      ws.pos[p] = j;
-    }
-    if (pass && e == 0 && p < P && (id < 0 || id >= E)) {
-      ws.pos[p] = -1;
-      atomicOr(err, kErrBadExpertId);
-    }
-    n += __popc(m);
+constexpr int kChunk = 256;  // pairs per CTA in the large-P grouping
+
+// Pass 1 (one CTA per chunk of 256 pairs): per-chunk histogram chunk_cnt[chunk][e].
+__global__ void __launch_bounds__(kChunk) group_chunk_hist(const int32_t* __restrict__ ids, int P, int E,
+                                                           int32_t* __restrict__ chunk_cnt, int32_t* __restrict__ err) {
+  __shared__ int s_cnt[kMaxExperts];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = 0;
+  __syncthreads();
+  const int p = blockIdx.x * kChunk + threadIdx.x;
+  if (p < P) {
+    const int e = ids[p];
+    if (e >= 0 && e < E) atomicAdd(&s_cnt[e], 1);
+    else atomicOr(err, kErrBadExpertId);
   }
-  if (!pass && lane == 0) ws.counts[e] = n;
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) chunk_cnt[(size_t)blockIdx.x * E + e] = s_cnt[e];
+}
+
+// Pass 2 (one thread per expert): counts[e] and, in place, the exclusive prefix of
+// chunk_cnt[.][e] over chunks (the pairs of e in earlier chunks).
+__global__ void __launch_bounds__(256) group_chunk_scan(int n_chunks, int E, int32_t* __restrict__ chunk_cnt,
+                                                        int32_t* __restrict__ counts) {
+  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= E) return;
+  int run = 0;
+  for (int c = 0; c < n_chunks; ++c) {
+    const int v = chunk_cnt[(size_t)c * E + e];
+    chunk_cnt[(size_t)c * E + e] = run;
+    run += v;
+  }
+  counts[e] = run;
+}
+
+// Pass 4 (one CTA per chunk): stable position of every pair:
+// pos = offs[e] + (pairs of e in earlier chunks) + (pairs of e earlier in this chunk).
+__global__ void __launch_bounds__(kChunk) group_chunk_place(const int32_t* __restrict__ ids, int P, int E,
+                                                            const int32_t* __restrict__ chunk_pre, Workspace ws) {
+  __shared__ int s_ids[kChunk];
+  const int p = blockIdx.x * kChunk + threadIdx.x;
+  const int id = (p < P) ? ids[p] : -1;
+  s_ids[threadIdx.x] = id;
+  __syncthreads();
+  if (p >= P) return;
+  if (id < 0 || id >= E) {
+    ws.pos[p] = -1;
+    return;
+  }
+  int before = 0;
+  for (int i = 0; i < (int)threadIdx.x; ++i) before += (s_ids[i] == id);
+  const int j = ws.offs[id] + chunk_pre[(size_t)blockIdx.x * E + id] + before;
+  ws.perm[j] = p;
+  ws.pos[p] = j;
 }
 
 // Single CTA: offs = scan(counts); per-wave tiles of at most tile_n pairs.
@@ -101,6 +131,10 @@ __global__ void __launch_bounds__(1024) group_scan_tiles(int E, const int32_t* _
     int t = (j == 0) ? 0 : s_t[j - 1];
     if (t > ws.max_tiles) t = ws.max_tiles;
     ws.tile_wave[tid] = t;
+    const int jh = j + (tid < n_waves ? plan[L.wave_hits() + tid] : 0);  // first non-resident expert
+    int th = (jh == 0) ? 0 : s_t[jh - 1];
+    if (th > ws.max_tiles) th = ws.max_tiles;
+    ws.tile_split[tid] = th;
   }
 }
 
@@ -169,11 +203,12 @@ cudaError_t launch_group(const int32_t* ids, int P, int E, const int32_t* plan, 
     group_small<<<1, 1024, 0, s>>>(ids, P, E, plan, ws, err);
     return cudaGetLastError();
   }
-  const int wpb = 8;
-  const int blocks = (E + wpb - 1) / wpb;
-  group_expert_pass<<<blocks, wpb * 32, 0, s>>>(ids, P, E, 0, ws, err);
+  const int n_chunks = (P + kChunk - 1) / kChunk;
+  if ((size_t)n_chunks * E > (size_t)ws.chunk_cap) return cudaErrorInvalidValue;
+  group_chunk_hist<<<n_chunks, kChunk, 0, s>>>(ids, P, E, ws.chunk_cnt, err);
+  group_chunk_scan<<<(E + 255) / 256, 256, 0, s>>>(n_chunks, E, ws.chunk_cnt, ws.counts);
   group_scan_tiles<<<1, 1024, 0, s>>>(E, plan, ws, tile_n, err);
-  group_expert_pass<<<blocks, wpb * 32, 0, s>>>(ids, P, E, 1, ws, err);
+  group_chunk_place<<<n_chunks, kChunk, 0, s>>>(ids, P, E, ws.chunk_cnt, ws);
   return cudaGetLastError();
 }
 

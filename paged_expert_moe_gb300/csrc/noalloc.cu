@@ -118,6 +118,8 @@ __global__ void __launch_bounds__(1024) resident_plan_kernel(const int32_t* __re
     plan[L.wave_start() + 1] = n;
     plan[L.miss_start() + 0] = 0;
     plan[L.miss_start() + 1] = 0;
+    plan[L.wave_hits() + 0] = n;
+    plan[L.wave_hits() + 1] = 0;
   }
 }
 

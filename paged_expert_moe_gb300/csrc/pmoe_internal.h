@@ -29,7 +29,8 @@ struct PlanLayout {
   __host__ __device__ int miss_exp() const { return 8 + 4 * E + 2; }   // E
   __host__ __device__ int miss_slot() const { return 8 + 5 * E + 2; }  // E
   __host__ __device__ int wave_of() const { return 8 + 6 * E + 2; }    // E
-  __host__ __device__ int words() const { return 8 + 7 * E + 2; }
+  __host__ __device__ int wave_hits() const { return 8 + 7 * E + 2; }  // E + 1: resident experts first in each wave
+  __host__ __device__ int words() const { return 8 + 8 * E + 3; }
 };
 // header words
 enum { kPlanUnique = 0, kPlanWaves = 1, kPlanMisses = 2, kPlanError = 3, kPlanStep = 4 };
@@ -51,9 +52,14 @@ struct Workspace {
   int32_t* pos;         // [P]  pair -> grouped position
   int32_t* tiles;       // [3 * max_tiles] (slot, pair start, pair count) per tile, grouped by wave
   int32_t* tile_wave;   // [E + 2] tile range of each wave
+  int32_t* tile_split;  // [E + 2] first tile of each wave's non-resident (just paged-in) experts
   __nv_bfloat16* h;     // [P][I] intermediate activations, grouped order
   float* o_part;        // [P][H] per-pair down-projection outputs, grouped order
   __nv_bfloat16* x_perm;  // [P][H] tokens gathered in grouped order (tensor-core path)
+  int32_t* chunk_cnt;   // [ceil(P/256)][E] per-chunk histograms / prefixes (large-P grouping)
+  unsigned* gbar;       // [2] exit counter of the fused decode kernel (zeroed once, reset by its last CTA)
+  unsigned* done;       // [E] per-expert count of finished h rows in a fused decode launch (same reset)
+  int chunk_cap;        // entries of chunk_cnt
   int max_tiles;
 };
 
@@ -73,7 +79,13 @@ cudaError_t launch_gemv_down(int fmt, int H, int I, const int32_t* plan, int E, 
                              const Workspace& ws, const uint8_t* arena, size_t stride, int num_sms,
                              cudaStream_t s);
 cudaError_t launch_combine(const Workspace& ws, const float* w, const __nv_bfloat16* residual,
-                           __nv_bfloat16* y, int T, int top_k, int H, cudaStream_t s);
+                           __nv_bfloat16* y, int T, int top_k, int H, cudaStream_t s,
+                           const int32_t* skip_if_single_wave_plan = nullptr);
+bool decode_fused_supported(int fmt, int T, int top_k, int H, int I, int num_sms);
+cudaError_t launch_decode_fused(int fmt, const __nv_bfloat16* x, const int32_t* ids, const float* w,
+                                const __nv_bfloat16* residual, __nv_bfloat16* y, int T, int top_k, int H, int I,
+                                const int32_t* plan, int E, int wave, int sub, int fuse_combine, const Workspace& ws,
+                                const uint8_t* arena, size_t stride, int32_t* err, int num_sms, cudaStream_t s);
 cudaError_t launch_pull_pages(const int32_t* plan, int E, int wave, const uint8_t* host_store_dev,
                               size_t stride, size_t expert_bytes, uint8_t* arena, int32_t* err,
                               cudaStream_t s);

@@ -120,19 +120,26 @@ __global__ void __launch_bounds__(kThreads) residency_kernel(const int32_t* __re
       }
     }
     __syncthreads();
+    // wave list: the experts that were resident (hits) first, then this wave's misses,
+    // each part in ascending id, so compute on the hits can start before the page-in
     const bool inw = tid < E && s_pend[tid] != 0 && s_slot_of[tid] >= 0;
-    int n_w;
-    const int wrank = block_exclusive_scan(inw ? 1 : 0, s_warp, &n_w);
+    const bool inw_hit = inw && res;
+    int n_w, n_h;
+    const int hrank = block_exclusive_scan(inw_hit ? 1 : 0, s_warp, &n_h);
+    const int mrank = block_exclusive_scan((inw && !inw_hit) ? 1 : 0, s_warp, &n_w);
+    n_w += n_h;
     if (inw) {
       const int slot = s_slot_of[tid];
-      plan[L.wave_exp() + n_wexp + wrank] = tid;
-      plan[L.wave_slot() + n_wexp + wrank] = slot;
+      const int at = n_wexp + (inw_hit ? hrank : n_h + mrank);
+      plan[L.wave_exp() + at] = tid;
+      plan[L.wave_slot() + at] = slot;
       plan[L.wave_of() + tid] = wave;
       s_last[slot] = step;
     }
     if (tid == 0) {
       plan[L.wave_start() + wave] = n_wexp;
       plan[L.miss_start() + wave] = n_miss;
+      plan[L.wave_hits() + wave] = n_h;
     }
     __syncthreads();
     if (inw) s_pend[tid] = 0;
@@ -144,6 +151,7 @@ __global__ void __launch_bounds__(kThreads) residency_kernel(const int32_t* __re
   if (tid == 0) {
     plan[L.wave_start() + wave] = n_wexp;
     plan[L.miss_start() + wave] = n_miss;
+    plan[L.wave_hits() + wave] = 0;
     plan[kPlanUnique] = n_unique;
     plan[kPlanWaves] = wave;
     plan[kPlanMisses] = n_miss;

@@ -7,11 +7,14 @@
 // With ~128 pairs per expert the contraction is dense enough for the tensor cores.
 //
 // Tiles (swap-AB: the weight rows are the MMA's M side, the expert's pairs the N side):
-//   gate/up  D_g[128 rows j][N pairs] = W_g[j0:j0+128, :] . x_perm[pairs, :]^T and the
-//            same for W_u into a second accumulator; the epilogue writes
-//            h[pair][j] = bf16(silu(D_g) * D_u).           K = H, BK = 64
+//   gate/up  D[128][N pairs] = [W_g[j0:j0+64]; W_u[j0:j0+64]] . x_perm[pairs]^T: TMEM
+//            lanes 0-63 hold gate, 64-127 the matching up rows; the epilogue exchanges
+//            them through shared memory and writes h[pair][j0:j0+64] =
+//            bf16(silu(gate) * up) as 16-byte rows.           K = H, BK = 64
 //   down     D[128 rows n][N pairs] = W_d[n0:n0+128, :] . h[pairs, :]^T; the epilogue
-//            writes the fp32 partial o_part[pair][n].      K = I, BK = 64
+//            writes the fp32 partial o_part[pair][n].          K = I, BK = 64
+// The two TMEM accumulator buffers (2 x 256 columns) let the epilogue of one item run
+// while the MMAs of the next fill the other buffer; 4 TMA stages of 48 KB.
 // N = the tile's pair count rounded up to 16 (<= 256): the instruction descriptor is
 // built per tile, so no MMA work is spent on other experts' pairs beyond that.
 // Warp roles: warp 0 lane 0 issues TMA, warp 1 lane 0 issues tcgen05.mma (warp 1 owns
@@ -134,37 +137,60 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
-template <bool GATEUP>
+// Stage: A = 128 weight rows x 64 K (16 KB) + B = up to 256 pair rows x 64 K (32 KB).
+// Gate/up A tiles hold 64 gate rows (TMEM lanes 0-63) then the matching 64 up rows
+// (lanes 64-127), so one M=128 MMA feeds both halves of SiLU*mul.
 struct TcCfg {
-  static constexpr int kA = GATEUP ? 2 : 1;                 // A tiles per stage (gate + up)
-  static constexpr int kABytes = 128 * kBK * 2;             // 16 KB
-  static constexpr int kBBytes = 256 * kBK * 2;             // 32 KB (room for N = 256)
-  static constexpr int kStageBytes = kA * kABytes + kBBytes;
-  static constexpr int kStages = GATEUP ? 3 : 4;
-  static constexpr int kTmemCols = GATEUP ? 512 : 256;
-  static constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align slack*/ + 256 /*barriers*/;
+  static constexpr int kABytes = 128 * kBK * 2;
+  static constexpr int kBBytes = 256 * kBK * 2;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kStages = 4;
+  static constexpr int kAccCols = 256;   // one accumulator buffer (N <= 256 fp32 columns)
+  static constexpr int kTmemCols = 512;  // two buffers: the epilogue of tile i overlaps the MMAs of tile i+1
+  static constexpr int kStagingFloats = 128 * 17;
+  static constexpr int kSmemBytes = kStages * kStageBytes + kStagingFloats * 4 + 1024 + 256;
 };
+
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// Named barrier over the 128 epilogue threads that also ORs a predicate across them,
+// so a failed wait in any epilogue thread makes all of them leave together.
+__device__ __forceinline__ int epi_bar_or(int pred) {
+  int r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.s32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 1, 128, p;\n\t"
+      "selp.s32 %0, 1, 0, q;\n\t}\n"
+      : "=r"(r)
+      : "r"(pred)
+      : "memory");
+  return r;
+}
 
 // One persistent CTA per SM loops over (tile, m-tile) items of one wave.
 template <bool GATEUP>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_grouped_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_b,
-                      const int32_t* __restrict__ plan, int E, int wave, Workspace ws, int I, int H,
+                      const int32_t* __restrict__ plan, int E, int wave, int sub, Workspace ws, int I, int H,
                       int32_t* __restrict__ err) {
-  using C = TcCfg<GATEUP>;
+  using C = TcCfg;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes);
+  float* staging = reinterpret_cast<float*>(smem + C::kStages * C::kStageBytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(staging + C::kStagingFloats);
   uint64_t* empty = full + C::kStages;
-  uint64_t* acc_full = empty + C::kStages;
-  uint64_t* acc_empty = acc_full + 1;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acc_empty + 1);
+  uint64_t* acc_full = empty + C::kStages;  // [2]
+  uint64_t* acc_empty = acc_full + 2;       // [2]
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acc_empty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (wave >= plan[kPlanWaves]) return;
-  const int t0 = ws.tile_wave[wave], t1 = ws.tile_wave[wave + 1];
-  const int m_tiles = GATEUP ? (I / 128) : (H / 128);
+  int t0 = ws.tile_wave[wave], t1 = ws.tile_wave[wave + 1];
+  if (sub == 1) t1 = ws.tile_split[wave];       // experts resident before the step
+  else if (sub == 2) t0 = ws.tile_split[wave];  // experts paged in for this wave
+  const int m_tiles = GATEUP ? (I / 64) : (H / 128);
   const int n_items = (t1 - t0) * m_tiles;
   if ((int)blockIdx.x >= n_items) return;
   const int kdim = GATEUP ? H : I;
@@ -175,8 +201,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(acc_full, 1);
-    mbar_init(acc_empty, 128);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 128);
+    }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     prefetch_map(&map_w);
@@ -203,7 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int tile = t0 + item / m_tiles, mt = item % m_tiles;
         const int slot = ws.tiles[3 * tile + 0], pstart = ws.tiles[3 * tile + 1], np = ws.tiles[3 * tile + 2];
         const int nb = (np + kTileRowsB - 1) / kTileRowsB;
-        const uint32_t bytes = C::kA * C::kABytes + nb * kTileRowsB * kBK * 2;
+        const uint32_t bytes = C::kABytes + nb * kTileRowsB * kBK * 2;
         for (int kb = 0; kb < n_kb; ++kb) {
           if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, err)) {
             ok = false;
@@ -212,12 +240,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* st = smem + s * C::kStageBytes;
           mbar_arrive_expect_tx(&full[s], bytes);
           if (GATEUP) {
-            tma_load_3d(st, &map_w, &full[s], kb * kBK, mt * 128, slot);
-            tma_load_3d(st + C::kABytes, &map_w, &full[s], kb * kBK, I + mt * 128, slot);
+            tma_load_3d(st, &map_w, &full[s], kb * kBK, mt * 64, slot);                 // gate rows
+            tma_load_3d(st + C::kABytes / 2, &map_w, &full[s], kb * kBK, I + mt * 64, slot);  // up rows
           } else {
             tma_load_3d(st, &map_w, &full[s], kb * kBK, mt * 128, slot);
           }
-          uint8_t* bst = st + C::kA * C::kABytes;
+          uint8_t* bst = st + C::kABytes;
           for (int b = 0; b < nb; ++b)
             tma_load_2d(bst + b * kTileRowsB * kBK * 2, &map_b, &full[s], kb * kBK, pstart + b * kTileRowsB);
           if (++s == C::kStages) {
@@ -239,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       // ---------------- MMA issuer
       int s = 0;
-      uint32_t ph = 0, acc_ph = 0;
+      uint32_t ph = 0;
       bool ok = true;
       int it = 0;
       for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++it) {
@@ -247,11 +275,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int np = ws.tiles[3 * tile + 2];
         const int n_mma = (np + 15) & ~15;
         const uint32_t idesc = idesc_bf16(128, n_mma < 16 ? 16 : n_mma);
-        if (it > 0) {
-          if (!mbar_wait(acc_empty, acc_ph, abort_flag, err)) break;
-          acc_ph ^= 1u;
+        const int ab = it & 1, use = it >> 1;
+        if (use > 0) {
+          if (!mbar_wait(&acc_empty[ab], (uint32_t)((use - 1) & 1), abort_flag, err)) break;
           fence_after();
         }
+        const uint32_t d = tmem + (uint32_t)(ab * C::kAccCols);
         for (int kb = 0; kb < n_kb; ++kb) {
           if (!mbar_wait(&full[s], ph, abort_flag, err)) {
             ok = false;
@@ -260,62 +289,67 @@ __global__ void __launch_bounds__(kThreads, 1)
           fence_after();
           const uint8_t* st = smem + s * C::kStageBytes;
           const uint32_t a0 = smem_u32(st);
-          const uint32_t bb = smem_u32(st + C::kA * C::kABytes);
+          const uint32_t bb = smem_u32(st + C::kABytes);
 #pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk) {
-            const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
-            mma_bf16(tmem, sw128_desc(a0 + kk * 32), sw128_desc(bb + kk * 32), idesc, acc);
-            if (GATEUP) mma_bf16(tmem + 256, sw128_desc(a0 + C::kABytes + kk * 32), sw128_desc(bb + kk * 32), idesc, acc);
-          }
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            mma_bf16(d, sw128_desc(a0 + kk * 32), sw128_desc(bb + kk * 32), idesc, (kb > 0 || kk > 0) ? 1u : 0u);
           mma_commit(&empty[s]);
           if (++s == C::kStages) {
             s = 0;
             ph ^= 1u;
           }
         }
-        if (ok) mma_commit(acc_full);
+        if (ok) mma_commit(&acc_full[ab]);
       }
     }
   } else {
     // ---------------- epilogue: warps 2..5, TMEM lanes 32*(warp%4) ..
     const int q = warp & 3;
     const int row = q * 32 + lane;
-    uint32_t acc_ph = 0;
-    for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+    const int et = threadIdx.x - 64;  // 0..127
+    int it = 0;
+    for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++it) {
       const int tile = t0 + item / m_tiles, mt = item % m_tiles;
       const int pstart = ws.tiles[3 * tile + 1], np = ws.tiles[3 * tile + 2];
       const int n_mma = (np + 15) & ~15;
-      if (!mbar_wait(acc_full, acc_ph, abort_flag, err)) break;
-      acc_ph ^= 1u;
+      const int ab = it & 1, use = it >> 1;
+      const bool got = mbar_wait(&acc_full[ab], (uint32_t)(use & 1), abort_flag, err);
+      if (epi_bar_or(got ? 0 : 1)) break;
       fence_after();
-      const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16);
+      const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(ab * C::kAccCols);
       for (int c = 0; c < n_mma; c += 16) {
+        uint32_t v[16];
+        tmem_ld16(tbase + c, v);
+        tmem_wait_ld();
         if (GATEUP) {
-          uint32_t g[16], u[16];
-          tmem_ld16(tbase + c, g);
-          tmem_ld16(tbase + 256 + c, u);
-          tmem_wait_ld();
-          const int j = mt * 128 + row;
+          // stage gate (rows 0-63) and up (rows 64-127) values, then each thread forms
+          // 8 consecutive h values of one pair: one 16-byte store, 128 B per pair row
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            if (c + i < np) {
-              const float gv = __uint_as_float(g[i]), uv = __uint_as_float(u[i]);
-              const float hv = gv / (1.f + expf(-gv)) * uv;
-              ws.h[(size_t)(pstart + c + i) * I + j] = __float2bfloat16_rn(hv);
+          for (int i = 0; i < 16; ++i) staging[row * 17 + i] = __uint_as_float(v[i]);
+          epi_bar();
+          const int pl = et >> 3, js = (et & 7) * 8;
+          if (c + pl < np) {
+            uint32_t packed[4];
+#pragma unroll
+            for (int jj = 0; jj < 8; jj += 2) {
+              const float g0 = staging[(js + jj) * 17 + pl], u0 = staging[(64 + js + jj) * 17 + pl];
+              const float g1 = staging[(js + jj + 1) * 17 + pl], u1 = staging[(64 + js + jj + 1) * 17 + pl];
+              const __nv_bfloat162 hv = __floats2bfloat162_rn(g0 / (1.f + expf(-g0)) * u0, g1 / (1.f + expf(-g1)) * u1);
+              packed[jj >> 1] = *reinterpret_cast<const uint32_t*>(&hv);
             }
+            *reinterpret_cast<uint4*>(ws.h + (size_t)(pstart + c + pl) * I + mt * 64 + js) =
+                make_uint4(packed[0], packed[1], packed[2], packed[3]);
           }
+          epi_bar();
         } else {
-          uint32_t o[16];
-          tmem_ld16(tbase + c, o);
-          tmem_wait_ld();
           const int n = mt * 128 + row;
 #pragma unroll
           for (int i = 0; i < 16; ++i)
-            if (c + i < np) ws.o_part[(size_t)(pstart + c + i) * H + n] = __uint_as_float(o[i]);
+            if (c + i < np) ws.o_part[(size_t)(pstart + c + i) * H + n] = __uint_as_float(v[i]);
         }
       }
       fence_before();
-      mbar_arrive(acc_empty);
+      mbar_arrive(&acc_empty[ab]);
     }
   }
   fence_before();
@@ -357,9 +391,9 @@ int encode(CUtensorMap* m, void* base, int rank, const cuuint64_t* dims, const c
 }
 
 template <bool GATEUP>
-cudaError_t launch_tc(const CUtensorMap& mw, const CUtensorMap& mb, const int32_t* plan, int E, int wave,
+cudaError_t launch_tc(const CUtensorMap& mw, const CUtensorMap& mb, const int32_t* plan, int E, int wave, int sub,
                       const Workspace& ws, int I, int H, int num_sms, int32_t* err, cudaStream_t s) {
-  using C = TcCfg<GATEUP>;
+  using C = TcCfg;
   static bool attr_set = false;
   if (!attr_set) {
     const cudaError_t e = cudaFuncSetAttribute(tc_grouped_kernel<GATEUP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -367,7 +401,7 @@ cudaError_t launch_tc(const CUtensorMap& mw, const CUtensorMap& mb, const int32_
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  tc_grouped_kernel<GATEUP><<<num_sms, kThreads, C::kSmemBytes, s>>>(mw, mb, plan, E, wave, ws, I, H, err);
+  tc_grouped_kernel<GATEUP><<<num_sms, kThreads, C::kSmemBytes, s>>>(mw, mb, plan, E, wave, sub, ws, I, H, err);
   return cudaGetLastError();
 }
 
@@ -382,7 +416,7 @@ int tc_make_weight_maps(uint8_t* arena, size_t stride, int K, int H, int I, TcMa
   {
     const cuuint64_t dims[3] = {(cuuint64_t)H, (cuuint64_t)(2 * I), (cuuint64_t)K};
     const cuuint64_t strides[2] = {(cuuint64_t)H * 2, (cuuint64_t)stride};
-    const cuuint32_t box[3] = {(cuuint32_t)kBK, 128, 1};
+    const cuuint32_t box[3] = {(cuuint32_t)kBK, 64, 1};  // 64 gate or 64 up rows
     if (encode(&out->gu, arena, 3, dims, strides, box) != PMOE_OK) return PMOE_ECUDA;
   }
   {
@@ -411,14 +445,14 @@ int tc_make_act_maps(__nv_bfloat16* x_perm, __nv_bfloat16* h, size_t P, int H, i
   return PMOE_OK;
 }
 
-cudaError_t tc_gateup(const TcMaps& wm, const TcMaps& am, const int32_t* plan, int E, int wave, const Workspace& ws,
-                      int I, int H, int num_sms, int32_t* err, cudaStream_t s) {
-  return launch_tc<true>(wm.gu, am.x, plan, E, wave, ws, I, H, num_sms, err, s);
+cudaError_t tc_gateup(const TcMaps& wm, const TcMaps& am, const int32_t* plan, int E, int wave, int sub,
+                      const Workspace& ws, int I, int H, int num_sms, int32_t* err, cudaStream_t s) {
+  return launch_tc<true>(wm.gu, am.x, plan, E, wave, sub, ws, I, H, num_sms, err, s);
 }
 
-cudaError_t tc_down(const TcMaps& wm, const TcMaps& am, const int32_t* plan, int E, int wave, const Workspace& ws,
-                    int I, int H, int num_sms, int32_t* err, cudaStream_t s) {
-  return launch_tc<false>(wm.d, am.h, plan, E, wave, ws, I, H, num_sms, err, s);
+cudaError_t tc_down(const TcMaps& wm, const TcMaps& am, const int32_t* plan, int E, int wave, int sub,
+                    const Workspace& ws, int I, int H, int num_sms, int32_t* err, cudaStream_t s) {
+  return launch_tc<false>(wm.d, am.h, plan, E, wave, sub, ws, I, H, num_sms, err, s);
 }
 
 }  // namespace pmoe

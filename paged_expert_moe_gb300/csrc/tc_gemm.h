@@ -19,9 +19,11 @@ struct TcMaps {
 bool tc_supported(int H, int I);
 int tc_make_weight_maps(uint8_t* arena, size_t stride, int K, int H, int I, TcMaps* out);
 int tc_make_act_maps(__nv_bfloat16* x_perm, __nv_bfloat16* h, size_t P, int H, int I, TcMaps* out);
-cudaError_t tc_gateup(const TcMaps& wm, const TcMaps& am, const int32_t* plan, int E, int wave, const Workspace& ws,
-                      int I, int H, int num_sms, int32_t* err, cudaStream_t s);
-cudaError_t tc_down(const TcMaps& wm, const TcMaps& am, const int32_t* plan, int E, int wave, const Workspace& ws,
-                    int I, int H, int num_sms, int32_t* err, cudaStream_t s);
+// sub: 0 = the whole wave, 1 = its experts that were resident before the step,
+// 2 = its experts paged in for this wave (tiles of the two parts are contiguous).
+cudaError_t tc_gateup(const TcMaps& wm, const TcMaps& am, const int32_t* plan, int E, int wave, int sub,
+                      const Workspace& ws, int I, int H, int num_sms, int32_t* err, cudaStream_t s);
+cudaError_t tc_down(const TcMaps& wm, const TcMaps& am, const int32_t* plan, int E, int wave, int sub,
+                    const Workspace& ws, int I, int H, int num_sms, int32_t* err, cudaStream_t s);
 
 }  // namespace pmoe
