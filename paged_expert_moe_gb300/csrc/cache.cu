@@ -406,7 +406,7 @@ int expert_cache_create(const pmoe_cache_desc* desc, pmoe_cache** out) {
   {
     // forward workspace
     const size_t P = (size_t)d.max_tokens * d.top_k;
-    c->use_tc = (d.format == PMOE_BF16) && d.max_tokens > kGemvMaxTokens && tc_supported(d.hidden, d.intermediate);
+    c->use_tc = d.max_tokens > kGemvMaxTokens && tc_supported(d.hidden, d.intermediate);
     c->ws.max_tiles = (int)(E + P / 16 + 1);
     size_t off = 0;
     auto carve = [&](size_t bytes) {
@@ -451,7 +451,7 @@ int expert_cache_create(const pmoe_cache_desc* desc, pmoe_cache** out) {
   if (c->use_tc) {
     c->maps.resize(Lr);
     for (int l = 0; l < Lr; ++l) {
-      const int r = tc_make_weight_maps(c->arena[l], c->stride, K, d.hidden, d.intermediate, &c->maps[l]);
+      const int r = tc_make_weight_maps(c->arena[l], c->stride, K, d.hidden, d.intermediate, d.format, &c->maps[l]);
       if (r != PMOE_OK) {
         status = r;
         goto fail;
@@ -600,12 +600,12 @@ int moe_paged_forward(pmoe_cache* c, int layer, const void* x, int T, const int3
     if (tc) {
       {
         KernelMark km(c, PMOE_K_GATEUP, s);
-        PMOE_CUDA(tc_gateup(c->maps[layer], c->ws_maps, c->plan_dev[layer], E, wv, sub, c->ws, I, H, c->num_sms,
-                            c->err_dev, s));
+        PMOE_CUDA(tc_gateup(c->d.format, c->maps[layer], c->ws_maps, c->plan_dev[layer], E, wv, sub, c->ws, I, H,
+                            c->arena[layer], c->stride, c->num_sms, c->err_dev, s));
       }
       KernelMark km(c, PMOE_K_DOWN, s);
-      PMOE_CUDA(tc_down(c->maps[layer], c->ws_maps, c->plan_dev[layer], E, wv, sub, c->ws, I, H, c->num_sms,
-                        c->err_dev, s));
+      PMOE_CUDA(tc_down(c->d.format, c->maps[layer], c->ws_maps, c->plan_dev[layer], E, wv, sub, c->ws, I, H,
+                        c->arena[layer], c->stride, c->num_sms, c->err_dev, s));
     } else if (fused) {
       KernelMark km(c, PMOE_K_DECODE, s);
       PMOE_CUDA(launch_decode_fused(c->d.format, (const __nv_bfloat16*)x, ids, w, (const __nv_bfloat16*)residual,

@@ -24,6 +24,8 @@
 #include "tc_gemm.h"
 
 #include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cstdio>
 
 namespace pmoe {
@@ -31,7 +33,6 @@ namespace {
 
 constexpr int kBK = 64;             // K elements per stage (128 bytes of bf16 = one swizzle row)
 constexpr int kTileRowsB = 32;      // rows per TMA box of the pair operand
-constexpr int kThreads = 192;       // 6 warps
 constexpr long long kWaitLimit = 4000000000LL;  // clock64 cycles (~2 s) before a wait gives up
 constexpr int32_t kErrTcTimeout = 16;
 
@@ -140,15 +141,19 @@ __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.
 // Stage: A = 128 weight rows x 64 K (16 KB) + B = up to 256 pair rows x 64 K (32 KB).
 // Gate/up A tiles hold 64 gate rows (TMEM lanes 0-63) then the matching 64 up rows
 // (lanes 64-127), so one M=128 MMA feeds both halves of SiLU*mul.
+template <int FMT>
 struct TcCfg {
-  static constexpr int kABytes = 128 * kBK * 2;
-  static constexpr int kBBytes = 256 * kBK * 2;
-  static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kStages = 4;
+  static constexpr int kABytes = 128 * kBK * 2;            // bf16 A tile (MMA operand)
+  static constexpr int kBBytes = 256 * kBK * 2;            // bf16 B tile (up to 256 pairs)
+  // quantised A tile as loaded by TMA, before the converter warps dequantise it
+  static constexpr int kQBytes = FMT == PMOE_FP8_BLOCK128 ? 128 * kBK : FMT == PMOE_INT4_GPTQ_G128 ? 128 * kBK / 2 : 0;
+  static constexpr int kStageBytes = kABytes + kBBytes + kQBytes;
+  static constexpr int kStages = FMT == PMOE_FP8_BLOCK128 ? 3 : 4;
   static constexpr int kAccCols = 256;   // one accumulator buffer (N <= 256 fp32 columns)
   static constexpr int kTmemCols = 512;  // two buffers: the epilogue of tile i overlaps the MMAs of tile i+1
   static constexpr int kStagingFloats = 128 * 17;
-  static constexpr int kSmemBytes = kStages * kStageBytes + kStagingFloats * 4 + 1024 + 256;
+  static constexpr int kSmemBytes = kStages * kStageBytes + kStagingFloats * 4 + 1024 + 512;
+  static constexpr int kThreads = FMT == PMOE_BF16 ? 192 : 320;  // + 4 converter warps
 };
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
@@ -169,12 +174,13 @@ __device__ __forceinline__ int epi_bar_or(int pred) {
 }
 
 // One persistent CTA per SM loops over (tile, m-tile) items of one wave.
-template <bool GATEUP>
-__global__ void __launch_bounds__(kThreads, 1)
+template <bool GATEUP, int FMT>
+__global__ void __launch_bounds__(TcCfg<FMT>::kThreads, 1)
     tc_grouped_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_b,
                       const int32_t* __restrict__ plan, int E, int wave, int sub, Workspace ws, int I, int H,
-                      int32_t* __restrict__ err) {
-  using C = TcCfg;
+                      const uint8_t* __restrict__ arena, size_t stride, ExpertLayout lay, int32_t* __restrict__ err) {
+  using C = TcCfg<FMT>;
+  constexpr bool kQuant = FMT != PMOE_BF16;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   float* staging = reinterpret_cast<float*>(smem + C::kStages * C::kStageBytes);
@@ -182,7 +188,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* empty = full + C::kStages;
   uint64_t* acc_full = empty + C::kStages;  // [2]
   uint64_t* acc_empty = acc_full + 2;       // [2]
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acc_empty + 2);
+  uint64_t* conv = acc_empty + 2;           // [kStages] quantised A converted (kQuant only)
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(conv + C::kStages);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -205,6 +212,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&acc_full[b], 1);
       mbar_init(&acc_empty[b], 128);
     }
+    if (kQuant)
+      for (int s = 0; s < C::kStages; ++s) mbar_init(&conv[s], 128);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     prefetch_map(&map_w);
@@ -231,7 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int tile = t0 + item / m_tiles, mt = item % m_tiles;
         const int slot = ws.tiles[3 * tile + 0], pstart = ws.tiles[3 * tile + 1], np = ws.tiles[3 * tile + 2];
         const int nb = (np + kTileRowsB - 1) / kTileRowsB;
-        const uint32_t bytes = C::kABytes + nb * kTileRowsB * kBK * 2;
+        const uint32_t bytes = (kQuant ? C::kQBytes : C::kABytes) + nb * kTileRowsB * kBK * 2;
         for (int kb = 0; kb < n_kb; ++kb) {
           if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, err)) {
             ok = false;
@@ -239,7 +248,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           uint8_t* st = smem + s * C::kStageBytes;
           mbar_arrive_expect_tx(&full[s], bytes);
-          if (GATEUP) {
+          if (kQuant) {
+            // quantised rows land in the stage's staging area (row-major, unswizzled)
+            uint8_t* q = st + C::kABytes + C::kBBytes;
+            const int kc = FMT == PMOE_FP8_BLOCK128 ? kb * kBK : kb * kBK / 2;  // bytes along K
+            if (GATEUP) {
+              tma_load_3d(q, &map_w, &full[s], kc, mt * 64, slot);
+              tma_load_3d(q + C::kQBytes / 2, &map_w, &full[s], kc, I + mt * 64, slot);
+            } else {
+              tma_load_3d(q, &map_w, &full[s], kc, mt * 128, slot);
+            }
+          } else if (GATEUP) {
             tma_load_3d(st, &map_w, &full[s], kb * kBK, mt * 64, slot);                 // gate rows
             tma_load_3d(st + C::kABytes / 2, &map_w, &full[s], kb * kBK, I + mt * 64, slot);  // up rows
           } else {
@@ -282,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const uint32_t d = tmem + (uint32_t)(ab * C::kAccCols);
         for (int kb = 0; kb < n_kb; ++kb) {
-          if (!mbar_wait(&full[s], ph, abort_flag, err)) {
+          if (!mbar_wait(kQuant ? &conv[s] : &full[s], ph, abort_flag, err)) {
             ok = false;
             break;
           }
@@ -302,7 +321,77 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) mma_commit(&acc_full[ab]);
       }
     }
-  } else {
+  } else if (kQuant && warp >= 6) {
+    // ---------------- converters: warps 6..9, thread r owns row r of the A tile. Each
+    // quantised row (64 K values) is dequantised with its scale (block-FP8: the fp32
+    // scale of its 128x128 block; int4: (q - z) * s of its group of 128) to bf16 and
+    // written in the 128-byte-swizzled K-major layout TMA would have produced.
+    const int r = threadIdx.x - 192;
+    int s = 0;
+    uint32_t ph = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+      const int tile = t0 + item / m_tiles, mt = item % m_tiles;
+      const int slot = ws.tiles[3 * tile + 0];
+      const uint8_t* ex = arena + (size_t)slot * stride;
+      const int grow = GATEUP ? (r < 64 ? mt * 64 + r : I + mt * 64 + (r - 64)) : mt * 128 + r;
+      const int cols = GATEUP ? H : I;
+      const uint8_t* sc = ex + (GATEUP ? lay.gu_s : lay.d_s);
+      for (int kb = 0; kb < n_kb; ++kb) {
+        if (!mbar_wait(&full[s], ph, abort_flag, err)) {
+          ok = false;
+          break;
+        }
+        uint8_t* st = smem + s * C::kStageBytes;
+        uint4* arow = reinterpret_cast<uint4*>(st + r * 128);
+        if (FMT == PMOE_FP8_BLOCK128) {
+          const uint8_t* q = st + C::kABytes + C::kBBytes + r * kBK;
+          const float sv = reinterpret_cast<const float*>(sc)[(size_t)(grow >> 7) * (cols >> 7) + ((kb * kBK) >> 7)];
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint2 v = *reinterpret_cast<const uint2*>(q + c * 8);
+            const uint32_t wv[2] = {v.x, v.y};
+            uint32_t out[4];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(wv[h] & 0xffffu), __NV_E4M3);
+              const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(wv[h] >> 16), __NV_E4M3);
+              const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&lo));
+              const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+              const __nv_bfloat162 b0 = __floats2bfloat162_rn(f0.x * sv, f0.y * sv);
+              const __nv_bfloat162 b1 = __floats2bfloat162_rn(f1.x * sv, f1.y * sv);
+              out[2 * h] = *reinterpret_cast<const uint32_t*>(&b0);
+              out[2 * h + 1] = *reinterpret_cast<const uint32_t*>(&b1);
+            }
+            arow[c ^ (r & 7)] = make_uint4(out[0], out[1], out[2], out[3]);
+          }
+        } else {
+          const uint8_t* q = st + C::kABytes + C::kBBytes + r * (kBK / 2);
+          const float2 sz = __half22float2(
+              reinterpret_cast<const __half2*>(sc)[(size_t)grow * (cols >> 7) + ((kb * kBK) >> 7)]);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint32_t word = *reinterpret_cast<const uint32_t*>(q + c * 4);  // 8 nibbles, low first
+            uint32_t out[4];
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              const float w0 = ((float)((word >> (8 * h)) & 0xFu) - sz.y) * sz.x;
+              const float w1 = ((float)((word >> (8 * h + 4)) & 0xFu) - sz.y) * sz.x;
+              const __nv_bfloat162 bv = __floats2bfloat162_rn(w0, w1);
+              out[h] = *reinterpret_cast<const uint32_t*>(&bv);
+            }
+            arow[c ^ (r & 7)] = make_uint4(out[0], out[1], out[2], out[3]);
+          }
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_arrive(&conv[s]);
+        if (++s == C::kStages) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
+    }
+  } else if (warp >= 2 && warp <= 5) {
     // ---------------- epilogue: warps 2..5, TMEM lanes 32*(warp%4) ..
     const int q = warp & 3;
     const int row = q * 32 + lane;
@@ -380,28 +469,31 @@ EncodeTiledFn get_encode() {
 }
 
 int encode(CUtensorMap* m, void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides_bytes,
-           const cuuint32_t* box) {
+           const cuuint32_t* box, bool bytes_unswizzled = false) {
   EncodeTiledFn fn = get_encode();
   if (fn == nullptr) return PMOE_ECUDA;
   cuuint32_t estr[3] = {1, 1, 1};
-  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, base, dims, strides_bytes, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  const CUresult r = fn(m, bytes_unswizzled ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank,
+                        base, dims, strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        bytes_unswizzled ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? PMOE_OK : PMOE_ECUDA;
 }
 
-template <bool GATEUP>
+template <bool GATEUP, int FMT>
 cudaError_t launch_tc(const CUtensorMap& mw, const CUtensorMap& mb, const int32_t* plan, int E, int wave, int sub,
-                      const Workspace& ws, int I, int H, int num_sms, int32_t* err, cudaStream_t s) {
-  using C = TcCfg;
+                      const Workspace& ws, int I, int H, const uint8_t* arena, size_t stride, int num_sms,
+                      int32_t* err, cudaStream_t s) {
+  using C = TcCfg<FMT>;
   static bool attr_set = false;
   if (!attr_set) {
-    const cudaError_t e = cudaFuncSetAttribute(tc_grouped_kernel<GATEUP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               C::kSmemBytes);
+    const cudaError_t e = cudaFuncSetAttribute(tc_grouped_kernel<GATEUP, FMT>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  tc_grouped_kernel<GATEUP><<<num_sms, kThreads, C::kSmemBytes, s>>>(mw, mb, plan, E, wave, sub, ws, I, H, err);
+  tc_grouped_kernel<GATEUP, FMT><<<num_sms, C::kThreads, C::kSmemBytes, s>>>(
+      mw, mb, plan, E, wave, sub, ws, I, H, arena, stride, expert_layout(FMT, H, I), err);
   return cudaGetLastError();
 }
 
@@ -411,22 +503,36 @@ bool tc_supported(int H, int I) {
   return H % 128 == 0 && I % 128 == 0 && H >= 128 && I >= 128 && get_encode() != nullptr;
 }
 
-int tc_make_weight_maps(uint8_t* arena, size_t stride, int K, int H, int I, TcMaps* out) {
+int tc_make_weight_maps(uint8_t* arena, size_t stride, int K, int H, int I, int fmt, TcMaps* out) {
   if (stride % 16 != 0) return PMOE_EUNSUPPORTED;
-  {
-    const cuuint64_t dims[3] = {(cuuint64_t)H, (cuuint64_t)(2 * I), (cuuint64_t)K};
-    const cuuint64_t strides[2] = {(cuuint64_t)H * 2, (cuuint64_t)stride};
-    const cuuint32_t box[3] = {(cuuint32_t)kBK, 64, 1};  // 64 gate or 64 up rows
-    if (encode(&out->gu, arena, 3, dims, strides, box) != PMOE_OK) return PMOE_ECUDA;
-  }
-  {
+  const ExpertLayout lay = expert_layout(fmt, H, I);
+  if (fmt == PMOE_BF16) {
+    {
+      const cuuint64_t dims[3] = {(cuuint64_t)H, (cuuint64_t)(2 * I), (cuuint64_t)K};
+      const cuuint64_t strides[2] = {(cuuint64_t)H * 2, (cuuint64_t)stride};
+      const cuuint32_t box[3] = {(cuuint32_t)kBK, 64, 1};  // 64 gate or 64 up rows
+      if (encode(&out->gu, arena, 3, dims, strides, box) != PMOE_OK) return PMOE_ECUDA;
+    }
     const cuuint64_t dims[3] = {(cuuint64_t)I, (cuuint64_t)H, (cuuint64_t)K};
     const cuuint64_t strides[2] = {(cuuint64_t)I * 2, (cuuint64_t)stride};
     const cuuint32_t box[3] = {(cuuint32_t)kBK, 128, 1};
-    uint8_t* base = arena + (size_t)2 * 2 * I * H;  // W_d follows W_gu in a bf16 expert
-    if (encode(&out->d, base, 3, dims, strides, box) != PMOE_OK) return PMOE_ECUDA;
+    return encode(&out->d, arena + lay.d_w, 3, dims, strides, box) == PMOE_OK ? PMOE_OK : PMOE_ECUDA;
   }
-  return PMOE_OK;
+  if (fmt != PMOE_FP8_BLOCK128 && fmt != PMOE_INT4_GPTQ_G128) return PMOE_EUNSUPPORTED;
+  // quantised weights are loaded as bytes (one e4m3 or two int4 per byte), unswizzled
+  const cuuint64_t hb = fmt == PMOE_FP8_BLOCK128 ? (cuuint64_t)H : (cuuint64_t)H / 2;
+  const cuuint64_t ib = fmt == PMOE_FP8_BLOCK128 ? (cuuint64_t)I : (cuuint64_t)I / 2;
+  const cuuint32_t kbb = fmt == PMOE_FP8_BLOCK128 ? (cuuint32_t)kBK : (cuuint32_t)kBK / 2;
+  {
+    const cuuint64_t dims[3] = {hb, (cuuint64_t)(2 * I), (cuuint64_t)K};
+    const cuuint64_t strides[2] = {hb, (cuuint64_t)stride};
+    const cuuint32_t box[3] = {kbb, 64, 1};
+    if (encode(&out->gu, arena + lay.gu_w, 3, dims, strides, box, true) != PMOE_OK) return PMOE_ECUDA;
+  }
+  const cuuint64_t dims[3] = {ib, (cuuint64_t)H, (cuuint64_t)K};
+  const cuuint64_t strides[2] = {ib, (cuuint64_t)stride};
+  const cuuint32_t box[3] = {kbb, 128, 1};
+  return encode(&out->d, arena + lay.d_w, 3, dims, strides, box, true) == PMOE_OK ? PMOE_OK : PMOE_ECUDA;
 }
 
 int tc_make_act_maps(__nv_bfloat16* x_perm, __nv_bfloat16* h, size_t P, int H, int I, TcMaps* out) {
@@ -445,14 +551,26 @@ int tc_make_act_maps(__nv_bfloat16* x_perm, __nv_bfloat16* h, size_t P, int H, i
   return PMOE_OK;
 }
 
-cudaError_t tc_gateup(const TcMaps& wm, const TcMaps& am, const int32_t* plan, int E, int wave, int sub,
-                      const Workspace& ws, int I, int H, int num_sms, int32_t* err, cudaStream_t s) {
-  return launch_tc<true>(wm.gu, am.x, plan, E, wave, sub, ws, I, H, num_sms, err, s);
+cudaError_t tc_gateup(int fmt, const TcMaps& wm, const TcMaps& am, const int32_t* plan, int E, int wave, int sub,
+                      const Workspace& ws, int I, int H, const uint8_t* arena, size_t stride, int num_sms,
+                      int32_t* err, cudaStream_t s) {
+  if (fmt == PMOE_FP8_BLOCK128)
+    return launch_tc<true, PMOE_FP8_BLOCK128>(wm.gu, am.x, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, s);
+  if (fmt == PMOE_INT4_GPTQ_G128)
+    return launch_tc<true, PMOE_INT4_GPTQ_G128>(wm.gu, am.x, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err,
+                                                s);
+  return launch_tc<true, PMOE_BF16>(wm.gu, am.x, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, s);
 }
 
-cudaError_t tc_down(const TcMaps& wm, const TcMaps& am, const int32_t* plan, int E, int wave, int sub,
-                    const Workspace& ws, int I, int H, int num_sms, int32_t* err, cudaStream_t s) {
-  return launch_tc<false>(wm.d, am.h, plan, E, wave, sub, ws, I, H, num_sms, err, s);
+cudaError_t tc_down(int fmt, const TcMaps& wm, const TcMaps& am, const int32_t* plan, int E, int wave, int sub,
+                    const Workspace& ws, int I, int H, const uint8_t* arena, size_t stride, int num_sms, int32_t* err,
+                    cudaStream_t s) {
+  if (fmt == PMOE_FP8_BLOCK128)
+    return launch_tc<false, PMOE_FP8_BLOCK128>(wm.d, am.h, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, s);
+  if (fmt == PMOE_INT4_GPTQ_G128)
+    return launch_tc<false, PMOE_INT4_GPTQ_G128>(wm.d, am.h, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err,
+                                                 s);
+  return launch_tc<false, PMOE_BF16>(wm.d, am.h, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, s);
 }
 
 }  // namespace pmoe

@@ -10,20 +10,24 @@ namespace pmoe {
 constexpr int kTcMaxN = 256;  // pairs per tile (MMA N)
 
 struct TcMaps {
-  CUtensorMap gu;  // gate/up rows of every slot: dims {H, 2I, K} bf16
-  CUtensorMap d;   // down rows of every slot: dims {I, H, K} bf16
+  CUtensorMap gu;  // gate/up rows of every slot: dims {H (bytes if quantised), 2I, K}
+  CUtensorMap d;   // down rows of every slot: dims {I (bytes if quantised), H, K}
   CUtensorMap x;   // gathered activations x_perm: dims {H, P} bf16
   CUtensorMap h;   // intermediate h: dims {I, P} bf16
 };
 
 bool tc_supported(int H, int I);
-int tc_make_weight_maps(uint8_t* arena, size_t stride, int K, int H, int I, TcMaps* out);
+// Weight tensor maps over one layer's slot arena: bf16 rows (128-byte swizzle) or, for
+// block-FP8 and GPTQ-int4, the raw quantised bytes (dequantised in shared memory).
+int tc_make_weight_maps(uint8_t* arena, size_t stride, int K, int H, int I, int fmt, TcMaps* out);
 int tc_make_act_maps(__nv_bfloat16* x_perm, __nv_bfloat16* h, size_t P, int H, int I, TcMaps* out);
 // sub: 0 = the whole wave, 1 = its experts that were resident before the step,
 // 2 = its experts paged in for this wave (tiles of the two parts are contiguous).
-cudaError_t tc_gateup(const TcMaps& wm, const TcMaps& am, const int32_t* plan, int E, int wave, int sub,
-                      const Workspace& ws, int I, int H, int num_sms, int32_t* err, cudaStream_t s);
-cudaError_t tc_down(const TcMaps& wm, const TcMaps& am, const int32_t* plan, int E, int wave, int sub,
-                    const Workspace& ws, int I, int H, int num_sms, int32_t* err, cudaStream_t s);
+cudaError_t tc_gateup(int fmt, const TcMaps& wm, const TcMaps& am, const int32_t* plan, int E, int wave, int sub,
+                      const Workspace& ws, int I, int H, const uint8_t* arena, size_t stride, int num_sms,
+                      int32_t* err, cudaStream_t s);
+cudaError_t tc_down(int fmt, const TcMaps& wm, const TcMaps& am, const int32_t* plan, int E, int wave, int sub,
+                    const Workspace& ws, int I, int H, const uint8_t* arena, size_t stride, int num_sms, int32_t* err,
+                    cudaStream_t s);
 
 }  // namespace pmoe

@@ -45,10 +45,12 @@ def _forward(cache, x_bits, logits, k):
     return y
 
 
-@pytest.mark.parametrize("T,skew", [(300, True), (9, False), (64, False), (1000, False)])
-def test_prefill_small_layer_parity_and_bitwise_k_invariance(pm, T, skew):
+@pytest.mark.parametrize("T,skew,fmt", [(300, True, 0), (9, False, 0), (64, False, 0), (1000, False, 0),
+                                        (300, True, 1), (64, False, 1), (300, True, 2), (64, False, 2)])
+def test_prefill_small_layer_parity_and_bitwise_k_invariance(pm, T, skew, fmt):
+    """bf16, block-FP8 (dequantised in shared memory) and GPTQ-int4 prefill tiles."""
     E, k, H, I = 16, 4, 256, 384
-    L = hz.SyntheticLayer(0, E, H, I, seed=200 + T)
+    L = hz.SyntheticLayer(fmt, E, H, I, seed=200 + T)
     rng = np.random.default_rng(200 + T)
     sets = _skewed_sets(rng, T, E, k) if skew else gen.uniform_routing_sets(rng, T, E, k)
     x_bits, logits = hz.step_inputs(rng, sets, E, H)
@@ -62,7 +64,7 @@ def test_prefill_small_layer_parity_and_bitwise_k_invariance(pm, T, skew):
         assert (st["misses"], st["waves"]) == (out["n_misses"], len(out["waves"]))
         cache.close()
     ids, w = orouter.router_topk(logits, k)
-    hz.assert_layer_close(hz.bf16_to_f64(ys[16]), L.oracle_y(x_bits, ids, w), 0)
+    hz.assert_layer_close(hz.bf16_to_f64(ys[16]), L.oracle_y(x_bits, ids, w), fmt)
     for K in (5, 1):
         assert torch.equal(ys[K].view(torch.int16), ys[16].view(torch.int16)), f"K={K} differs"
 
@@ -105,3 +107,27 @@ def test_gemv_and_tensor_core_paths_agree_at_the_boundary(pm):
         cache.close()
         ids, w = orouter.router_topk(logits, k)
         hz.assert_layer_close(hz.bf16_to_f64(y), L.oracle_y(x_bits, ids, w), 0)
+
+
+def test_prefill_fp8_512_tokens_k40(pm):
+    """Block-FP8 Qwen3-30B-A3B layer, 512-token prefill, K=40 (several waves): sampled tokens
+    against the oracle (rel-Frobenius 3e-2) and all outputs bit for bit against K=128."""
+    E, k, H, I, T = 128, 8, 2048, 768, 512
+    L = hz.SyntheticLayer(1, E, H, I, seed=500)
+    rng = np.random.default_rng(500)
+    sets = gen.uniform_routing_sets(rng, T, E, k)
+    x_bits, logits = hz.step_inputs(rng, sets, E, H)
+    cache = hz.make_cache([L], k, 40, max_tokens=T)
+    y40 = _forward(cache, x_bits, logits, k)
+    st = cache.expert_cache_stats(0)
+    sim = olru.LayerLRU(E, 40)
+    out = sim.step(np.asarray(sets).ravel().tolist())
+    assert (st["misses"], st["waves"]) == (out["n_misses"], len(out["waves"]))
+    cache.close()
+    cache = hz.make_cache([L], k, 128, max_tokens=T)
+    y128 = _forward(cache, x_bits, logits, k)
+    cache.close()
+    assert torch.equal(y40.view(torch.int16), y128.view(torch.int16))
+    sample = np.random.default_rng(501).choice(T, size=16, replace=False)
+    ids, w = orouter.router_topk(logits[sample], k)
+    hz.assert_layer_close(hz.bf16_to_f64(y40)[sample], L.oracle_y(x_bits[sample], ids, w), 1)
