@@ -188,7 +188,7 @@ PMOE_API int expert_cache_host_store(pmoe_cache* cache, int layer, void** host_p
 PMOE_API int expert_cache_load_expert(pmoe_cache* cache, int layer, int expert, const void* bytes, size_t nbytes);
 
 /* Empty one layer's slot table (layer = -1: all layers); statistics are kept.
- * Stream-ordered on the cache's copy stream after the layer's last forward. */
+ * Stream-ordered after the layer's last forward and residency step. */
 PMOE_API int expert_cache_reset(pmoe_cache* cache, int layer);
 
 /*
@@ -225,6 +225,23 @@ PMOE_API int expert_cache_ensure_resident(pmoe_cache* cache, int layer, const in
  */
 PMOE_API int moe_paged_forward(pmoe_cache* cache, int layer, const void* x, int T, const int32_t* ids,
                       const float* w, const void* residual, void* y, void* stream);
+
+/*
+ * moe_paged_stack_forward — all num_layers MoE layers of the cache in sequence, attention
+ * omitted: h_0 = x, h_{l+1} = h_l + moe_l(h_l) (the residual add of a decoder block; a
+ * token at batch 1 activates layers x top_k experts, article "Running an MoE Model
+ * Larger Than Your VRAM", section "Why is it fast when experts keep crossing PCIe?").
+ * Each layer's residency step and page-in run on the cache's side streams while the
+ * previous layer computes on `stream` (prefetch overlap; the copy/compute overlap
+ * t ~ max(t_read, t_H2D)).
+ *   x     device bf16 [T][H] (h_0)             y     device bf16 [T][H] (h_L)
+ *   ids   device int32 [L][T][top_k]           w     device fp32 [L][T][top_k]
+ *   work  device bf16 [T][H] scratch for the alternating activations (may be NULL if L == 1)
+ * x, y and work must not overlap. The ids of every layer must be ready in stream order
+ * at the call. Results are those of L moe_paged_forward calls with residual = input.
+ */
+PMOE_API int moe_paged_stack_forward(pmoe_cache* cache, const void* x, int T, const int32_t* ids, const float* w,
+                                     void* y, void* work, void* stream);
 
 /* Counters of one layer (layer = -1: summed over layers). Synchronises the cache's
  * streams; returns PMOE_EDEVICE if a kernel recorded an error. */

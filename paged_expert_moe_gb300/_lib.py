@@ -68,6 +68,7 @@ _SIGS = {
     "expert_cache_set_timing": ([_P, _I], _I),
     "expert_cache_kernel_times": ([_P, ctypes.POINTER(pmoe_kernel_times)], _I),
     "moe_decode_forward_noalloc": ([_P, ctypes.c_size_t, _P, _I, _I, _I, _I, _I, _P, _I, _P, _P, _P, _P, _P], _I),
+    "moe_paged_stack_forward": ([_P, _P, _I, _P, _P, _P, _P, _P], _I),
 }
 EXPORTED = tuple(_SIGS)
 
@@ -203,6 +204,17 @@ class ExpertCache:
         assert x.dtype == torch.bfloat16 and ids.dtype == torch.int32 and w.dtype == torch.float32
         _check(load().moe_paged_forward(self.handle, layer, _ptr(x), T, _ptr(ids), _ptr(w), _ptr(residual), _ptr(y),
                                         _stream_handle(stream)), "moe_paged_forward")
+        return y
+
+    def moe_paged_stack_forward(self, x, ids_all, w_all, y=None, work=None, stream=None):
+        """All layers: h_{l+1} = h_l + moe_l(h_l). ids_all/w_all: [L, T, top_k] device."""
+        import torch
+        if y is None:
+            y = torch.empty_like(x)
+        if work is None and self.layers > 1:
+            work = torch.empty_like(x)
+        _check(load().moe_paged_stack_forward(self.handle, _ptr(x), x.shape[0], _ptr(ids_all), _ptr(w_all), _ptr(y),
+                                              _ptr(work), _stream_handle(stream)), "moe_paged_stack_forward")
         return y
 
     def expert_cache_stats(self, layer=-1):

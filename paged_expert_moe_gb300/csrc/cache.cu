@@ -101,6 +101,7 @@ struct pmoe_cache {
   int words = 0;
   bool use_tc = false;  // tensor-core prefill path available
   cudaStream_t copy_stream = nullptr;
+  cudaStream_t plan_stream = nullptr;  // residency kernels + plan read-back (copy-engine mode)
   std::vector<uint8_t*> host_store, host_store_dev, arena;
   std::vector<LayerState> st;
   std::vector<int32_t*> plan_dev;
@@ -110,7 +111,7 @@ struct pmoe_cache {
   int32_t* err_dev = nullptr;
   std::vector<cudaEvent_t> ev_plan, ev_layer_done, ev_ready;
   std::vector<int> staged, staged_waves, layer_used;
-  cudaEvent_t ev_ids = nullptr, ev_wave_done = nullptr;
+  cudaEvent_t ev_ids = nullptr, ev_wave_done = nullptr, ev_stack = nullptr;
   Workspace ws{};
   void* ws_buf = nullptr;
   std::vector<TcMaps> maps;  // per layer tensor maps (bf16 prefill path)
@@ -186,6 +187,7 @@ struct KernelMark {
 void free_cache(pmoe_cache* c) {
   if (c == nullptr) return;
   if (c->copy_stream) cudaStreamSynchronize(c->copy_stream);
+  if (c->plan_stream) cudaStreamSynchronize(c->plan_stream);
   for (cudaEvent_t e : c->ev_layer_done)
     if (e) cudaEventSynchronize(e);
   resolve_marks(c);
@@ -205,7 +207,9 @@ void free_cache(pmoe_cache* c) {
       if (e) cudaEventDestroy(e);
   if (c->ev_ids) cudaEventDestroy(c->ev_ids);
   if (c->ev_wave_done) cudaEventDestroy(c->ev_wave_done);
+  if (c->ev_stack) cudaEventDestroy(c->ev_stack);
   if (c->copy_stream) cudaStreamDestroy(c->copy_stream);
+  if (c->plan_stream) cudaStreamDestroy(c->plan_stream);
   delete c;
 }
 
@@ -341,8 +345,10 @@ int expert_cache_create(const pmoe_cache_desc* desc, pmoe_cache** out) {
     }                               \
   } while (0)
   PMOE_TRY(cudaStreamCreateWithFlags(&c->copy_stream, cudaStreamNonBlocking));
+  PMOE_TRY(cudaStreamCreateWithFlags(&c->plan_stream, cudaStreamNonBlocking));
   PMOE_TRY(cudaEventCreateWithFlags(&c->ev_ids, cudaEventDisableTiming));
   PMOE_TRY(cudaEventCreateWithFlags(&c->ev_wave_done, cudaEventDisableTiming));
+  PMOE_TRY(cudaEventCreateWithFlags(&c->ev_stack, cudaEventDisableTiming));
   for (int l = 0; l < Lr; ++l) {
     PMOE_TRY(cudaEventCreateWithFlags(&c->ev_plan[l], cudaEventDisableTiming));
     PMOE_TRY(cudaEventCreateWithFlags(&c->ev_layer_done[l], cudaEventDisableTiming));
@@ -498,17 +504,46 @@ int expert_cache_reset(pmoe_cache* c, int layer) {
       const int r = flush_staged(c, l);
       if (r != PMOE_OK) return r;
     }
-    PMOE_CUDA(cudaStreamWaitEvent(c->copy_stream, c->ev_layer_done[l], 0));
+    // the table is updated on the stream the residency kernels run on
+    cudaStream_t ps = c->d.pagein_mode == PMOE_PAGEIN_COPY_ENGINE ? c->plan_stream : c->copy_stream;
+    PMOE_CUDA(cudaStreamWaitEvent(ps, c->ev_layer_done[l], 0));
     const LayerState& s = c->st[l];
-    PMOE_CUDA(cudaMemsetAsync(s.slot_of, 0xFF, 4 * (size_t)c->d.num_experts, c->copy_stream));
-    PMOE_CUDA(cudaMemsetAsync(s.expert_in, 0xFF, 4 * (size_t)c->d.num_slots, c->copy_stream));
-    PMOE_CUDA(cudaMemsetAsync(s.last_use, 0xFF, 4 * (size_t)c->d.num_slots, c->copy_stream));
+    PMOE_CUDA(cudaMemsetAsync(s.slot_of, 0xFF, 4 * (size_t)c->d.num_experts, ps));
+    PMOE_CUDA(cudaMemsetAsync(s.expert_in, 0xFF, 4 * (size_t)c->d.num_slots, ps));
+    PMOE_CUDA(cudaMemsetAsync(s.last_use, 0xFF, 4 * (size_t)c->d.num_slots, ps));
   }
   return PMOE_OK;
 }
 
+}  // extern "C"
+
+namespace {
+
+// The residency step of `layer`, ordered after `ids_ready` (the ids' producer) and after
+// the layer's previous forward.
+int ensure_resident_impl(pmoe_cache* c, int layer, const int32_t* ids, int n_ids, cudaEvent_t ids_ready,
+                         int* waves_out);
+
+}  // namespace
+
+extern "C" {
+
 int expert_cache_ensure_resident(pmoe_cache* c, int layer, const int32_t* ids, int n_ids, void* stream,
                                  int* waves_out) {
+  if (c == nullptr || layer < 0 || layer >= c->d.num_layers || n_ids < 0 ||
+      n_ids > c->d.max_tokens * c->d.top_k || (n_ids > 0 && ids == nullptr))
+    return PMOE_EINVAL;
+  PMOE_CUDA(cudaSetDevice(c->d.device));
+  PMOE_CUDA(cudaEventRecord(c->ev_ids, (cudaStream_t)stream));
+  return ensure_resident_impl(c, layer, ids, n_ids, c->ev_ids, waves_out);
+}
+
+}  // extern "C"
+
+namespace {
+
+int ensure_resident_impl(pmoe_cache* c, int layer, const int32_t* ids, int n_ids, cudaEvent_t ids_ready,
+                         int* waves_out) {
   if (c == nullptr || layer < 0 || layer >= c->d.num_layers || n_ids < 0 ||
       n_ids > c->d.max_tokens * c->d.top_k || (n_ids > 0 && ids == nullptr))
     return PMOE_EINVAL;
@@ -517,22 +552,26 @@ int expert_cache_ensure_resident(pmoe_cache* c, int layer, const int32_t* ids, i
     const int r = flush_staged(c, layer);  // a previous staged step that was never consumed
     if (r != PMOE_OK) return r;
   }
-  cudaStream_t s = (cudaStream_t)stream;
-  PMOE_CUDA(cudaEventRecord(c->ev_ids, s));
-  PMOE_CUDA(cudaStreamWaitEvent(c->copy_stream, c->ev_ids, 0));
-  PMOE_CUDA(cudaStreamWaitEvent(c->copy_stream, c->ev_layer_done[layer], 0));
+  const bool ce = c->d.pagein_mode == PMOE_PAGEIN_COPY_ENGINE;
+  // copy-engine mode plans on its own stream, so planning the next layer never queues
+  // behind this layer's copies; SM-pull plans and pulls in one stream order
+  cudaStream_t ps = ce ? c->plan_stream : c->copy_stream;
+  PMOE_CUDA(cudaStreamWaitEvent(ps, ids_ready, 0));
+  PMOE_CUDA(cudaStreamWaitEvent(ps, c->ev_layer_done[layer], 0));
   {
-    KernelMark km(c, PMOE_K_RESIDENCY, c->copy_stream);
+    KernelMark km(c, PMOE_K_RESIDENCY, ps);
     PMOE_CUDA(launch_residency(ids, n_ids, c->d.num_experts, c->d.num_slots, c->st[layer], c->plan_dev[layer],
-                               c->err_dev, c->copy_stream));
+                               c->err_dev, ps));
   }
   c->layer_used[layer] = 1;
   int waves = -1;
   int status = PMOE_OK;
-  if (c->d.pagein_mode == PMOE_PAGEIN_COPY_ENGINE) {
-    PMOE_CUDA(cudaMemcpyAsync(c->plan_h(layer), c->plan_dev[layer], (size_t)c->words * 4, cudaMemcpyDeviceToHost,
-                              c->copy_stream));
-    PMOE_CUDA(cudaEventRecord(c->ev_plan[layer], c->copy_stream));
+  if (ce) {
+    PMOE_CUDA(cudaMemcpyAsync(c->plan_h(layer), c->plan_dev[layer], (size_t)c->words * 4, cudaMemcpyDeviceToHost, ps));
+    PMOE_CUDA(cudaEventRecord(c->ev_plan[layer], ps));
+    // the copies overwrite victim slots: they follow the plan (which followed this
+    // layer's previous forward)
+    PMOE_CUDA(cudaStreamWaitEvent(c->copy_stream, c->ev_plan[layer], 0));
     const int r = wait_event_bounded(c->ev_plan[layer]);
     if (r != PMOE_OK) return r;
     const int32_t* plan = c->plan_h(layer);
@@ -544,9 +583,9 @@ int expert_cache_ensure_resident(pmoe_cache* c, int layer, const int32_t* ids, i
         // the table already names experts whose bytes never arrived: empty it, so the
         // next step pages everything in again rather than computing with stale slots
         const LayerState& ls = c->st[layer];
-        cudaMemsetAsync(ls.slot_of, 0xFF, 4 * (size_t)c->d.num_experts, c->copy_stream);
-        cudaMemsetAsync(ls.expert_in, 0xFF, 4 * (size_t)c->d.num_slots, c->copy_stream);
-        cudaMemsetAsync(ls.last_use, 0xFF, 4 * (size_t)c->d.num_slots, c->copy_stream);
+        cudaMemsetAsync(ls.slot_of, 0xFF, 4 * (size_t)c->d.num_experts, ps);
+        cudaMemsetAsync(ls.expert_in, 0xFF, 4 * (size_t)c->d.num_slots, ps);
+        cudaMemsetAsync(ls.last_use, 0xFF, 4 * (size_t)c->d.num_slots, ps);
         return r2;
       }
     }
@@ -561,6 +600,10 @@ int expert_cache_ensure_resident(pmoe_cache* c, int layer, const int32_t* ids, i
   if (waves_out) *waves_out = waves;
   return status;
 }
+
+}  // namespace
+
+extern "C" {
 
 int moe_paged_forward(pmoe_cache* c, int layer, const void* x, int T, const int32_t* ids, const float* w,
                       const void* residual, void* y, void* stream) {
@@ -672,9 +715,49 @@ int moe_paged_forward(pmoe_cache* c, int layer, const void* x, int T, const int3
   return status;
 }
 
+int moe_paged_stack_forward(pmoe_cache* c, const void* x, int T, const int32_t* ids, const float* w, void* y,
+                            void* work, void* stream) {
+  if (c == nullptr || T < 0 || T > c->d.max_tokens) return PMOE_EINVAL;
+  if (T == 0) return PMOE_OK;
+  const int L = c->d.num_layers;
+  if (x == nullptr || ids == nullptr || w == nullptr || y == nullptr || x == y) return PMOE_EINVAL;
+  if (L > 1 && (work == nullptr || work == x || work == y)) return PMOE_EINVAL;
+  PMOE_CUDA(cudaSetDevice(c->d.device));
+  cudaStream_t s = (cudaStream_t)stream;
+  const int P = T * c->d.top_k;
+  const size_t act = (size_t)T * c->d.hidden * 2;
+  // every layer's ids are ready once the work already on `stream` is done
+  PMOE_CUDA(cudaEventRecord(c->ev_stack, s));
+  int status = PMOE_OK;
+  if (!c->staged[0]) {
+    const int r = ensure_resident_impl(c, 0, ids, P, c->ev_stack, nullptr);
+    if (r == PMOE_EDEVICE) status = r;
+    else if (r != PMOE_OK) return r;
+  }
+  const uint8_t* in = (const uint8_t*)x;
+  for (int l = 0; l < L; ++l) {
+    // h_{l+1} = h_l + moe_l(h_l); the buffers alternate so that the last layer writes y
+    uint8_t* out = (((L - 1 - l) & 1) == 0) ? (uint8_t*)y : (uint8_t*)work;
+    (void)act;
+    int r = moe_paged_forward(c, l, in, T, ids + (size_t)l * P, w + (size_t)l * P, in, out, stream);
+    if (r == PMOE_EDEVICE) status = r;
+    else if (r != PMOE_OK) return r;
+    if (l + 1 < L && !c->staged[l + 1]) {
+      // plan and page in layer l+1 while layer l computes (the host's plan read-back in
+      // copy-engine mode overlaps the kernels just enqueued)
+      r = ensure_resident_impl(c, l + 1, ids + (size_t)(l + 1) * P, P, c->ev_stack, nullptr);
+      if (r == PMOE_EDEVICE) status = r;
+      else if (r != PMOE_OK) return r;
+    }
+    in = out;
+  }
+  return status;
+}
+
 int expert_cache_stats(pmoe_cache* c, int layer, pmoe_stats* out) {
   if (c == nullptr || out == nullptr || layer < -1 || layer >= c->d.num_layers) return PMOE_EINVAL;
   PMOE_CUDA(cudaSetDevice(c->d.device));
+  PMOE_CUDA(cudaStreamSynchronize(c->plan_stream));
   PMOE_CUDA(cudaStreamSynchronize(c->copy_stream));
   for (int l = 0; l < c->d.num_layers; ++l) {
     const int r = wait_event_bounded(c->ev_layer_done[l]);
@@ -699,6 +782,7 @@ int expert_cache_stats(pmoe_cache* c, int layer, pmoe_stats* out) {
 int expert_cache_slot_table(pmoe_cache* c, int layer, int32_t* expert_in_slot, int32_t* last_use) {
   if (c == nullptr || layer < 0 || layer >= c->d.num_layers || expert_in_slot == nullptr) return PMOE_EINVAL;
   PMOE_CUDA(cudaSetDevice(c->d.device));
+  PMOE_CUDA(cudaStreamSynchronize(c->plan_stream));
   PMOE_CUDA(cudaStreamSynchronize(c->copy_stream));
   PMOE_CUDA(cudaMemcpy(expert_in_slot, c->st[layer].expert_in, 4 * (size_t)c->d.num_slots, cudaMemcpyDeviceToHost));
   if (last_use)

@@ -185,13 +185,17 @@ def fast_int4_expert_bytes(H, I, seed, layer=0, expert=0):
     return out
 
 
-def layer_store(fmt, H, I, E, seed, layer=0, fast=False, threads=None):
+def layer_store(fmt, H, I, E, seed, layer=0, fast=False, threads=None, out=None):
     """All E experts of one layer, [E, expert_nbytes] uint8 (experts drawn in parallel
-    threads; each expert's bytes depend only on its own seed)."""
+    threads; each expert's bytes depend only on its own seed). `out` may be a
+    preallocated [E, >= expert_nbytes] uint8 view (for instance a pinned store)."""
     import concurrent.futures
     import os
     nb = expert_nbytes(fmt, H, I)
-    out = np.empty((E, nb), dtype=np.uint8)
+    if out is None:
+        out = np.empty((E, nb), dtype=np.uint8)
+    else:
+        out = out[:, :nb]
 
     def fill(e):
         if fast and fmt == 2:
