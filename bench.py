@@ -361,6 +361,7 @@ def run_ours(args):
     clocks = clock.stop(*head["t_wall"]) if clock else None
     others = {}
     prefill = {}
+    stack = {}
     h2d = measure_h2d(torch, torch.device("cuda", local))
     if not args.headline_only:
         for B in (2, 4):
@@ -369,6 +370,7 @@ def run_ours(args):
         prefill["cold"] = run_prefill(pm, torch, store, args.prefill_steps, 2, local, cold=True)
         prefill["cold_sm_pull"] = run_prefill(pm, torch, store, args.prefill_steps, 2, local, cold=True, mode=1)
         prefill["warm_all_resident"] = run_prefill(pm, torch, store, args.prefill_steps, 2, local, K=E, cold=False)
+        stack = {f"B{B}": run_stack(pm, torch, B, args.stack_steps, 3, local) for B in (1, 4)}
     job_ms = reduce_max(head["total_ms"], ws, torch.device("cuda", local))
     value = ws * 1 * args.steps / (job_ms / 1e3)
     if rank != 0:
@@ -420,6 +422,10 @@ def run_ours(args):
                       "decode_pagein_gbs": (head["bytes_paged_per_step"] * args.steps /
                                             (kt["pagein_copy"]["ms"] / 1e3) / 1e9) if kt["pagein_copy"]["ms"] else None},
         "prefill": _prefill_summary(prefill, hbm_peak, _peaks()[1]) if prefill else None,
+        "stack_int4": ({"workload": "48-layer Qwen3-30B-A3B-shaped MoE stack (attention omitted), GPTQ-int4 g128 "
+                                    "experts, K=26 slots/layer, p=0.8 reuse routing per layer, residual stream",
+                        "hbm_roofline_tokens_per_s_B1": hbm_peak * 1e9 / (STACK_L * TOPK * 2_506_752),
+                        **stack} if stack else None),
         "e2e": head.get("e2e"),
         "gpu_launches": head["launches"],
         "clocks": clocks,
@@ -428,6 +434,68 @@ def run_ours(args):
     if not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline_decode(1, budget_s=args.cpu_budget, store=store)
     print(json.dumps(out))
+
+
+STACK_L, STACK_K = 48, 26
+
+
+def run_stack(pm, torch, B, steps, warmup, device, mode=0, layers=STACK_L, K=STACK_K):
+    """48-layer MoE stack, GPTQ-int4 experts, K=26 slots per layer, decode batch B, each
+    layer with its own p=0.8 reuse routing; h_{l+1} = h_l + moe_l(h_l) through
+    moe_paged_stack_forward (next layer's page-in overlapped with the current layer)."""
+    dev = torch.device("cuda", device)
+    cache = pm.ExpertCache(E, TOPK, H, I, K, num_layers=layers, fmt=pm.PMOE_INT4_GPTQ_G128, max_tokens=B,
+                           device=device, pagein_mode=mode)
+    for l in range(layers):
+        gen.layer_store(2, H, I, E, SEED, layer=l, fast=True, out=cache.host_store(l))
+    rng = np.random.default_rng([SEED, 48, B])
+    traces = [gen.reuse_routing_trace(rng, E, TOPK, B, TRACE_STEPS) for _ in range(layers)]
+    n_inputs = min(TRACE_STEPS, warmup + steps)
+    logits = [torch.from_numpy(np.concatenate([gen.logits_for_sets(rng, traces[l][s], E) for l in range(layers)])).to(dev)
+              for s in range(n_inputs)]
+    xs = [torch.from_numpy(gen.activations_bf16(rng, B, H).view(np.int16)).view(torch.bfloat16).to(dev)
+          for _ in range(n_inputs)]
+    distinct = [sum(len({e for st in traces[l][s] for e in st}) for l in range(layers)) for s in range(n_inputs)]
+    ids = torch.empty((layers * B, TOPK), dtype=torch.int32, device=dev)
+    w = torch.empty((layers * B, TOPK), dtype=torch.float32, device=dev)
+    y = torch.empty((B, H), dtype=torch.bfloat16, device=dev)
+    work = torch.empty((B, H), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def one(s):
+        pm.moe_router_topk(logits[s], TOPK, ids_out=ids, w_out=w)
+        cache.moe_paged_stack_forward(xs[s], ids, w, y=y, work=work)
+
+    for i in range(warmup):
+        one(i % n_inputs)
+    torch.cuda.synchronize(dev)
+    s0 = cache.expert_cache_stats(-1)
+    cache.expert_cache_set_timing(True)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    ids_used = [(warmup + i) % n_inputs for i in range(steps)]
+    for i, si in enumerate(ids_used):
+        flush.zero_()
+        evs[i][0].record(stream)
+        one(si)
+        evs[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    total_ms = float(sum(a.elapsed_time(b) for a, b in evs))
+    kt = cache.expert_cache_kernel_times()
+    s1 = cache.expert_cache_stats(-1)
+    cache.close()
+    nb = pm.pmoe_expert_bytes(pm.PMOE_INT4_GPTQ_G128, H, I)
+    wbytes = sum(distinct[si] for si in ids_used) * nb
+    dec_ms = kt["decode"]["ms"]
+    return {"B": B, "layers": layers, "K": K, "steps": steps, "ms_per_step": total_ms / steps,
+            "tokens_per_s": B * steps / (total_ms / 1e3),
+            "misses_per_token": (s1["misses"] - s0["misses"]) / (steps * B),
+            "waves_per_layer_step": (s1["waves"] - s0["waves"]) / (steps * layers),
+            "pagein_gb_per_step": (s1["bytes_paged"] - s0["bytes_paged"]) / steps / 1e9,
+            "expert_weight_gb_per_step": wbytes / steps / 1e9,
+            "decode_kernel_gbs": wbytes / (dec_ms / 1e3) / 1e9 if dec_ms else None,
+            "kernel_ms_per_step": {k_: v["ms"] / steps for k_, v in kt.items() if k_ != "copies" and v["ms"]},
+            "hbm_roofline_tokens_per_s_before_misses": None}
 
 
 def _prefill_summary(prefill, hbm_peak, tc_peak):
@@ -503,6 +571,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--prefill-steps", type=int, default=6)
+    ap.add_argument("--stack-steps", type=int, default=60)
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

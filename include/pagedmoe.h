@@ -222,6 +222,11 @@ PMOE_API int expert_cache_ensure_resident(pmoe_cache* cache, int layer, const in
  * If no ensure_resident was staged for `layer`, the call runs it first. Waves run
  * in order, each after its own page-in. T in 0..max_tokens. Calls on one cache
  * share its workspace: issue them on one stream (or serialise them).
+ * CUDA graphs: with PMOE_PAGEIN_SM_PULL no call waits on the host, so ensure_resident,
+ * moe_paged_forward and moe_paged_stack_forward can be recorded by stream capture and
+ * replayed (the single-wave decode step of section "What happens with more than one
+ * request?"); a copy-engine cache returns PMOE_EUNSUPPORTED under capture. Synchronise
+ * the replay stream before reading statistics or the slot table.
  */
 PMOE_API int moe_paged_forward(pmoe_cache* cache, int layer, const void* x, int T, const int32_t* ids,
                       const float* w, const void* residual, void* y, void* stream);

@@ -35,6 +35,7 @@ thread_local char g_last_error[256] = "";
 
 void set_cuda_error(cudaError_t e, const char* what) {
   snprintf(g_last_error, sizeof(g_last_error), "%s: %s", what, cudaGetErrorString(e));
+  cudaGetLastError();  // a non-sticky error must not resurface at the next launch check
 }
 
 #define PMOE_CUDA(call)                                   \
@@ -81,6 +82,15 @@ int wait_event_bounded(cudaEvent_t ev) {
 
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
+bool stream_capturing(cudaStream_t s) {
+  cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &st) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return st == cudaStreamCaptureStatusActive;
+}
+
 int validate_shape(int fmt, int H, int I) {
   if (H <= 0 || I <= 0 || H % 8 != 0 || I % 8 != 0) return PMOE_EINVAL;
   if (fmt != PMOE_BF16 && fmt != PMOE_FP8_BLOCK128 && fmt != PMOE_INT4_GPTQ_G128) return PMOE_EUNSUPPORTED;
@@ -118,6 +128,7 @@ struct pmoe_cache {
   TcMaps ws_maps{};
   // per-kernel timers
   bool timing = false;
+  bool in_capture = false;  // the current call is being recorded into a CUDA graph
   struct Mark {
     int cls;
     cudaEvent_t a, b;
@@ -165,7 +176,7 @@ struct KernelMark {
   cudaEvent_t a = nullptr;
   KernelMark(pmoe_cache* c_, int cls_, cudaStream_t s_) : c(c_), cls(cls_), s(s_) {
     c->launches[cls] += 1;
-    if (c->timing) {
+    if (c->timing && !c->in_capture) {
       if (c->marks.size() >= 2048) resolve_marks(c);
       a = pool_get(c);
       if (a) cudaEventRecord(a, s);
@@ -247,7 +258,7 @@ int flush_staged(pmoe_cache* c, int layer) {
                                   c->expert_bytes, c->arena[layer], c->err_dev, c->copy_stream));
     }
   }
-  PMOE_CUDA(cudaEventRecord(c->ev_layer_done[layer], c->copy_stream));
+  if (!c->in_capture) PMOE_CUDA(cudaEventRecord(c->ev_layer_done[layer], c->copy_stream));
   return PMOE_OK;
 }
 
@@ -534,6 +545,7 @@ int expert_cache_ensure_resident(pmoe_cache* c, int layer, const int32_t* ids, i
       n_ids > c->d.max_tokens * c->d.top_k || (n_ids > 0 && ids == nullptr))
     return PMOE_EINVAL;
   PMOE_CUDA(cudaSetDevice(c->d.device));
+  c->in_capture = stream_capturing((cudaStream_t)stream);
   PMOE_CUDA(cudaEventRecord(c->ev_ids, (cudaStream_t)stream));
   return ensure_resident_impl(c, layer, ids, n_ids, c->ev_ids, waves_out);
 }
@@ -556,8 +568,14 @@ int ensure_resident_impl(pmoe_cache* c, int layer, const int32_t* ids, int n_ids
   // copy-engine mode plans on its own stream, so planning the next layer never queues
   // behind this layer's copies; SM-pull plans and pulls in one stream order
   cudaStream_t ps = ce ? c->plan_stream : c->copy_stream;
+  if (c->in_capture && ce) {
+    snprintf(g_last_error, sizeof(g_last_error),
+             "graph capture needs PMOE_PAGEIN_SM_PULL (copy-engine page-in reads the plan on the host)");
+    return PMOE_EUNSUPPORTED;
+  }
   PMOE_CUDA(cudaStreamWaitEvent(ps, ids_ready, 0));
-  PMOE_CUDA(cudaStreamWaitEvent(ps, c->ev_layer_done[layer], 0));
+  // inside a captured graph the layer's previous forward precedes this step by graph order
+  if (!c->in_capture) PMOE_CUDA(cudaStreamWaitEvent(ps, c->ev_layer_done[layer], 0));
   {
     KernelMark km(c, PMOE_K_RESIDENCY, ps);
     PMOE_CUDA(launch_residency(ids, n_ids, c->d.num_experts, c->d.num_slots, c->st[layer], c->plan_dev[layer],
@@ -613,6 +631,7 @@ int moe_paged_forward(pmoe_cache* c, int layer, const void* x, int T, const int3
   if (T > kGemvMaxTokens && !c->use_tc) return PMOE_EUNSUPPORTED;
   PMOE_CUDA(cudaSetDevice(c->d.device));
   cudaStream_t s = (cudaStream_t)stream;
+  c->in_capture = stream_capturing(s);
   const int k = c->d.top_k, P = T * k, E = c->d.num_experts, H = c->d.hidden, I = c->d.intermediate;
   int status = PMOE_OK;
   if (!c->staged[layer]) {
@@ -711,7 +730,9 @@ int moe_paged_forward(pmoe_cache* c, int layer, const void* x, int T, const int3
     PMOE_CUDA(launch_combine(c->ws, w, (const __nv_bfloat16*)residual, (__nv_bfloat16*)y, T, k, H, s,
                              (fused && !ce) ? c->plan_dev[layer] : nullptr));
   }
-  PMOE_CUDA(cudaEventRecord(c->ev_layer_done[layer], s));
+  // (under graph capture the graph's own order takes this event's place, and an event
+  // recorded into a graph could not be waited on or queried outside it)
+  if (!c->in_capture) PMOE_CUDA(cudaEventRecord(c->ev_layer_done[layer], s));
   return status;
 }
 
@@ -724,6 +745,7 @@ int moe_paged_stack_forward(pmoe_cache* c, const void* x, int T, const int32_t* 
   if (L > 1 && (work == nullptr || work == x || work == y)) return PMOE_EINVAL;
   PMOE_CUDA(cudaSetDevice(c->d.device));
   cudaStream_t s = (cudaStream_t)stream;
+  c->in_capture = stream_capturing(s);
   const int P = T * c->d.top_k;
   const size_t act = (size_t)T * c->d.hidden * 2;
   // every layer's ids are ready once the work already on `stream` is done

@@ -486,8 +486,19 @@ cudaError_t launch_df(const DfArgs& a, int grid, size_t smem, cudaStream_t s) {
   auto k = decode_fused_kernel<FMT, NCH1, NCH2>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  void* args[] = {(void*)&a};
-  return cudaLaunchCooperativeKernel((void*)k, dim3(grid), dim3(kDfThreads), args, smem, s);
+  // cooperative (all CTAs co-resident), launched through cudaLaunchKernelEx so that the
+  // launch can also be recorded into a CUDA graph
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kDfThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, a);
 }
 
 size_t fmt_row_bytes(int fmt, int n) {
