@@ -162,8 +162,9 @@ def aggregate(units_per_rank, time_s_per_rank):
 
 # --------------------------------------------------------------------------- our arm
 
-def run_decode(pm, torch, store, B, steps, warmup, device, timed_clock=None, e2e=True, mode=0):
+def run_decode(pm, torch, store, B, steps, warmup, device, timed_clock=None, e2e=True, mode=0, graph=False):
     trace, xs, logits, distinct = make_inputs(B)
+    graph_launches = 0
     cache = pm.ExpertCache(E, TOPK, H, I, K_SLOTS, fmt=pm.PMOE_BF16, max_tokens=B, device=device, pagein_mode=mode)
     cache.load_layer(0, store)
     dev = torch.device("cuda", device)
@@ -175,15 +176,37 @@ def run_decode(pm, torch, store, B, steps, warmup, device, timed_clock=None, e2e
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def one(s):
-        pm.moe_router_topk(l_dev[s], TOPK, ids_out=ids, w_out=w)
-        cache.moe_paged_forward(0, x_dev[s], ids, w, y=y)
+    if graph:
+        # the whole step (router, residency, SM-pull page-in, fused MoE) as one CUDA graph
+        # over static buffers; each step first copies its inputs into them (device to device)
+        x_s = torch.empty((B, H), dtype=torch.bfloat16, device=dev)
+        l_s = torch.empty((B, E), dtype=torch.float32, device=dev)
+        for i in range(2):
+            pm.moe_router_topk(l_dev[i], TOPK, ids_out=ids, w_out=w)
+            cache.moe_paged_forward(0, x_dev[i], ids, w, y=y)
+        torch.cuda.synchronize(dev)
+        cache.expert_cache_set_timing(False)  # resets the launch counters
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            pm.moe_router_topk(l_s, TOPK, ids_out=ids, w_out=w)
+            cache.moe_paged_forward(0, x_s, ids, w, y=y)
+        graph_launches = sum(v["launches"] for k_, v in cache.expert_cache_kernel_times().items()
+                             if k_ not in ("copies", "pagein_copy")) + 1  # + the router
+
+        def one(s):
+            x_s.copy_(x_dev[s])
+            l_s.copy_(l_dev[s])
+            g.replay()
+    else:
+        def one(s):
+            pm.moe_router_topk(l_dev[s], TOPK, ids_out=ids, w_out=w)
+            cache.moe_paged_forward(0, x_dev[s], ids, w, y=y)
 
     for i in range(warmup):
         one(i % TRACE_STEPS)
     torch.cuda.synchronize(dev)
     stats0 = cache.expert_cache_stats(0)
-    cache.expert_cache_set_timing(True)
+    cache.expert_cache_set_timing(not graph)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     step_ids = [(warmup + i) % TRACE_STEPS for i in range(steps)]
     torch.cuda.synchronize(dev)
@@ -212,7 +235,10 @@ def run_decode(pm, torch, store, B, steps, warmup, device, timed_clock=None, e2e
         "gateup_weight_bytes": sum(d * 2 * I * H * 2 for d in d_steps),
         "down_weight_bytes": sum(d * H * I * 2 for d in d_steps),
         "expert_weight_bytes": sum(d * 3 * I * H * 2 for d in d_steps),
-        "launches": sum(v["launches"] for k_, v in kt.items() if k_ not in ("copies", "pagein_copy")) + steps,
+        "launches": (graph_launches * steps if graph else
+                     sum(v["launches"] for k_, v in kt.items() if k_ not in ("copies", "pagein_copy")) + steps),
+        "mode": ("SM-pull page-in, whole step replayed as one CUDA graph" if graph else
+                 ("SM-pull page-in" if mode == 1 else "copy-engine page-in (host reads the plan)")),
     }
     cache.expert_cache_set_timing(False)
     if e2e:
@@ -220,16 +246,19 @@ def run_decode(pm, torch, store, B, steps, warmup, device, timed_clock=None, e2e
         x_h = [torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory() for x in xs]
         l_h = [torch.from_numpy(l).pin_memory() for l in logits]
         y_h = torch.empty((B, H), dtype=torch.bfloat16).pin_memory()
-        x_d = torch.empty((B, H), dtype=torch.bfloat16, device=dev)
-        l_d = torch.empty((B, E), dtype=torch.float32, device=dev)
+        x_d = x_s if graph else torch.empty((B, H), dtype=torch.bfloat16, device=dev)
+        l_d = l_s if graph else torch.empty((B, E), dtype=torch.float32, device=dev)
         evs2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
         for i, s in enumerate(step_ids):
             flush.zero_()
             evs2[i][0].record(stream)
             x_d.copy_(x_h[s], non_blocking=True)
             l_d.copy_(l_h[s], non_blocking=True)
-            pm.moe_router_topk(l_d, TOPK, ids_out=ids, w_out=w)
-            cache.moe_paged_forward(0, x_d, ids, w, y=y)
+            if graph:
+                g.replay()
+            else:
+                pm.moe_router_topk(l_d, TOPK, ids_out=ids, w_out=w)
+                cache.moe_paged_forward(0, x_d, ids, w, y=y)
             y_h.copy_(y, non_blocking=True)
             evs2[i][1].record(stream)
         torch.cuda.synchronize(dev)
@@ -355,30 +384,38 @@ def run_ours(args):
     torch.cuda.synchronize()
     clock = ClockSampler(local).start() if rank == 0 else None
     time.sleep(0.3)
-    head = run_decode(pm, torch, store, 1, args.steps, args.warmup, local)
+    head = run_decode(pm, torch, store, 1, args.steps, args.warmup, local, mode=1, graph=True)
     torch.cuda.synchronize()
     barrier(ws)
     clocks = clock.stop(*head["t_wall"]) if clock else None
+    # the same workload without the graph, with per-kernel CUDA-event timers on the
+    # kernels' own streams: the decode kernel's duration for the roofline
+    timed = run_decode(pm, torch, store, 1, args.steps, args.warmup, local, e2e=False, mode=1)
     others = {}
     prefill = {}
     stack = {}
     h2d = measure_h2d(torch, torch.device("cuda", local))
     if not args.headline_only:
+        others["B1_sm_pull_no_graph"] = timed
+        others["B1_copy_engine"] = run_decode(pm, torch, store, 1, args.steps, args.warmup, local, e2e=False)
         for B in (2, 4):
+            others[f"B{B}_graph"] = run_decode(pm, torch, store, B, args.steps, args.warmup, local, e2e=False,
+                                               mode=1, graph=True)
             others[B] = run_decode(pm, torch, store, B, args.steps, args.warmup, local, e2e=False)
-        others["B1_sm_pull"] = run_decode(pm, torch, store, 1, args.steps, args.warmup, local, e2e=False, mode=1)
         prefill["cold"] = run_prefill(pm, torch, store, args.prefill_steps, 2, local, cold=True)
         prefill["cold_sm_pull"] = run_prefill(pm, torch, store, args.prefill_steps, 2, local, cold=True, mode=1)
         prefill["warm_all_resident"] = run_prefill(pm, torch, store, args.prefill_steps, 2, local, K=E, cold=False)
-        stack = {f"B{B}": run_stack(pm, torch, B, args.stack_steps, 3, local) for B in (1, 4)}
+        for B in (1, 4):
+            stack[f"B{B}"] = run_stack(pm, torch, B, args.stack_steps, 3, local)
+            stack[f"B{B}_graph"] = run_stack(pm, torch, B, args.stack_steps, 3, local, mode=1, graph=True)
     job_ms = reduce_max(head["total_ms"], ws, torch.device("cuda", local))
     value = ws * 1 * args.steps / (job_ms / 1e3)
     if rank != 0:
         return
-    kt = head["kernel_times"]
+    kt = timed["kernel_times"]
     dec_ms = kt["decode"]["ms"]
     dec_launch = max(1, kt["decode"]["launches"])
-    achieved = head["expert_weight_bytes"] / (dec_ms / 1e3) / 1e9
+    achieved = timed["expert_weight_bytes"] / (dec_ms / 1e3) / 1e9
     layer_gbs = achieved
     traffic = None
     tp = os.path.join(ROOT, "profiles", "traffic.json")
@@ -394,7 +431,7 @@ def run_ours(args):
         "config": {"workload": "Qwen3-30B-A3B-shaped MoE layer, bf16 experts, decode B=1, K=40 slots, "
                                "256-step p=0.8 reuse routing trace",
                    "E": E, "top_k": TOPK, "hidden": H, "intermediate": I, "K": K_SLOTS, "batch": 1,
-                   "pagein": "copy engine (cudaMemcpyAsync from pinned host store)",
+                   "pagein": "SM pull from the mapped pinned host store; the step replayed as one CUDA graph",
                    "l2": "flushed before every timed step (256 MB write, outside the events)",
                    "parallelism": f"replicas x{ws}"},
         "expert_weight_hbm_gbs": layer_gbs,
@@ -404,14 +441,16 @@ def run_ours(args):
                      "peak": hbm_peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / hbm_peak,
                      "traffic": traffic,
                      "avg_launch_us": dec_ms / dec_launch * 1e3,
-                     "algorithmic_bytes_per_launch": head["expert_weight_bytes"] / dec_launch,
+                     "algorithmic_bytes_per_launch": timed["expert_weight_bytes"] / dec_launch,
+                     "measured_in": "the same workload run without the graph (per-kernel CUDA events)",
                      "algorithmic_bytes_note": "distinct routed experts x 3*H*I*2 bytes (gate, up, down weights)"},
         "layer": {"misses_per_step": head["misses_per_step"], "hit_rate": head["hit_rate"],
                   "waves_per_step": head["waves_per_step"], "distinct_experts_per_step": head["distinct_per_step"],
                   "bytes_paged_per_step": head["bytes_paged_per_step"],
-                  "kernel_ms_per_step": {k_: v["ms"] / args.steps for k_, v in kt.items() if k_ != "copies"},
-                  "copies_per_step": kt["copies"] / args.steps},
-        "batches": {(f"B{B}" if isinstance(B, int) else B): {"tokens_per_s": r["tokens_per_s"], "ms_per_step": r["ms_per_step"],
+                  "kernel_ms_per_step_without_graph": {k_: v["ms"] / args.steps for k_, v in kt.items()
+                                                       if k_ != "copies" and v["ms"]}},
+        "batches": {(f"B{B}" if isinstance(B, int) else B): {"mode": r["mode"], "tokens_per_s": r["tokens_per_s"],
+                              "ms_per_step": r["ms_per_step"],
                               "misses_per_step": r["misses_per_step"], "waves_per_step": r["waves_per_step"],
                               "decode_kernel_gbs": r["expert_weight_bytes"] /
                               (r["kernel_times"]["decode"]["ms"] / 1e3) / 1e9 if r["kernel_times"]["decode"]["ms"] else None,
@@ -419,8 +458,9 @@ def run_ours(args):
                                                      if k_ != "copies" and v["ms"]}}
                     for B, r in others.items()},
         "host_link": {"pinned_h2d_gbs": h2d, "chunk_bytes": 9_437_184,
-                      "decode_pagein_gbs": (head["bytes_paged_per_step"] * args.steps /
-                                            (kt["pagein_copy"]["ms"] / 1e3) / 1e9) if kt["pagein_copy"]["ms"] else None},
+                      "decode_pagein_gbs": (timed["bytes_paged_per_step"] * args.steps /
+                                            (kt["pull"]["ms"] / 1e3) / 1e9) if kt["pull"]["ms"] else None,
+                      "decode_pagein_kind": "SM pull kernel (CUDA-event time on the copy stream)"},
         "prefill": _prefill_summary(prefill, hbm_peak, _peaks()[1]) if prefill else None,
         "stack_int4": ({"workload": "48-layer Qwen3-30B-A3B-shaped MoE stack (attention omitted), GPTQ-int4 g128 "
                                     "experts, K=26 slots/layer, p=0.8 reuse routing per layer, residual stream",
@@ -439,7 +479,7 @@ def run_ours(args):
 STACK_L, STACK_K = 48, 26
 
 
-def run_stack(pm, torch, B, steps, warmup, device, mode=0, layers=STACK_L, K=STACK_K):
+def run_stack(pm, torch, B, steps, warmup, device, mode=0, layers=STACK_L, K=STACK_K, graph=False):
     """48-layer MoE stack, GPTQ-int4 experts, K=26 slots per layer, decode batch B, each
     layer with its own p=0.8 reuse routing; h_{l+1} = h_l + moe_l(h_l) through
     moe_paged_stack_forward (next layer's page-in overlapped with the current layer)."""
@@ -463,15 +503,31 @@ def run_stack(pm, torch, B, steps, warmup, device, mode=0, layers=STACK_L, K=STA
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def one(s):
-        pm.moe_router_topk(logits[s], TOPK, ids_out=ids, w_out=w)
-        cache.moe_paged_stack_forward(xs[s], ids, w, y=y, work=work)
+    if graph:
+        x_s = torch.empty((B, H), dtype=torch.bfloat16, device=dev)
+        l_s = torch.empty((layers * B, E), dtype=torch.float32, device=dev)
+        pm.moe_router_topk(logits[0], TOPK, ids_out=ids, w_out=w)
+        cache.moe_paged_stack_forward(xs[0], ids, w, y=y, work=work)
+        torch.cuda.synchronize(dev)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            pm.moe_router_topk(l_s, TOPK, ids_out=ids, w_out=w)
+            cache.moe_paged_stack_forward(x_s, ids, w, y=y, work=work)
+
+        def one(s):
+            x_s.copy_(xs[s])
+            l_s.copy_(logits[s])
+            g.replay()
+    else:
+        def one(s):
+            pm.moe_router_topk(logits[s], TOPK, ids_out=ids, w_out=w)
+            cache.moe_paged_stack_forward(xs[s], ids, w, y=y, work=work)
 
     for i in range(warmup):
         one(i % n_inputs)
     torch.cuda.synchronize(dev)
     s0 = cache.expert_cache_stats(-1)
-    cache.expert_cache_set_timing(True)
+    cache.expert_cache_set_timing(not graph)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     ids_used = [(warmup + i) % n_inputs for i in range(steps)]
     for i, si in enumerate(ids_used):
@@ -488,14 +544,14 @@ def run_stack(pm, torch, B, steps, warmup, device, mode=0, layers=STACK_L, K=STA
     wbytes = sum(distinct[si] for si in ids_used) * nb
     dec_ms = kt["decode"]["ms"]
     return {"B": B, "layers": layers, "K": K, "steps": steps, "ms_per_step": total_ms / steps,
+            "mode": ("SM-pull, CUDA graph" if graph else ("SM-pull" if mode == 1 else "copy engine")),
             "tokens_per_s": B * steps / (total_ms / 1e3),
             "misses_per_token": (s1["misses"] - s0["misses"]) / (steps * B),
             "waves_per_layer_step": (s1["waves"] - s0["waves"]) / (steps * layers),
             "pagein_gb_per_step": (s1["bytes_paged"] - s0["bytes_paged"]) / steps / 1e9,
             "expert_weight_gb_per_step": wbytes / steps / 1e9,
             "decode_kernel_gbs": wbytes / (dec_ms / 1e3) / 1e9 if dec_ms else None,
-            "kernel_ms_per_step": {k_: v["ms"] / steps for k_, v in kt.items() if k_ != "copies" and v["ms"]},
-            "hbm_roofline_tokens_per_s_before_misses": None}
+            "kernel_ms_per_step": {k_: v["ms"] / steps for k_, v in kt.items() if k_ != "copies" and v["ms"]}}
 
 
 def _prefill_summary(prefill, hbm_peak, tc_peak):

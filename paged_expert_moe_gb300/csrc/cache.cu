@@ -608,6 +608,9 @@ int ensure_resident_impl(pmoe_cache* c, int layer, const int32_t* ids, int n_ids
       }
     }
   } else {
+    // the plan is on the device now: compute on the resident experts may start while the
+    // pull kernel brings the missing ones
+    PMOE_CUDA(cudaEventRecord(c->ev_plan[layer], c->copy_stream));
     KernelMark km(c, PMOE_K_PULL, c->copy_stream);
     PMOE_CUDA(launch_pull_pages(c->plan_dev[layer], c->d.num_experts, 0, c->host_store_dev[layer], c->stride,
                                 c->expert_bytes, c->arena[layer], c->err_dev, c->copy_stream));
@@ -646,6 +649,8 @@ int moe_paged_forward(pmoe_cache* c, int layer, const void* x, int T, const int3
   const bool ce = c->d.pagein_mode == PMOE_PAGEIN_COPY_ENGINE;
   // Copy-engine steps whose first wave has both resident and paged-in experts compute
   // the resident ones while the copies are still in flight (the plan lists them first).
+  // (SM-pull mode: the host does not know the split, and launching both parts
+  // unconditionally cost more than the overlap gained, so the wave runs whole.)
   bool split0 = false;
   if (ce && (tc || fused) && nw > 0) {
     const int32_t* plan = c->plan_h(layer);
@@ -655,7 +660,7 @@ int moe_paged_forward(pmoe_cache* c, int layer, const void* x, int T, const int3
     split0 = hits0 > 0 && hits0 < size0;
   }
   // the fused decode kernel forms y itself when the step has a single unsplit wave
-  const int fuse_combine = fused ? (ce ? ((nw == 1 && !split0) ? 1 : 0) : 1) : 0;
+  const int fuse_combine = (fused && !split0) ? (ce ? (nw == 1 ? 1 : 0) : 1) : 0;
   const bool need_combine = !fused || nw > 1 || split0;
 
   auto compute = [&](int wv, int sub) -> int {
@@ -728,7 +733,7 @@ int moe_paged_forward(pmoe_cache* c, int layer, const void* x, int T, const int3
     // turned out to have one wave (the fused kernel then already wrote y)
     KernelMark km(c, PMOE_K_COMBINE, s);
     PMOE_CUDA(launch_combine(c->ws, w, (const __nv_bfloat16*)residual, (__nv_bfloat16*)y, T, k, H, s,
-                             (fused && !ce) ? c->plan_dev[layer] : nullptr));
+                             (fused && !ce && !split0) ? c->plan_dev[layer] : nullptr));
   }
   // (under graph capture the graph's own order takes this event's place, and an event
   // recorded into a graph could not be waited on or queried outside it)

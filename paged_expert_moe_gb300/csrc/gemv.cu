@@ -200,7 +200,7 @@ __global__ void __launch_bounds__(256) pull_pages_kernel(const int32_t* __restri
   const size_t vec_per = stride / 16;
   const size_t total = (size_t)(m1 - m0) * vec_per;
   const size_t nthreads = (size_t)gridDim.x * blockDim.x;
-  constexpr int U = 4;
+  constexpr int U = 8;
   for (size_t base = (size_t)blockIdx.x * blockDim.x + threadIdx.x; base < total; base += nthreads * U) {
     uint4 v[U];
     size_t idx[U];
@@ -328,10 +328,13 @@ cudaError_t launch_pull_pages(const int32_t* plan, int E, int wave, const uint8_
                               size_t expert_bytes, uint8_t* arena, int32_t* err, cudaStream_t s) {
   (void)expert_bytes;
   (void)err;
+  // at most one small CTA per SM on half of the SMs: the pull then leaves room for the
+  // (cooperative, one CTA per SM) decode kernel to run beside it, and 8 x 16-byte loads
+  // per thread keep ~2 MB in flight over the host link
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  pull_pages_kernel<<<sms * 2, 256, 0, s>>>(plan, E, wave, host_store_dev, stride, arena);
+  pull_pages_kernel<<<sms / 2, 256, 0, s>>>(plan, E, wave, host_store_dev, stride, arena);
   return cudaGetLastError();
 }
 
