@@ -375,6 +375,7 @@ __global__ void __launch_bounds__(kDfThreads, 1) decode_fused_kernel(const DfArg
       if (group_bar_or(grp, got ? 0 : 1)) break;
       if (k == 0 && lane == 0) DF_TRACE(2);
       if (k == ch.n1 && lane == 0) DF_TRACE(3);
+      if (k == ch.n1 - 1 && lane == 0) DF_TRACE(6);  // wait for this CTA's last phase-1 chunk
       const int4 cd = chunks[k];
       const int4 we = s_we[cd.y];
       const uint8_t* ex = a.arena + (size_t)we.y * a.stride;

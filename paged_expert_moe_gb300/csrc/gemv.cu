@@ -331,6 +331,14 @@ cudaError_t launch_pull_pages(const int32_t* plan, int E, int wave, const uint8_
   // at most one small CTA per SM on half of the SMs: the pull then leaves room for the
   // (cooperative, one CTA per SM) decode kernel to run beside it, and 8 x 16-byte loads
   // per thread keep ~2 MB in flight over the host link
+  // The SMs it runs on keep the largest shared-memory carveout, so a decode CTA (which
+  // needs most of the shared memory) can be placed beside a pull CTA.
+  static bool carveout_set = false;
+  if (!carveout_set) {
+    cudaFuncSetAttribute(pull_pages_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                         (int)cudaSharedmemCarveoutMaxShared);
+    carveout_set = true;
+  }
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);

@@ -175,6 +175,12 @@ __global__ void __launch_bounds__(kThreads) residency_kernel(const int32_t* __re
 
 cudaError_t launch_residency(const int32_t* ids, int n_ids, int E, int K, LayerState st, int32_t* plan,
                              int32_t* err, cudaStream_t s) {
+  static bool carveout_set = false;  // keep room for a decode CTA on the same SM
+  if (!carveout_set) {
+    cudaFuncSetAttribute(residency_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                         (int)cudaSharedmemCarveoutMaxShared);
+    carveout_set = true;
+  }
   residency_kernel<<<1, kThreads, 0, s>>>(ids, n_ids, E, K, st, plan, err);
   return cudaGetLastError();
 }
