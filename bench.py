@@ -380,6 +380,20 @@ def run_ours(args):
     pm.load()
     store = make_store()
     hbm_peak, _, peak_kind = _peaks()
+    if args.section in ("prefill", "stack"):
+        # one part of the bench alone (for profiling); one JSON line with that part
+        out = {"metric": METRIC, "impl": "ours", "section": args.section}
+        if args.section == "prefill":
+            out["prefill"] = _prefill_summary(
+                {"cold": run_prefill(pm, torch, store, args.prefill_steps, 2, local, cold=True),
+                 "warm_all_resident": run_prefill(pm, torch, store, args.prefill_steps, 2, local, K=E, cold=False)},
+                hbm_peak, _peaks()[1])
+        else:
+            out["stack_int4"] = {f"B{B}_graph": run_stack(pm, torch, B, args.stack_steps, 3, local, mode=1, graph=True)
+                                 for B in (1, 4)}
+        if rank == 0:
+            print(json.dumps(out))
+        return
     barrier(ws)
     torch.cuda.synchronize()
     clock = ClockSampler(local).start() if rank == 0 else None
@@ -628,6 +642,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--prefill-steps", type=int, default=6)
     ap.add_argument("--stack-steps", type=int, default=60)
+    ap.add_argument("--section", default="all", choices=["all", "prefill", "stack"],
+                    help="run only one part (profiling); the default runs everything")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
