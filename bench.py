@@ -9,8 +9,10 @@ weighted combine. B=2 and B=4 are reported alongside under "batches".
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-Timing: W untimed warm-up steps, then K timed steps; L2 is flushed (256 MB write)
-before every timed step, outside the events; each step is bracketed by CUDA events
+Timing: W untimed warm-up steps, then K timed steps; L2 is flushed before every
+timed step, outside the events: a 256 MB write, then a read sweep of another 256 MB
+buffer, so that the step finds none of its data in L2 and does not pay for writing
+back the flush's own dirty lines; each step is bracketed by CUDA events
 on the stream it runs on; a barrier and torch.cuda.synchronize() bracket the timed
 loop; the max over ranks is reported. The reference arm times the oracle (plain
 CPU float64) on the host cores on the same workload.
@@ -39,6 +41,20 @@ SEED = 0
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 
+
+
+class L2Flush:
+    """Evicts L2 (129 MB on GB300) before a timed step: a 256 MB write, then a read sweep
+    of another 256 MB, which also retires the write's dirty lines before the step."""
+
+    def __init__(self, dev):
+        import torch
+        self.w = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        self.r = torch.ones(32 << 20, dtype=torch.int64, device=dev)
+
+    def __call__(self):
+        self.w.zero_()
+        self.r.sum()
 
 def _peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -173,7 +189,7 @@ def run_decode(pm, torch, store, B, steps, warmup, device, timed_clock=None, e2e
     ids = torch.empty((B, TOPK), dtype=torch.int32, device=dev)
     w = torch.empty((B, TOPK), dtype=torch.float32, device=dev)
     y = torch.empty((B, H), dtype=torch.bfloat16, device=dev)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     stream = torch.cuda.current_stream(dev)
 
     if graph:
@@ -212,7 +228,7 @@ def run_decode(pm, torch, store, B, steps, warmup, device, timed_clock=None, e2e
     torch.cuda.synchronize(dev)
     t0 = time.time()
     for i, s in enumerate(step_ids):
-        flush.zero_()
+        flush()
         evs[i][0].record(stream)
         one(s)
         evs[i][1].record(stream)
@@ -250,7 +266,7 @@ def run_decode(pm, torch, store, B, steps, warmup, device, timed_clock=None, e2e
         l_d = l_s if graph else torch.empty((B, E), dtype=torch.float32, device=dev)
         evs2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
         for i, s in enumerate(step_ids):
-            flush.zero_()
+            flush()
             evs2[i][0].record(stream)
             x_d.copy_(x_h[s], non_blocking=True)
             l_d.copy_(l_h[s], non_blocking=True)
@@ -301,7 +317,7 @@ def run_prefill(pm, torch, store, steps, warmup, device, K=PREFILL_K, cold=True,
     ids = torch.empty((PREFILL_T, TOPK), dtype=torch.int32, device=dev)
     w = torch.empty((PREFILL_T, TOPK), dtype=torch.float32, device=dev)
     y = torch.empty((PREFILL_T, H), dtype=torch.bfloat16, device=dev)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     stream = torch.cuda.current_stream(dev)
 
     def one(i):
@@ -320,7 +336,7 @@ def run_prefill(pm, torch, store, steps, warmup, device, K=PREFILL_K, cold=True,
     for i in range(steps):
         if cold:
             cache.expert_cache_reset(0)
-        flush.zero_()
+        flush()
         evs[i][0].record(stream)
         one(warmup + i)
         evs[i][1].record(stream)
@@ -446,7 +462,7 @@ def run_ours(args):
                                "256-step p=0.8 reuse routing trace",
                    "E": E, "top_k": TOPK, "hidden": H, "intermediate": I, "K": K_SLOTS, "batch": 1,
                    "pagein": "SM pull from the mapped pinned host store; the step replayed as one CUDA graph",
-                   "l2": "flushed before every timed step (256 MB write, outside the events)",
+                   "l2": "flushed before every timed step (256 MB write, then a 256 MB read sweep; outside the events)",
                    "parallelism": f"replicas x{ws}"},
         "expert_weight_hbm_gbs": layer_gbs,
         "expert_weight_hbm_frac": layer_gbs / hbm_peak,
@@ -514,7 +530,7 @@ def run_stack(pm, torch, B, steps, warmup, device, mode=0, layers=STACK_L, K=STA
     w = torch.empty((layers * B, TOPK), dtype=torch.float32, device=dev)
     y = torch.empty((B, H), dtype=torch.bfloat16, device=dev)
     work = torch.empty((B, H), dtype=torch.bfloat16, device=dev)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     stream = torch.cuda.current_stream(dev)
 
     if graph:
@@ -545,7 +561,7 @@ def run_stack(pm, torch, B, steps, warmup, device, mode=0, layers=STACK_L, K=STA
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     ids_used = [(warmup + i) % n_inputs for i in range(steps)]
     for i, si in enumerate(ids_used):
-        flush.zero_()
+        flush()
         evs[i][0].record(stream)
         one(si)
         evs[i][1].record(stream)

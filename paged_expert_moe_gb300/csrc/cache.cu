@@ -18,6 +18,7 @@
 #include "pmoe_internal.h"
 #include "tc_gemm.h"
 
+#include <algorithm>
 #include <atomic>
 #include <chrono>
 #include <cstdio>
@@ -438,8 +439,8 @@ int expert_cache_create(const pmoe_cache_desc* desc, pmoe_cache** out) {
                  o_o = carve(4 * P * d.hidden), o_x = c->use_tc ? carve(2 * P * d.hidden) : 0;
     const size_t chunk_cap = ((P + 255) / 256) * (size_t)E;
     const size_t o_ch = carve(4 * chunk_cap);
-    const size_t o_gb = carve(8);
-    const size_t o_dn = carve(4 * (size_t)E);
+    const size_t o_ep = carve(8);
+    const size_t o_hq = carve(8 * std::min(P, (size_t)kDecodeMaxPairs) * d.intermediate);
     const cudaError_t e = cudaMalloc(&c->ws_buf, off);
     if (e != cudaSuccess) {
       set_cuda_error(e, "cudaMalloc (workspace)");
@@ -460,10 +461,10 @@ int expert_cache_create(const pmoe_cache_desc* desc, pmoe_cache** out) {
     c->ws.x_perm = c->use_tc ? (__nv_bfloat16*)(b + o_x) : nullptr;
     c->ws.chunk_cnt = (int32_t*)(b + o_ch);
     c->ws.chunk_cap = (int)chunk_cap;
-    c->ws.gbar = (unsigned*)(b + o_gb);
-    PMOE_TRY(cudaMemset(c->ws.gbar, 0, 8));
-    c->ws.done = (unsigned*)(b + o_dn);
-    PMOE_TRY(cudaMemset(c->ws.done, 0, 4 * (size_t)E));
+    c->ws.epoch = (unsigned long long*)(b + o_ep);
+    PMOE_TRY(cudaMemset(c->ws.epoch, 0, 8));
+    c->ws.hq = (unsigned long long*)(b + o_hq);
+    PMOE_TRY(cudaMemset(c->ws.hq, 0, 8 * std::min(P, (size_t)kDecodeMaxPairs) * d.intermediate));
   }
   if (c->use_tc) {
     c->maps.resize(Lr);
@@ -579,7 +580,7 @@ int ensure_resident_impl(pmoe_cache* c, int layer, const int32_t* ids, int n_ids
   {
     KernelMark km(c, PMOE_K_RESIDENCY, ps);
     PMOE_CUDA(launch_residency(ids, n_ids, c->d.num_experts, c->d.num_slots, c->st[layer], c->plan_dev[layer],
-                               c->err_dev, ps));
+                               c->err_dev, c->ws.epoch, ps));
   }
   c->layer_used[layer] = 1;
   int waves = -1;

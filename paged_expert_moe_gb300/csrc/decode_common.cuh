@@ -19,6 +19,14 @@ __device__ __forceinline__ uint4 ld_stream(const void* p) {
   return v;
 }
 
+// 16-byte load from shared memory (an explicit shared-window access)
+__device__ __forceinline__ uint4 lds128(const void* p) {
+  uint4 v;
+  const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(p));
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+  return v;
+}
+
 __device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
 
@@ -54,10 +62,20 @@ __device__ __forceinline__ ChunkQ chunk_q(const uint8_t* scales, int row, int c,
 }
 
 // sum over the chunk's elements of w_i * a_i, with a (bf16) read from `av` (EPC/8 uint4).
-template <int FMT, bool SHARED>
+// Where chunk_dot reads its activations from.
+enum : int { kSrcGlobal = 0, kSrcShared = 1, kSrcRegs = 2 };
+
+template <int FMT, int SRC>
+__device__ __forceinline__ uint4 load_act(const uint4* p) {
+  if constexpr (SRC == kSrcShared) return lds128(p);
+  else if constexpr (SRC == kSrcGlobal) return __ldg(p);
+  else return *p;
+}
+
+template <int FMT, int SRC>
 __device__ __forceinline__ float chunk_dot(uint4 w, const uint4* av, ChunkQ q) {
   if constexpr (FMT == PMOE_BF16) {
-    const uint4 a = SHARED ? av[0] : __ldg(av);
+    const uint4 a = load_act<FMT, SRC>(av);
     float acc = 0.f;
     acc = dot_bf16x8(w.x, a.x, acc);
     acc = dot_bf16x8(w.y, a.y, acc);
@@ -69,7 +87,7 @@ __device__ __forceinline__ float chunk_dot(uint4 w, const uint4* av, ChunkQ q) {
     float acc = 0.f;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      const uint4 a = SHARED ? av[h] : __ldg(av + h);
+      const uint4 a = load_act<FMT, SRC>(av + h);
       const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
@@ -91,7 +109,7 @@ __device__ __forceinline__ float chunk_dot(uint4 w, const uint4* av, ChunkQ q) {
     float acc = 0.f;
 #pragma unroll
     for (int h = 0; h < 4; ++h) {
-      const uint4 a = SHARED ? av[h] : __ldg(av + h);
+      const uint4 a = load_act<FMT, SRC>(av + h);
       const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
       const uint32_t word = wv[h];  // 8 nibbles = elements 8h .. 8h+7
 #pragma unroll

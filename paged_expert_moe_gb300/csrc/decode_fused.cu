@@ -4,43 +4,59 @@
 // does ~1 FLOP per byte, so it is bound by HBM bandwidth (the decode-is-memory-bound
 // discussion in "SGLang serving optimisation"; "Running an MoE Model Larger Than Your
 // VRAM", section "Why is it fast when experts keep crossing PCIe?"). One persistent
-// CTA per SM (cooperative launch, so all CTAs are resident) does, for the wave's
-// experts in order:
-//   phase 1  gate/up + SiLU*mul: the wave's row pairs, cut into chunks that never cross
-//            an expert, are dealt out in one contiguous range per CTA; a producer
-//            thread streams each chunk's gate rows and the matching up rows into a
-//            shared-memory ring (cp.async.bulk, completion on mbarriers); consumer
-//            warps reduce them against the tokens' x (in shared memory), write
-//            h[pair][j] (bf16) and then add the finished row count to the expert's
-//            completion counter.
-//   phase 2  down: CTA b owns output rows [b*H/G, (b+1)*H/G) of every expert. The
-//            producer streams those W_d rows (they do not depend on h), waits until the
-//            expert's counter shows all I rows of h are written, and then bulk-copies
-//            the expert's h rows into the same stage (no grid-wide barrier).
-//   phase 3  combine (single-wave steps): the CTA holds o[pair][n] for every pair of
-//            its rows, so it writes y[t][n] = res + sum_r w[t,r] o[(t,r)][n] in rank
-//            order; otherwise o_part is written and the combine kernel runs after the
-//            last wave (same arithmetic and order, so the bits agree).
+// CTA per SM (cooperative launch, so all CTAs are resident) walks a schedule of
+// chunks. A producer thread streams each chunk's weight rows into a byte ring in
+// shared memory (cp.async.bulk, completion on mbarriers), a fetcher warp supplies the
+// intermediate rows that down chunks need, and two groups of four consumer warps take
+// the chunks in turn.
+//
+//   gate/up  Every expert's I row pairs (gate row j with up row j) are cut into one
+//            part per CTA; CTA b takes part (b + e) mod G of the wave's e-th expert,
+//            so each CTA touches every expert and the per-CTA totals differ by at
+//            most one row pair. The consumers reduce the rows against the tokens' x
+//            (in shared memory) and store h[pair][j] = silu(g) * u (bf16) as a 64-bit
+//            word whose upper 48 bits carry the plan's tag.
+//   down     CTA b owns output rows [b*H/G, (b+1)*H/G) of every expert. The W_d rows
+//            stream like any other chunk; the fetcher polls the expert's h words until
+//            each carries this launch's tag and stores the bf16 values next to the
+//            rows. The tag makes every word self-validating, so no counter, fence or
+//            grid barrier sits between the two halves, and the consumers never wait on
+//            a global-memory round trip (under full HBM load one takes microseconds).
+//   order    gate/up of expert e is followed, kDfLag experts later, by the down chunk
+//            of expert e: by then every CTA has finished e's gate/up, so the fetch
+//            overlaps the streaming of later experts.
+//   combine  (single-wave steps) the CTA holds o[pair][n] for every pair of its rows,
+//            so it writes y[t][n] = res + sum_r w[t,r] o[(t,r)][n] in rank order;
+//            otherwise o_part is written and the combine kernel runs after the last
+//            wave (same arithmetic and order, so the bits agree).
 // The token -> expert grouping (stable: expert ascending, pair index ascending) is
 // computed by every CTA from the ids; CTA 0 also writes pos/perm for the combine.
 // Per-pair dot products have a fixed order (lane-strided 16-byte chunks, then an
-// xor-shuffle tree), independent of slot, wave and of how many tokens share the
+// xor-shuffle tree), independent of slot, wave, grid and of how many tokens share the
 // expert. Every wait is bounded; on expiry the kernel records an error and stops.
 #include "decode_common.cuh"
+
+#include <algorithm>
 
 namespace pmoe {
 namespace {
 
 using namespace dec;
 
-constexpr int kDfThreads = 288;  // warps 0-7 consume (two groups of four), warp 8 produces
-constexpr int kDfStageBytes = 32 * 1024;
-constexpr int kDfMaxStages = 6;
-constexpr int kDfMaxPairs = 64;   // T * top_k
-constexpr int kDfMaxRows = 32;    // phase-2 output rows per CTA (H / grid)
-constexpr int kDfMaxChunks = 512;
+constexpr int kDfConsumerWarps = 12;        // warps 0-11 consume, 12 produces, 13 fetches h
+constexpr int kDfThreads = (kDfConsumerWarps + 2) * 32;
+constexpr int kDfSlots = 16;                // chunks in flight at most (one mbarrier pair each)
+constexpr int kDfMaxChunkBytes = 32 * 1024;  // weight bytes of one chunk
+constexpr int kDfMaxPairs = kDecodeMaxPairs;
+constexpr int kDfMaxRows = 32;              // down-projection output rows per CTA (ceil(H / grid))
+constexpr int kDfMaxChunks = 256;           // chunks per CTA
+static_assert(kDfMaxChunks <= 2 * kDfThreads, "the chunk-list scan covers two entries per thread");
+constexpr int kDfLag = 3;                   // down of expert e follows gate/up of expert e + kDfLag
+constexpr int kDfMaxTokens = kGemvMaxTokens;
+constexpr size_t kDfSmemBudget = 223 * 1024;  // dynamic shared memory; the static arrays fit in the rest
 constexpr long long kDfWaitLimit = 4000000000LL;
 constexpr int32_t kErrDecodeTimeout = 32;
+constexpr unsigned long long kTagMask = (1ull << 48) - 1;
 
 #ifdef PMOE_TRACE
 // Debug builds only: per-CTA %globaltimer stamps of the last launch.
@@ -54,7 +70,16 @@ __device__ __forceinline__ unsigned long long gtimer() {
   do {                 \
     g_df_trace[blockIdx.x][slot] = gtimer(); \
   } while (0)
+// per chunk: producer issue, data landed (consumer), h rows ready (down chunks), done
+__device__ unsigned long long g_df_chunk[1024][256][4];
+#define DF_CHUNK(k, slot)                                   \
+  do {                                                      \
+    if ((k) < 256) g_df_chunk[blockIdx.x][(k)][(slot)] = gtimer(); \
+  } while (0)
 #else
+#define DF_CHUNK(k, slot) \
+  do {                    \
+  } while (0)
 #define DF_TRACE(slot) \
   do {                 \
   } while (0)
@@ -66,7 +91,9 @@ struct DfArgs {
   const float* w;
   const __nv_bfloat16* residual;
   __nv_bfloat16* y;
-  int T, top_k, H, I, E, wave, sub, stages, fuse_combine;
+  int T, top_k, H, I, E, wave, sub, fuse_combine;
+  int ring_bytes;  // byte ring for the weight chunks
+  int cg, cd;      // chunks per gate/up part and per down part
   const int32_t* plan;
   Workspace ws;
   const uint8_t* arena;
@@ -95,6 +122,16 @@ __device__ __forceinline__ bool mb_try(uint64_t* b, uint32_t par) {
       : "memory");
   return ok != 0;
 }
+// non-blocking probe (try_wait may suspend the thread until the phase completes)
+__device__ __forceinline__ bool mb_test(uint64_t* b, uint32_t par) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(su32(b)), "r"(par)
+      : "memory");
+  return ok != 0;
+}
 __device__ __forceinline__ bool mb_wait(uint64_t* b, uint32_t par, volatile int* abort_flag, int32_t* err) {
   if (mb_try(b, par)) return true;
   const long long t0 = clock64();
@@ -114,134 +151,224 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
                "l"(src), "r"(bytes), "r"(su32(bar))
                : "memory");
 }
-__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
-  unsigned v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ ulonglong2 ld_relaxed_u64x2(const unsigned long long* p) {
+  ulonglong2 v;
+  asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(v.x), "=l"(v.y) : "l"(p) : "memory");
   return v;
 }
-__device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
-  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-__device__ __forceinline__ unsigned atom_acq_rel_add(unsigned* p, unsigned v) {
-  unsigned old;
-  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-  return old;
-}
-__device__ __forceinline__ void consumers_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
-__device__ __forceinline__ void group_sync(int grp) { asm volatile("bar.sync %0, 128;" ::"r"(2 + grp) : "memory"); }
-// Group barrier that ORs a predicate over the group's 128 threads: a failed wait in any
-// warp makes the whole group leave together (no warp is left at a named barrier).
-__device__ __forceinline__ int group_bar_or(int grp, int pred) {
-  int r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\tsetp.ne.s32 p, %2, 0;\n\tbar.red.or.pred q, %1, 128, p;\n\t"
-      "selp.s32 %0, 1, 0, q;\n\t}\n"
-      : "=r"(r)
-      : "r"(2 + grp), "r"(pred)
-      : "memory");
+// Gate and up partial dot products of one 16-byte chunk (8 bf16 weights of each row)
+// against the same 8 bf16 activations. The two chains advance together in packed
+// fp32 FMAs; each lane of the pair is an ordinary fused multiply-add, so the sums are
+// bit-identical to two separate fmaf chains.
+__device__ __forceinline__ float2 gu_dot_bf16(uint4 wg, uint4 wu, uint4 xa) {
+  unsigned long long acc = 0ull;  // (+0.f, +0.f)
+  const uint32_t g4[4] = {wg.x, wg.y, wg.z, wg.w}, u4[4] = {wu.x, wu.y, wu.z, wu.w}, x4[4] = {xa.x, xa.y, xa.z, xa.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    unsigned long long wlo, whi, xlo, xhi;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(wlo) : "r"(g4[i] << 16), "r"(u4[i] << 16));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(whi) : "r"(g4[i] & 0xffff0000u), "r"(u4[i] & 0xffff0000u));
+    asm("mov.b64 %0, {%1, %1};" : "=l"(xlo) : "r"(x4[i] << 16));
+    asm("mov.b64 %0, {%1, %1};" : "=l"(xhi) : "r"(x4[i] & 0xffff0000u));
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(wlo), "l"(xlo));
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(whi), "l"(xhi));
+  }
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(acc));
   return r;
 }
 
-struct ChunkList {
-  int n1, n2, n_lo, n_hi;
+// Reads n16 * 8 tagged h words starting at src (waiting until each carries `tag`) and
+// packs their bf16 values into n16 16-byte vectors. Used only for an expert that one
+// token routes to more than once.
+__device__ bool fetch_h_direct(const unsigned long long* src, unsigned long long tag, uint4* out, int n16,
+                               volatile int* abort_flag, int32_t* err) {
+  for (int q = 0; q < n16; ++q) {
+    uint32_t w[4];
+    for (int h = 0; h < 4; ++h) {
+      const long long t0 = clock64();
+      ulonglong2 v = ld_relaxed_u64x2(src + q * 8 + h * 2);
+      while ((v.x >> 16) != tag || (v.y >> 16) != tag) {
+        if (*abort_flag) return false;
+        if (clock64() - t0 > kDfWaitLimit) {
+          *abort_flag = 1;
+          atomicOr(err, kErrDecodeTimeout);
+          return false;
+        }
+        __nanosleep(64);
+        v = ld_relaxed_u64x2(src + q * 8 + h * 2);
+      }
+      w[h] = (uint32_t)(v.x & 0xffffu) | ((uint32_t)(v.y & 0xffffu) << 16);
+    }
+    out[q] = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  return true;
+}
+__device__ __forceinline__ int ld_acquire_shared(const int* p) {
+  int v;
+  asm volatile("ld.acquire.cta.shared.u32 %0, [%1];" : "=r"(v) : "r"(su32(p)) : "memory");
+  return v;
+}
+__device__ __forceinline__ void consumers_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kDfConsumerWarps * 32) : "memory");
+}
+// A CTA's schedule. With D experts in the wave and lag L = min(kDfLag, D):
+//   GU(0) .. GU(L-1), then for e = L .. D-1: GU(e) D(e-L), then D(D-L) .. D(D-1),
+// where GU(e) is the CTA's gate/up part of expert e in cg chunks and D(e) its down
+// rows of expert e in cd chunks. Entry q is (kind, expert index, first row, rows),
+// computed from q alone so that the whole list is built in parallel.
+struct DfSched {
+  int D, G, b, I, H, cg, cd;
 };
 
-// Chunks of one CTA. Phase 1: every expert's I row pairs are cut into cpe = ceil(I/rj1)
-// chunks of rj1 rows; the n_we*cpe chunks are dealt out in one contiguous range per CTA
-// (so a CTA streams long contiguous runs and no chunk crosses an expert). Phase 2:
-// (expert index, first output row, count) over the CTA's output rows, every expert.
-// Entry q is computed by thread q from its index alone.
-__device__ ChunkList chunk_bounds(int b, int G, int n_we, int I, int H, int rj1, int rd, int* g0, int* c2) {
-  ChunkList cl;
-  const int cpe = (I + rj1 - 1) / rj1;
-  const long long total = (long long)n_we * cpe;
-  *g0 = (int)(total * b / G);
-  cl.n1 = (int)(total * (b + 1) / G) - *g0;
-  cl.n_lo = (int)((long long)H * b / G);
-  cl.n_hi = (int)((long long)H * (b + 1) / G);
-  *c2 = (cl.n_hi - cl.n_lo + rd - 1) / rd;
-  cl.n2 = n_we * *c2;
-  if (cl.n1 + cl.n2 > kDfMaxChunks) {  // excluded on the host; never write past the list
-    cl.n1 = 0;
-    cl.n2 = 0;
+__device__ __forceinline__ int4 sched_entry(int q, const DfSched& s) {
+  const int L = min(kDfLag, s.D), per = s.cg + s.cd;
+  int kind, e, sub;
+  if (q < L * s.cg) {
+    kind = 1;
+    e = q / s.cg;
+    sub = q - e * s.cg;
+  } else {
+    const int q1 = q - L * s.cg;
+    if (q1 < (s.D - L) * per) {
+      const int st = q1 / per, r = q1 - st * per;
+      if (r < s.cg) {
+        kind = 1;
+        e = L + st;
+        sub = r;
+      } else {
+        kind = 2;
+        e = st;
+        sub = r - s.cg;
+      }
+    } else {
+      const int q2 = q1 - (s.D - L) * per;
+      kind = 2;
+      e = s.D - L + q2 / s.cd;
+      sub = q2 - (q2 / s.cd) * s.cd;
+    }
   }
-  return cl;
+  // (32-bit arithmetic: I, H < 2^20 and G <= 1024 are checked on the host)
+  const unsigned G = (unsigned)s.G;
+  if (kind == 1) {
+    const unsigned part = ((unsigned)s.b + (unsigned)e) % G;
+    const int j0 = (int)((unsigned)s.I * part / G);
+    const int n = (int)((unsigned)s.I * (part + 1) / G) - j0;
+    const int a0 = n * sub / s.cg, a1 = n * (sub + 1) / s.cg;
+    return make_int4(1, e, j0 + a0, a1 - a0);
+  }
+  const int r0 = (int)((unsigned)s.H * (unsigned)s.b / G);
+  const int n = (int)((unsigned)s.H * (unsigned)(s.b + 1) / G) - r0;
+  const int a0 = n * sub / s.cd, a1 = n * (sub + 1) / s.cd;
+  return make_int4(2, e, r0 + a0, a1 - a0);
 }
 
-__device__ int4 chunk_entry(int q, const ChunkList& cl, int g0, int c2, int I, int rj1, int rd) {
-  if (q < cl.n1) {
-    const int cpe = (I + rj1 - 1) / rj1;
-    const int g = g0 + q, i = g / cpe, j = (g - i * cpe) * rj1;
-    return make_int4(1, i, j, min(rj1, I - j));
+// Ring placement: the live chunks occupy [lo, head) or, wrapped, [lo, R) + [0, head).
+// Returns the offset for `need` bytes, or -1 if they do not fit until older chunks go.
+__device__ __forceinline__ int ring_place(unsigned head, unsigned lo, bool empty, unsigned need, unsigned R) {
+  if (empty) return (int)(head + need <= R ? head : 0u);
+  if (lo < head) {
+    if (head + need <= R) return (int)head;
+    if (need <= lo) return 0;
+    return -1;
   }
-  const int qq = q - cl.n1, i = qq / c2, r = cl.n_lo + (qq - i * c2) * rd;
-  return make_int4(2, i, r, min(rd, cl.n_hi - r));
+  return head + need <= lo ? (int)head : -1;
 }
 
 template <int FMT, int NCH1, int NCH2>
 __global__ void __launch_bounds__(kDfThreads, 1) decode_fused_kernel(const DfArgs a) {
   constexpr int EPC = Fmt<FMT>::EPC;
   extern __shared__ __align__(128) uint8_t dsm[];
-  __shared__ ChunkList s_cl;
   __shared__ int4 s_we[kDfMaxPairs];  // per wave expert: (expert, slot, first grouped pair, end)
+  __shared__ int2 s_wl[kDfMaxPairs];  // the wave's (expert, slot) list
   __shared__ int s_tok[kDfMaxPairs];  // token of each grouped pair
   __shared__ int s_pos[kDfMaxPairs];  // grouped position of each pair (t*k + r), -1 if invalid
   __shared__ int s_ids[kDfMaxPairs];
+  __shared__ float s_w[kDfMaxPairs];  // routing weights (combine)
+  __shared__ int s_hdr[6];
+  __shared__ unsigned s_off[kDfSlots];  // ring offset of each slot's chunk
+  __shared__ __align__(8) uint64_t s_full[kDfSlots];  // the chunk's weight bytes landed
+  __shared__ __align__(8) uint64_t s_hrdy[kDfSlots];  // the fetcher has passed the chunk (down: h copied)
+  __shared__ __align__(8) uint64_t s_empty[kDfSlots];
+  __shared__ int s_abort;
+  __shared__ int s_placed;  // chunks placed in the ring so far
 
-  const int S = a.stages;
+  const unsigned R = (unsigned)a.ring_bytes;
   uint8_t* ring = dsm;
-  uint4* x_s = reinterpret_cast<uint4*>(ring + (size_t)S * kDfStageBytes);
+  uint4* x_s = reinterpret_cast<uint4*>(ring + R);
   float* o_s = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(x_s) + (size_t)a.T * a.H * 2);
-  uint64_t* full = reinterpret_cast<uint64_t*>(o_s + kDfMaxPairs * kDfMaxRows);
-  uint64_t* empty = full + kDfMaxStages;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kDfMaxStages);
-  int4* chunks = reinterpret_cast<int4*>(empty + kDfMaxStages + 2);
+  __nv_bfloat16* res_s = reinterpret_cast<__nv_bfloat16*>(o_s + kDfMaxPairs * kDfMaxRows);
+  int4* chunks = reinterpret_cast<int4*>(res_s + kDfMaxTokens * kDfMaxRows);
+  volatile int* abort_flag = &s_abort;
 
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (threadIdx.x == 0) DF_TRACE(0);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) DF_TRACE(0);
   const PlanLayout L{a.E};
   const int P = a.T * a.top_k;
-  // one round of independent loads: the plan words this launch needs and the ids
-  __shared__ int s_hdr[4];
-  if (threadIdx.x == 0) s_hdr[0] = a.plan[kPlanWaves];
-  if (threadIdx.x == 32) s_hdr[1] = a.plan[L.wave_start() + a.wave];
-  if (threadIdx.x == 64) s_hdr[2] = a.plan[L.wave_start() + a.wave + 1];
-  if (threadIdx.x == 96) s_hdr[3] = a.plan[L.wave_hits() + a.wave];
-  if (threadIdx.x >= 128 && threadIdx.x < 128 + P) s_ids[threadIdx.x - 128] = a.ids[threadIdx.x - 128];
-  __syncthreads();
-  if (a.wave >= s_hdr[0]) return;
-  int w0 = s_hdr[1], w1 = s_hdr[2];
-  if (a.sub == 1) w1 = w0 + s_hdr[3];
-  else if (a.sub == 2) w0 = w0 + s_hdr[3];
-  const int n_we = w1 - w0;
-  const size_t rbg = (size_t)a.H * Fmt<FMT>::BPE2 / 2;  // one gate (or up) row
-  const size_t rbd = (size_t)a.I * Fmt<FMT>::BPE2 / 2;  // one down row
-  const size_t hrow = (size_t)a.I * 2;                  // one h row (bf16)
-  const int rj1 = (int)(kDfStageBytes / (2 * rbg));
-  const size_t h_room = (size_t)a.T * hrow;              // an expert has at most T pairs
-  const int rd = (int)((kDfStageBytes - h_room) / rbd);
-  const size_t h_off = ((size_t)rd * rbd + 15) & ~(size_t)15;
-  unsigned* done = a.ws.done;
-
-  // grouping: stable by expert id, then pair index
-  __shared__ int2 s_wl[kDfMaxPairs];  // the launch's wave experts and slots, loaded in parallel
-  if (threadIdx.x < n_we)
-    s_wl[threadIdx.x] = make_int2(a.plan[L.wave_exp() + w0 + threadIdx.x], a.plan[L.wave_slot() + w0 + threadIdx.x]);
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) {
-      mb_init(&full[s], 1);
-      mb_init(&empty[s], 1);
+  const int r_lo = (int)((long long)a.H * blockIdx.x / gridDim.x);
+  const int r_hi = (int)((long long)a.H * (blockIdx.x + 1) / gridDim.x);
+  // One round of independent loads: the plan words, the ids, the first wave's list (read
+  // on speculation: wave 0 starts at list index 0), the tokens' x, the routing weights and
+  // the residual rows this CTA combines.
+  const int nspec = min(P, a.E);
+  if (tid < P) {
+    s_ids[tid] = a.ids[tid];
+  } else if (tid >= 64 && tid < 64 + nspec) {
+    s_wl[tid - 64].x = a.plan[L.wave_exp() + tid - 64];
+  } else if (tid >= 128 && tid < 128 + nspec) {
+    s_wl[tid - 128].y = a.plan[L.wave_slot() + tid - 128];
+  } else if (tid >= 192 && tid < 198) {
+    const int q = tid - 192;
+    const int at = q == 0   ? (int)kPlanWaves
+                   : q == 1 ? L.wave_start() + a.wave
+                   : q == 2 ? L.wave_start() + a.wave + 1
+                   : q == 3 ? L.wave_hits() + a.wave
+                   : q == 4 ? (int)kPlanEpochLo
+                            : (int)kPlanEpochHi;
+    s_hdr[q] = a.plan[at];
+  } else if (tid >= 256 && tid < 256 + P) {
+    s_w[tid - 256] = a.w[tid - 256];
+  }
+  for (int i = tid; i < a.T * (a.H / 8); i += kDfThreads) x_s[i] = __ldg(reinterpret_cast<const uint4*>(a.x) + i);
+  if (a.residual != nullptr && a.fuse_combine != 0 && r_hi > r_lo) {
+    const int rows = r_hi - r_lo;
+    for (int i = tid; i < a.T * rows; i += kDfThreads) {
+      const int t = i / rows;
+      res_s[t * kDfMaxRows + (i - t * rows)] = a.residual[(size_t)t * a.H + r_lo + (i - t * rows)];
     }
-    *abort_flag = 0;
+  }
+  if (tid == 224) {
+    for (int s = 0; s < kDfSlots; ++s) {
+      mb_init(&s_full[s], 1);
+      mb_init(&s_hrdy[s], 1);
+      mb_init(&s_empty[s], kDfConsumerWarps);
+    }
+    s_abort = 0;
+    s_placed = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  int g0, c2;
-  const ChunkList clb = chunk_bounds(blockIdx.x, gridDim.x, n_we, a.I, a.H, rj1, rd, &g0, &c2);
-  for (int q = threadIdx.x; q < clb.n1 + clb.n2; q += blockDim.x) chunks[q] = chunk_entry(q, clb, g0, c2, a.I, rj1, rd);
-  if (threadIdx.x == 0) s_cl = clb;
   __syncthreads();
-  if (threadIdx.x < P) {
-    const int p = threadIdx.x, id = s_ids[p];
+  if (tid == 0) DF_TRACE(7);
+  const int n_waves = s_hdr[0];
+  if (a.wave >= n_waves) return;
+  int w0 = s_hdr[1], w1 = s_hdr[2];
+  if (a.sub == 1) w1 = w0 + s_hdr[3];
+  else if (a.sub == 2) w0 += s_hdr[3];
+  const int D = w1 - w0;
+  if (w0 != 0) {  // not the speculated list: load this wave's part of it
+    if (tid < D) s_wl[tid] = make_int2(a.plan[L.wave_exp() + w0 + tid], a.plan[L.wave_slot() + w0 + tid]);
+    __syncthreads();
+  }
+  // tag of this launch's h words: unique per (plan epoch, wave, part of the wave)
+  const unsigned long long epoch = ((unsigned long long)(uint32_t)s_hdr[5] << 32) | (uint32_t)s_hdr[4];
+  const unsigned long long tag = ((epoch << 12) | ((unsigned long long)a.wave << 2) | (unsigned)a.sub) & kTagMask;
+
+  // grouping: stable by expert id, then pair index
+  if (tid < P) {
+    const int p = tid, id = s_ids[p];
     int pos = -1;
     if (id >= 0 && id < a.E) {
       pos = 0;
@@ -257,228 +384,351 @@ __global__ void __launch_bounds__(kDfThreads, 1) decode_fused_kernel(const DfArg
       if (pos >= 0) a.ws.perm[pos] = p;
     }
   }
-  if (threadIdx.x < n_we) {
-    const int2 es = s_wl[threadIdx.x];
+  if (tid < D) {
+    const int2 es = s_wl[tid];
     int lo = 0, cnt = 0;
     for (int q = 0; q < P; ++q) {
       const int o = s_ids[q];
       lo += (o >= 0 && o < es.x) ? 1 : 0;
       cnt += (o == es.x) ? 1 : 0;
     }
-    s_we[threadIdx.x] = make_int4(es.x, es.y, lo, lo + cnt);
+    s_we[tid] = make_int4(es.x, es.y, lo, lo + cnt);
+  }
+  const DfSched sc{D, (int)gridDim.x, (int)blockIdx.x, a.I, a.H, a.cg, a.cd};
+  const int n_chunks = D * (a.cg + a.cd);
+  if (n_chunks > kDfMaxChunks) {  // excluded on the host; never write past the list
+    if (tid == 0) atomicOr(a.err, kErrPlanOverflow);
+    return;
+  }
+  // chunk list; .x = kind | (rows of all earlier chunks) << 2, which deals each chunk's
+  // rows to the consumer warps round-robin in one sequence over the whole list
+  __shared__ int s_scan[kDfThreads / 32];
+  {
+    int4 e0 = make_int4(0, 0, 0, 0), e1 = make_int4(0, 0, 0, 0);
+    if (tid < n_chunks) e0 = sched_entry(tid, sc);
+    if (tid + kDfThreads < n_chunks) e1 = sched_entry(tid + kDfThreads, sc);
+    // chunks tid and tid + kDfThreads (n_chunks <= kDfMaxChunks < 2 * kDfThreads)
+    const int c0 = e0.w, c1 = e1.w;
+    int v = c0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += y;
+    }
+    if (lane == 31) s_scan[warp] = v;
+    __syncthreads();
+    int before = 0, total0 = 0;
+    for (int i = 0; i < kDfThreads / 32; ++i) {
+      if (i < warp) before += s_scan[i];
+      total0 += s_scan[i];
+    }
+    const int base0 = before + v - c0;
+    __syncthreads();
+    int v1 = c1;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, v1, o);
+      if (lane >= o) v1 += y;
+    }
+    if (lane == 31) s_scan[warp] = v1;
+    __syncthreads();
+    int before1 = 0;
+    for (int i = 0; i < warp; ++i) before1 += s_scan[i];
+    const int base1 = total0 + before1 + v1 - c1;
+    if (tid < n_chunks) chunks[tid] = make_int4(e0.x | (base0 << 2), e0.y, e0.z, e0.w);
+    if (tid + kDfThreads < n_chunks) chunks[tid + kDfThreads] = make_int4(e1.x | (base1 << 2), e1.y, e1.z, e1.w);
   }
   __syncthreads();
-  if (threadIdx.x == 0) DF_TRACE(1);
-  const ChunkList ch = s_cl;
-  const int n_chunks = ch.n1 + ch.n2;
+  if (tid == 0) DF_TRACE(1);
+  const size_t rbg = (size_t)a.H * Fmt<FMT>::BPE2 / 2;  // one gate (or up) row
+  const size_t rbd = (size_t)a.I * Fmt<FMT>::BPE2 / 2;  // one down row
 
-  if (warp == 8) {
-    // ---------------- producer warp. Lane 0 issues each chunk's weight copies as soon as
-    // its stage is free (phase-2 chunks announce their h bytes too); meanwhile the lanes
-    // poll the completion counters of up to 32 issued phase-2 chunks at once, and lane i
-    // issues the h copy of the chunk whose completion it observed.
-    __shared__ int s_ready[kDfMaxPairs];  // expert index -> its h is complete (observed)
-    for (int i = lane; i < n_we; i += 32) s_ready[i] = 0;
-    __syncwarp();
-    int k = 0, kh = ch.n1;
-    long long last = clock64();
-    while (true) {
-      // every branch below is decided by lane 0 (or a ballot) and broadcast, so the warp
-      // stays converged
-      int stop = ((k >= n_chunks && kh >= n_chunks) || *abort_flag) ? 1 : 0;
-      stop = __shfl_sync(0xffffffffu, stop, 0);
-      if (stop) break;
-      // issue every chunk whose stage is free (weights; phase-2 chunks also announce h)
-      int n_issued = 0;
-      if (lane == 0) {
-        while (k + n_issued < n_chunks &&
-               mb_try(&empty[(k + n_issued) % S], (uint32_t)(((k + n_issued) / S) & 1) ^ 1u)) {
-          const int kk = k + n_issued, s = kk % S;
-          const int4 cd = chunks[kk];
-          const int4 we = s_we[cd.y];
+  if (warp == kDfConsumerWarps) {
+    // ---------------- producer: lane 0 places every chunk in the byte ring as soon as
+    // its slot and its bytes are free (chunks are released in order) and issues its
+    // bulk copies. A down chunk also reserves room for the expert's h rows, which the
+    // fetcher warp fills.
+    if (lane == 0) {
+      unsigned head = 0;
+      int tail = 0, k = 0;
+      for (; k < n_chunks; ++k) {
+        const int4 cd = chunks[k];
+        const int kind = cd.x & 3;
+        const int4 we = s_we[cd.y];
+        const unsigned wbytes = kind == 1 ? (unsigned)(2 * (size_t)cd.w * rbg) : (unsigned)((size_t)cd.w * rbd);
+        const unsigned hbytes = (kind == 2 && cd.w > 0) ? (unsigned)(min(we.w - we.z, a.T) * a.I * 2) : 0u;
+        const unsigned need = (wbytes + hbytes + 127u) & ~127u;
+        int off = -1;
+        long long t0 = -1;
+        while (true) {
+          // place with what is known to be free; retire the oldest chunk only when
+          // that fails (the wait sleeps in the barrier)
+          if (k - tail < kDfSlots) {
+            off = ring_place(head, s_off[tail % kDfSlots], tail == k, need, R);
+            if (off >= 0) break;
+          }
+          if (mb_try(&s_empty[tail % kDfSlots], (uint32_t)((tail / kDfSlots) & 1))) {
+            ++tail;
+            continue;
+          }
+          if (*abort_flag) break;
+          if (t0 < 0) {
+            t0 = clock64();
+          } else if (clock64() - t0 > kDfWaitLimit) {
+            *abort_flag = 1;
+            atomicOr(a.err, kErrDecodeTimeout);
+            break;
+          }
+        }
+        if (off < 0) break;
+        const int s = k % kDfSlots;
+        s_off[s] = (unsigned)off;
+        head = (unsigned)off + need;
+        uint64_t* fb = &s_full[s];
+        DF_CHUNK(k, 0);
+        if (wbytes == 0) {
+          mb_arrive(fb);
+        } else {
           const uint8_t* ex = a.arena + (size_t)we.y * a.stride;
-          uint8_t* st = ring + (size_t)s * kDfStageBytes;
-          if (cd.x == 1) {
-            const uint32_t bytes = (uint32_t)(cd.w * rbg);
-            mb_expect(&full[s], 2 * bytes);
-            bulk_g2s(st, ex + a.lay.gu_w + (size_t)cd.z * rbg, bytes, &full[s]);
-            bulk_g2s(st + (size_t)rj1 * rbg, ex + a.lay.gu_w + (size_t)(a.I + cd.z) * rbg, bytes, &full[s]);
+          uint8_t* dst = ring + off;
+          mb_expect(fb, wbytes);
+          if (kind == 1) {
+            const uint32_t half = wbytes / 2;
+            bulk_g2s(dst, ex + a.lay.gu_w + (size_t)cd.z * rbg, half, fb);
+            bulk_g2s(dst + half, ex + a.lay.gu_w + (size_t)(a.I + cd.z) * rbg, half, fb);
           } else {
-            const uint32_t wbytes = (uint32_t)(cd.w * rbd);
-            const uint32_t hbytes = (uint32_t)((we.w - we.z) * hrow);
-            mb_expect(&full[s], wbytes + hbytes);
-            bulk_g2s(st, ex + a.lay.d_w + (size_t)cd.z * rbd, wbytes, &full[s]);
+            bulk_g2s(dst, ex + a.lay.d_w + (size_t)cd.z * rbd, wbytes, fb);
           }
-          ++n_issued;
         }
+        asm volatile("st.release.cta.shared.u32 [%0], %1;" ::"r"(su32(&s_placed)), "r"(k + 1) : "memory");
       }
-      n_issued = __shfl_sync(0xffffffffu, n_issued, 0);
-      k += n_issued;
-      bool progressed = n_issued > 0;
-      // h copies of issued phase-2 chunks whose expert is complete; the completion
-      // counters are read (one L2 round trip) only when nothing else could be issued
-      if (kh < k) {
-        const int q = kh + lane;
-        int ready = 0;
-        int4 we = make_int4(0, 0, 0, 0);
-        if (q < k) {
-          const int ei = chunks[q].y;
-          we = s_we[ei];
-          ready = s_ready[ei];
-          if (!ready && n_issued == 0) {
-            ready = ld_acquire(done + we.x) >= (unsigned)a.I ? 1 : 0;
-            if (ready) s_ready[ei] = 1;
+      if (*abort_flag) {
+        // stopped early: let the copies already issued land before the CTA exits
+        const long long t1 = clock64();
+        for (int q = max(0, k - kDfSlots); q < k; ++q)
+          while (!mb_test(&s_full[q % kDfSlots], (uint32_t)((q / kDfSlots) & 1)) && clock64() - t1 < kDfWaitLimit) {
           }
-        }
-        const unsigned m = __ballot_sync(0xffffffffu, ready);
-        const int n_ready = (m == 0xffffffffu) ? 32 : (__ffs(~m) - 1);  // leading run of ready chunks
-        if (lane < n_ready) {
-          asm volatile("fence.proxy.async.global;" ::: "memory");
-          const uint32_t hbytes = (uint32_t)((we.w - we.z) * hrow);
-          if (hbytes > 0) {
-            const int s = q % S;
-            bulk_g2s(ring + (size_t)s * kDfStageBytes + h_off, a.ws.h + (size_t)we.z * a.I, hbytes, &full[s]);
-          }
-        }
-        __syncwarp();
-        if (n_ready > 0) {
-          kh += n_ready;
-          progressed = true;
-        }
       }
-      if (progressed) {
-        last = clock64();
-      } else {
-        int expired = (clock64() - last > kDfWaitLimit) ? 1 : 0;
-        expired = __shfl_sync(0xffffffffu, expired, 0);
-        if (expired) {
+    }
+  } else if (warp == kDfConsumerWarps + 1) {
+    // ---------------- h fetcher: walks the chunks in order behind the producer. For a
+    // down chunk it polls the expert's h words (written by every CTA's gate/up chunks)
+    // until each carries this launch's tag, stores the bf16 values after the chunk's W_d
+    // rows and signals s_hrdy; other chunks are passed straight through.
+    for (int k = 0; k < n_chunks; ++k) {
+      long long t0 = -1;
+      bool ok = true;
+      while (ld_acquire_shared(&s_placed) <= k) {
+        if (*abort_flag) {
+          ok = false;
+          break;
+        }
+        if (t0 < 0) {
+          t0 = clock64();
+        } else if (clock64() - t0 > kDfWaitLimit) {
           if (lane == 0) {
             *abort_flag = 1;
             atomicOr(a.err, kErrDecodeTimeout);
           }
+          ok = false;
           break;
         }
+        __nanosleep(256);
       }
+      if (!__all_sync(0xffffffffu, ok)) break;
+      const int s = k % kDfSlots;
+      const int4 cd = chunks[k];
+      if ((cd.x & 3) == 2 && cd.w > 0) {
+        const int4 we = s_we[cd.y];
+        const int hb = min(we.w - we.z, a.T);
+        uint16_t* hdst = reinterpret_cast<uint16_t*>(ring + s_off[s] + (size_t)cd.w * rbd);
+        const int n = hb * a.I;  // even
+        const unsigned long long* src = a.ws.hq + (size_t)we.z * a.I;
+        int bad = 0;
+        for (int i0 = 2 * lane; i0 < n && !bad; i0 += 64 * 16) {
+          // up to 16 16-byte loads per lane in flight; the stale ones are re-read
+          // together, so each polling round costs one round trip
+          ulonglong2 v[16];
+          unsigned pend = 0;
+#pragma unroll
+          for (int u = 0; u < 16; ++u)
+            if (i0 + u * 64 < n) {
+              v[u] = ld_relaxed_u64x2(src + i0 + u * 64);
+              pend |= 1u << u;
+            }
+          long long t1 = -1;
+          while (true) {
+#pragma unroll
+            for (int u = 0; u < 16; ++u)
+              if ((pend >> u) & 1u) {
+                if ((v[u].x >> 16) == tag && (v[u].y >> 16) == tag) {
+                  *reinterpret_cast<uint32_t*>(hdst + i0 + u * 64) =
+                      (uint32_t)(v[u].x & 0xffffu) | ((uint32_t)(v[u].y & 0xffffu) << 16);
+                  pend &= ~(1u << u);
+                }
+              }
+            if (pend == 0) break;
+            if (*abort_flag) {
+              bad = 1;
+              break;
+            }
+            if (t1 < 0) {
+              t1 = clock64();
+            } else if (clock64() - t1 > kDfWaitLimit) {
+              *abort_flag = 1;
+              atomicOr(a.err, kErrDecodeTimeout);
+              bad = 1;
+              break;
+            }
+            __nanosleep(256);
+#pragma unroll
+            for (int u = 0; u < 16; ++u)
+              if ((pend >> u) & 1u) v[u] = ld_relaxed_u64x2(src + i0 + u * 64);
+          }
+        }
+        if (__any_sync(0xffffffffu, bad)) break;
+        // these generic stores share the ring with later bulk copies (async proxy)
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        if (lane == 0) DF_CHUNK(k, 2);
+      }
+      __syncwarp();
+      if (lane == 0) mb_arrive(&s_hrdy[s]);
     }
   } else {
-    // ---------------- consumers (warps 0-7): group grp takes chunks k = grp, grp+2, ...
+    // ---------------- consumers (warps 0 .. kDfConsumerWarps-1): every warp walks every
+    // chunk; the rows of the whole list are dealt to the warps round-robin (row i of the
+    // list goes to warp i mod kDfConsumerWarps), so a warp holds about one row of a chunk
+    // and moves on to the next chunk at once. Each warp waits on the chunk's barriers
+    // itself and releases it (the empty barrier counts one arrival per warp).
     const int nv = a.H / 8;
-    for (int i = threadIdx.x; i < a.T * nv; i += 256) x_s[i] = __ldg(reinterpret_cast<const uint4*>(a.x) + i);
-    consumers_sync();
-    const int grp = warp >> 2, wl = warp & 3;
     const int nch1 = (int)(rbg / 16), nch2 = (int)(rbd / 16);
-    const bool fuse = a.fuse_combine != 0 && a.sub == 0 && a.plan[kPlanWaves] == 1;
-    int pending_rows = 0;
-    for (int k = grp; k < n_chunks; k += 2) {
-      const int s = k % S;
-      const bool got = mb_wait(&full[s], (uint32_t)((k / S) & 1), abort_flag, a.err);
-      if (group_bar_or(grp, got ? 0 : 1)) break;
-      if (k == 0 && lane == 0) DF_TRACE(2);
-      if (k == ch.n1 && lane == 0) DF_TRACE(3);
-      if (k == ch.n1 - 1 && lane == 0) DF_TRACE(6);  // wait for this CTA's last phase-1 chunk
+    const bool fuse = a.fuse_combine != 0 && a.sub == 0 && n_waves == 1;
+    bool first_down = true;
+    for (int k = 0; k < n_chunks; ++k) {
+      const int s = k % kDfSlots;
       const int4 cd = chunks[k];
+      const int kind = cd.x & 3;
+      const int first = ((warp - (cd.x >> 2)) % kDfConsumerWarps + kDfConsumerWarps) % kDfConsumerWarps;  // this warp's first row
+      const uint32_t par = (uint32_t)((k / kDfSlots) & 1);
+      // every chunk's s_hrdy phase is waited for (not only down chunks'), so that a warp
+      // never waits on a phase two ahead of the barrier's (parity would alias)
+      bool got = mb_wait(&s_full[s], par, abort_flag, a.err);
+      if (got) got = mb_wait(&s_hrdy[s], par, abort_flag, a.err);
+      if (!__all_sync(0xffffffffu, got)) break;
+      if (k == 0 && lane == 0 && warp == 0) DF_TRACE(2);
+      if (warp == 0 && lane == 0) DF_CHUNK(k, 1);
       const int4 we = s_we[cd.y];
       const uint8_t* ex = a.arena + (size_t)we.y * a.stride;
-      const uint8_t* st = ring + (size_t)s * kDfStageBytes;
-      if (cd.x == 1) {
-        for (int rp = wl; rp < cd.w; rp += 4) {
+      const uint8_t* st = ring + s_off[s];
+      bool ok = true;
+      if (kind == 1) {
+        if (warp == 0 && lane == 0) DF_TRACE(6);  // (the last write is the last gate/up chunk)
+        for (int rp = first; rp < cd.w; rp += kDfConsumerWarps) {
           const uint4* grow = reinterpret_cast<const uint4*>(st + (size_t)rp * rbg);
-          const uint4* urow = reinterpret_cast<const uint4*>(st + (size_t)(rj1 + rp) * rbg);
+          const uint4* urow = reinterpret_cast<const uint4*>(st + (size_t)(cd.w + rp) * rbg);
           uint4 gw[NCH1], uw[NCH1];
 #pragma unroll
           for (int c = 0; c < NCH1; ++c) {
             const int idx = lane + 32 * c;
             if (idx < nch1) {
-              gw[c] = grow[idx];
-              uw[c] = urow[idx];
+              gw[c] = lds128(grow + idx);
+              uw[c] = lds128(urow + idx);
             }
           }
           const int j = cd.z + rp;
           for (int gp = we.z; gp < we.w; ++gp) {
             const uint4* xr = x_s + (size_t)s_tok[gp] * nv;
             float g = 0.f, u = 0.f;
+            if constexpr (FMT == PMOE_BF16) {
 #pragma unroll
-            for (int c = 0; c < NCH1; ++c) {
-              const int idx = lane + 32 * c;
-              if (idx < nch1) {
-                const ChunkQ qg = chunk_q<FMT>(ex + a.lay.gu_s, j, idx, a.H);
-                const ChunkQ qu = chunk_q<FMT>(ex + a.lay.gu_s, a.I + j, idx, a.H);
-                g += chunk_dot<FMT, true>(gw[c], xr + idx * (EPC / 8), qg);
-                u += chunk_dot<FMT, true>(uw[c], xr + idx * (EPC / 8), qu);
+              for (int c = 0; c < NCH1; ++c) {
+                const int idx = lane + 32 * c;
+                if (idx < nch1) {
+                  const float2 d = gu_dot_bf16(gw[c], uw[c], lds128(xr + idx));
+                  g += d.x;
+                  u += d.y;
+                }
+              }
+            } else {
+#pragma unroll
+              for (int c = 0; c < NCH1; ++c) {
+                const int idx = lane + 32 * c;
+                if (idx < nch1) {
+                  const ChunkQ qg = chunk_q<FMT>(ex + a.lay.gu_s, j, idx, a.H);
+                  const ChunkQ qu = chunk_q<FMT>(ex + a.lay.gu_s, a.I + j, idx, a.H);
+                  g += chunk_dot<FMT, kSrcShared>(gw[c], xr + idx * (EPC / 8), qg);
+                  u += chunk_dot<FMT, kSrcShared>(uw[c], xr + idx * (EPC / 8), qu);
+                }
               }
             }
             g = warp_sum(g);
             u = warp_sum(u);
-            if (lane == 0) a.ws.h[(size_t)gp * a.I + j] = __float2bfloat16_rn(silu_mul(g, u));
+            if (lane == 0) {
+              const __nv_bfloat16 hb = __float2bfloat16_rn(silu_mul(g, u));
+              const unsigned long long bits = (unsigned long long)__bfloat16_as_ushort(hb);
+              st_relaxed_u64(a.ws.hq + (size_t)gp * a.I + j, (tag << 16) | bits);
+            }
           }
         }
-        group_sync(grp);
-        if (wl == 0 && lane == 0) {
-          mb_arrive(&empty[s]);
-          // publish this group's finished rows once per expert (a release costs a round
-          // trip to L2): when its next chunk is another expert or not a phase-1 chunk
-          pending_rows += cd.w;
-          const int kn = k + 2;
-          if (kn >= ch.n1 || chunks[kn].y != cd.y) {
-            red_release_add(done + we.x, (unsigned)pending_rows);
-            pending_rows = 0;
-          }
-        }
-      } else {
-        const uint4* hs = reinterpret_cast<const uint4*>(st + h_off);
-        for (int gp = we.z; gp < we.w; ++gp) {
-          const uint4* hq = hs + (size_t)(gp - we.z) * (a.I / 8);
-          for (int rr = wl; rr < cd.w; rr += 4) {
-            const uint4* row = reinterpret_cast<const uint4*>(st + (size_t)rr * rbd);
-            const int n = cd.z + rr;
+      } else if (cd.w > 0) {
+        if (first_down && warp == 0 && lane == 0) DF_TRACE(3);
+        first_down = false;
+        // the fetcher stored the h rows of the expert's first T pairs after the W_d
+        // rows; further pairs (an expert routed twice by one token) read theirs here
+        const uint4* hsv = reinterpret_cast<const uint4*>(st + (size_t)cd.w * rbd);
+        for (int rr = first; rr < cd.w && ok; rr += kDfConsumerWarps) {
+          const uint4* row = reinterpret_cast<const uint4*>(st + (size_t)rr * rbd);
+          const int n_out = cd.z + rr;
+          for (int gp = we.z; gp < we.w && ok; ++gp) {
+            const int pi = gp - we.z;
             float acc = 0.f;
 #pragma unroll
             for (int c = 0; c < NCH2; ++c) {
               const int idx = lane + 32 * c;
               if (idx < nch2) {
-                const ChunkQ q = chunk_q<FMT>(ex + a.lay.d_s, n, idx, a.I);
-                acc += chunk_dot<FMT, true>(row[idx], hq + idx * (EPC / 8), q);
+                const ChunkQ q = chunk_q<FMT>(ex + a.lay.d_s, n_out, idx, a.I);
+                if (pi < a.T) {
+                  acc += chunk_dot<FMT, kSrcShared>(lds128(row + idx), hsv + (size_t)pi * (a.I / 8) + idx * (EPC / 8), q);
+                } else {
+                  uint4 hv[EPC / 8];
+                  ok = ok && fetch_h_direct(a.ws.hq + (size_t)gp * a.I + (size_t)idx * EPC, tag, hv, EPC / 8,
+                                            abort_flag, a.err);
+                  acc += chunk_dot<FMT, kSrcRegs>(lds128(row + idx), hv, q);
+                }
               }
             }
             acc = warp_sum(acc);
             if (lane == 0) {
-              if (fuse) o_s[gp * kDfMaxRows + (n - ch.n_lo)] = acc;
-              else a.ws.o_part[(size_t)gp * a.H + n] = acc;
+              if (fuse) o_s[gp * kDfMaxRows + (n_out - r_lo)] = acc;
+              else a.ws.o_part[(size_t)gp * a.H + n_out] = acc;
             }
           }
         }
-        group_sync(grp);
-        if (wl == 0 && lane == 0) mb_arrive(&empty[s]);
       }
+      __syncwarp();
+      if (lane == 0) {
+        if (warp == 0) DF_CHUNK(k, 3);
+        mb_arrive(&s_empty[s]);
+      }
+      if (!__all_sync(0xffffffffu, ok)) break;
     }
     consumers_sync();
-    if (threadIdx.x == 0) DF_TRACE(4);
+    if (tid == 0) DF_TRACE(4);
     if (fuse && !*abort_flag) {
-      const int rows = ch.n_hi - ch.n_lo;
-      for (int idx = threadIdx.x; idx < a.T * rows; idx += 256) {
+      const int rows = r_hi - r_lo;
+      for (int idx = tid; idx < a.T * rows; idx += kDfConsumerWarps * 32) {
         const int t = idx / rows, nl = idx - t * rows;
         float acc = 0.f;
         for (int r = 0; r < a.top_k; ++r) {
           const int gp = s_pos[t * a.top_k + r];
           if (gp < 0) continue;
-          acc = fmaf(a.w[t * a.top_k + r], o_s[gp * kDfMaxRows + nl], acc);
+          acc = fmaf(s_w[t * a.top_k + r], o_s[gp * kDfMaxRows + nl], acc);
         }
-        const size_t off = (size_t)t * a.H + ch.n_lo + nl;
-        if (a.residual != nullptr) acc = __bfloat162float(a.residual[off]) + acc;
-        a.y[off] = __float2bfloat16_rn(acc);
+        if (a.residual != nullptr) acc = __bfloat162float(res_s[t * kDfMaxRows + nl]) + acc;
+        a.y[(size_t)t * a.H + r_lo + nl] = __float2bfloat16_rn(acc);
       }
     }
-  }
-  // the last CTA out resets the completion counters for the next launch
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    const unsigned prev = atom_acq_rel_add(a.ws.gbar, 1u);
-    if (prev == gridDim.x - 1) {
-      for (int i = 0; i < n_we; ++i) done[s_we[i].x] = 0u;
-      atomicExch(a.ws.gbar, 0u);
-      __threadfence();
-    }
-    DF_TRACE(5);
+    if (tid == 0) DF_TRACE(5);
   }
 }
 
@@ -487,8 +737,8 @@ cudaError_t launch_df(const DfArgs& a, int grid, size_t smem, cudaStream_t s) {
   auto k = decode_fused_kernel<FMT, NCH1, NCH2>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  // cooperative (all CTAs co-resident), launched through cudaLaunchKernelEx so that the
-  // launch can also be recorded into a CUDA graph
+  // cooperative (all CTAs co-resident: the down chunks wait for other CTAs' gate/up
+  // rows), launched through cudaLaunchKernelEx so that it can be recorded into a graph
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kDfThreads);
@@ -506,8 +756,35 @@ size_t fmt_row_bytes(int fmt, int n) {
   return fmt == PMOE_BF16 ? (size_t)n * 2 : fmt == PMOE_FP8_BLOCK128 ? (size_t)n : (size_t)n / 2;
 }
 
-size_t df_fixed_smem(int T, int H) {
-  return (size_t)T * H * 2 + kDfMaxPairs * kDfMaxRows * 4 + 2 * kDfMaxStages * 8 + 16 + kDfMaxChunks * sizeof(int4);
+// Launch geometry: chunks per gate/up part (cg) and per down part (cd), each at most
+// kDfMaxChunkBytes, the fixed shared-memory areas and the byte ring that fills the rest.
+struct DfGeom {
+  int cg, cd;
+  size_t fixed, ring;
+};
+
+bool df_geometry(int fmt, int T, int top_k, int H, int I, int G, DfGeom* g) {
+  if (T < 1 || T * top_k > kDfMaxPairs || G < 1 || G > 1024 || H % 8 != 0 || I % 8 != 0) return false;
+  if (H >= (1 << 20) || I >= (1 << 20)) return false;  // the schedule's 32-bit products
+  const size_t rbg = fmt_row_bytes(fmt, H), rbd = fmt_row_bytes(fmt, I);
+  if (rbg % 16 != 0 || rbd % 16 != 0) return false;
+  if (2 * rbg > (size_t)kDfMaxChunkBytes || rbd > (size_t)kDfMaxChunkBytes) return false;
+  const int nch1 = (int)(rbg / 16), nch2 = (int)(rbd / 16);
+  if (nch1 > 32 * 8 || nch2 > 32 * 4) return false;
+  const long long gu_rows = (I + G - 1) / G, d_rows = (H + G - 1) / G;
+  if (d_rows > kDfMaxRows) return false;
+  const long long rj = kDfMaxChunkBytes / (2 * (long long)rbg), rd = kDfMaxChunkBytes / (long long)rbd;
+  g->cg = (int)std::max(1LL, (gu_rows + rj - 1) / rj);
+  g->cd = (int)std::max(1LL, (d_rows + rd - 1) / rd);
+  if ((long long)T * top_k * (g->cg + g->cd) > kDfMaxChunks) return false;
+  if (T > kDfMaxTokens) return false;
+  g->fixed = (size_t)T * H * 2 + (size_t)kDfMaxPairs * kDfMaxRows * 4 + (size_t)kDfMaxTokens * kDfMaxRows * 2 +
+             (size_t)kDfMaxChunks * sizeof(int4);
+  // a down chunk also holds the h rows of up to T pairs
+  const size_t max_chunk = std::max((size_t)kDfMaxChunkBytes, (size_t)kDfMaxChunkBytes + (size_t)T * I * 2 + 128);
+  if (g->fixed + 2 * max_chunk > kDfSmemBudget) return false;
+  g->ring = ((kDfSmemBudget - g->fixed) / 128) * 128;
+  return true;
 }
 
 }  // namespace
@@ -516,33 +793,24 @@ size_t df_fixed_smem(int T, int H) {
 extern "C" __attribute__((visibility("default"))) int pmoe_debug_decode_trace(unsigned long long* out, int n_ctas) {
   return cudaMemcpyFromSymbol(out, g_df_trace, (size_t)n_ctas * 8 * sizeof(unsigned long long)) == cudaSuccess ? 0 : -4;
 }
+extern "C" __attribute__((visibility("default"))) int pmoe_debug_decode_chunks(unsigned long long* out, int n_ctas) {
+  return cudaMemcpyFromSymbol(out, g_df_chunk, (size_t)n_ctas * 256 * 4 * sizeof(unsigned long long)) == cudaSuccess
+             ? 0
+             : -4;
+}
 #endif
 
 bool decode_fused_supported(int fmt, int T, int top_k, int H, int I, int num_sms) {
-  if (T < 1 || T * top_k > kDfMaxPairs || num_sms < 1 || num_sms > 1024) return false;
-  if ((H + num_sms - 1) / num_sms > kDfMaxRows) return false;
-  const size_t rbg = fmt_row_bytes(fmt, H), rbd = fmt_row_bytes(fmt, I);
-  if (rbg % 16 != 0 || rbd % 16 != 0) return false;
-  if (2 * rbg > (size_t)kDfStageBytes) return false;
-  const size_t h_room = (size_t)T * I * 2;
-  if (h_room + rbd > (size_t)kDfStageBytes) return false;
-  const int nch1 = (int)(rbg / 16), nch2 = (int)(rbd / 16);
-  if (nch1 > 32 * 8 || nch2 > 32 * 4) return false;
-  const size_t budget = 225 * 1024;  // leaves room for the static shared arrays
-  if (df_fixed_smem(T, H) + 2 * (size_t)kDfStageBytes > budget) return false;
-  // chunk list bound: every expert contributes ceil(rows/rj1) + ceil(out rows/rd) chunks
-  const long long n_we = (long long)T * top_k;
-  const long long rj1 = kDfStageBytes / (2 * (long long)rbg);
-  const long long rd = (kDfStageBytes - (long long)h_room) / (long long)rbd;
-  const long long nrows = (H + num_sms - 1) / num_sms;
-  const long long bound = (n_we * ((I + rj1 - 1) / rj1) + num_sms - 1) / num_sms + n_we * ((nrows + rd - 1) / rd);
-  return bound <= kDfMaxChunks;
+  DfGeom g;
+  return df_geometry(fmt, T, top_k, H, I, num_sms, &g);
 }
 
 cudaError_t launch_decode_fused(int fmt, const __nv_bfloat16* x, const int32_t* ids, const float* w,
                                 const __nv_bfloat16* residual, __nv_bfloat16* y, int T, int top_k, int H, int I,
                                 const int32_t* plan, int E, int wave, int sub, int fuse_combine, const Workspace& ws,
                                 const uint8_t* arena, size_t stride, int32_t* err, int num_sms, cudaStream_t s) {
+  DfGeom g;
+  if (!df_geometry(fmt, T, top_k, H, I, num_sms, &g)) return cudaErrorInvalidValue;
   DfArgs a;
   a.x = x;
   a.ids = ids;
@@ -557,19 +825,16 @@ cudaError_t launch_decode_fused(int fmt, const __nv_bfloat16* x, const int32_t* 
   a.wave = wave;
   a.sub = sub;
   a.fuse_combine = fuse_combine;
+  a.ring_bytes = (int)g.ring;
+  a.cg = g.cg;
+  a.cd = g.cd;
   a.plan = plan;
   a.ws = ws;
   a.arena = arena;
   a.stride = stride;
   a.lay = expert_layout(fmt, H, I);
   a.err = err;
-  const size_t fixed = df_fixed_smem(T, H);
-  const size_t budget = 225 * 1024;  // leaves room for the static shared arrays
-  int stages = (int)((budget - fixed) / kDfStageBytes);
-  if (stages > kDfMaxStages) stages = kDfMaxStages;
-  if (stages < 2) return cudaErrorInvalidValue;
-  a.stages = stages;
-  const size_t smem = (size_t)stages * kDfStageBytes + fixed;
+  const size_t smem = g.ring + g.fixed;
   const int nch1 = (int)(fmt_row_bytes(fmt, H) / 16), nch2 = (int)(fmt_row_bytes(fmt, I) / 16);
 #define PMOE_DF(F, A, B) return launch_df<F, A, B>(a, num_sms, smem, s)
   if (fmt == PMOE_BF16) {

@@ -73,8 +73,8 @@ __global__ void __launch_bounds__(256) gemv_gateup_kernel(const __nv_bfloat16* _
           if (idx < nch) {
             const ChunkQ qg = chunk_q<FMT>(ex + lay.gu_s, j0 + r, idx, H);
             const ChunkQ qu = chunk_q<FMT>(ex + lay.gu_s, I + j0 + r, idx, H);
-            g += chunk_dot<FMT, true>(gw[r][c], xr + idx * (EPC / 8), qg);
-            u += chunk_dot<FMT, true>(uw[r][c], xr + idx * (EPC / 8), qu);
+            g += chunk_dot<FMT, kSrcShared>(gw[r][c], xr + idx * (EPC / 8), qg);
+            u += chunk_dot<FMT, kSrcShared>(uw[r][c], xr + idx * (EPC / 8), qu);
           }
         }
         g = warp_sum(g);
@@ -128,7 +128,7 @@ __global__ void __launch_bounds__(256) gemv_down_kernel(int H, int I, const int3
           const int idx = lane + 32 * c;
           if (idx < nch) {
             const ChunkQ q = chunk_q<FMT>(ex + lay.d_s, n0 + r, idx, I);
-            acc[r] += chunk_dot<FMT, false>(wr[r][c], hr + idx * (EPC / 8), q);
+            acc[r] += chunk_dot<FMT, kSrcGlobal>(wr[r][c], hr + idx * (EPC / 8), q);
           }
         }
         acc[r] = warp_sum(acc[r]);

@@ -13,6 +13,7 @@ namespace pmoe {
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxTopK = 32;
 constexpr int kGemvMaxTokens = 8;  // decode (weight-streaming) path for T <= this
+constexpr int kDecodeMaxPairs = 64;  // T * top_k of the fused decode kernel
 
 // Device error word bits.
 enum : int32_t { kErrBadExpertId = 1, kErrPlanOverflow = 2, kErrBadSlot = 4, kErrPullTimeout = 8 };
@@ -33,7 +34,10 @@ struct PlanLayout {
   __host__ __device__ int words() const { return 8 + 8 * E + 3; }
 };
 // header words
-enum { kPlanUnique = 0, kPlanWaves = 1, kPlanMisses = 2, kPlanError = 3, kPlanStep = 4 };
+// kPlanEpochLo/Hi: a number the residency kernel draws from a cache-wide counter on
+// every call, unique per plan; the fused decode kernel tags its intermediate rows with it.
+enum { kPlanUnique = 0, kPlanWaves = 1, kPlanMisses = 2, kPlanError = 3, kPlanStep = 4, kPlanEpochLo = 5,
+       kPlanEpochHi = 6 };
 
 // One layer's device LRU state.
 struct LayerState {
@@ -57,8 +61,10 @@ struct Workspace {
   float* o_part;        // [P][H] per-pair down-projection outputs, grouped order
   __nv_bfloat16* x_perm;  // [P][H] tokens gathered in grouped order (tensor-core path)
   int32_t* chunk_cnt;   // [ceil(P/256)][E] per-chunk histograms / prefixes (large-P grouping)
-  unsigned* gbar;       // [2] exit counter of the fused decode kernel (zeroed once, reset by its last CTA)
-  unsigned* done;       // [E] per-expert count of finished h rows in a fused decode launch (same reset)
+  // [min(P, 64)][I] fused-decode intermediate rows, one 64-bit word per element: bf16 bits
+  // in the low 16, the launch's 48-bit tag above (zeroed once; tag 0 is never issued)
+  unsigned long long* hq;
+  unsigned long long* epoch;  // [1] counter the residency kernel draws plan epochs from
   int chunk_cap;        // entries of chunk_cnt
   int max_tiles;
 };
@@ -67,7 +73,7 @@ struct Workspace {
 cudaError_t launch_router_topk(const float* logits, int T, int E, int top_k, int renorm,
                                int32_t* ids, float* w, cudaStream_t s);
 cudaError_t launch_residency(const int32_t* ids, int n_ids, int E, int K, LayerState st,
-                             int32_t* plan, int32_t* err, cudaStream_t s);
+                             int32_t* plan, int32_t* err, unsigned long long* epoch, cudaStream_t s);
 cudaError_t launch_group(const int32_t* ids, int P, int E, const int32_t* plan, Workspace ws,
                          int tile_n, int32_t* err, cudaStream_t s);
 cudaError_t launch_gather_rows(const __nv_bfloat16* x, const int32_t* perm, int P, int top_k, int H,

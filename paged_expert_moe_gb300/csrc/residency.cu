@@ -53,7 +53,8 @@ __device__ int block_exclusive_scan(int v, int* s_warp, int* total) {
 
 __global__ void __launch_bounds__(kThreads) residency_kernel(const int32_t* __restrict__ ids, int n_ids, int E,
                                                              int K, LayerState st, int32_t* __restrict__ plan,
-                                                             int32_t* __restrict__ err) {
+                                                             int32_t* __restrict__ err,
+                                                             unsigned long long* __restrict__ epoch) {
   __shared__ int s_pend[kMaxExperts];
   __shared__ int s_slot_of[kMaxExperts];
   __shared__ int s_exp_in[kMaxExperts];
@@ -157,6 +158,9 @@ __global__ void __launch_bounds__(kThreads) residency_kernel(const int32_t* __re
     plan[kPlanMisses] = n_miss;
     plan[kPlanError] = s_bad ? kErrBadExpertId : 0;
     plan[kPlanStep] = step;
+    const unsigned long long ep = atomicAdd(epoch, 1ull) + 1ull;
+    plan[kPlanEpochLo] = (int32_t)(uint32_t)(ep & 0xffffffffull);
+    plan[kPlanEpochHi] = (int32_t)(uint32_t)(ep >> 32);
     if (s_bad) atomicOr(err, kErrBadExpertId);
     *st.step = step + 1;
     st.counters[0] += (unsigned long long)(n_unique - n_miss);
@@ -174,14 +178,14 @@ __global__ void __launch_bounds__(kThreads) residency_kernel(const int32_t* __re
 }  // namespace
 
 cudaError_t launch_residency(const int32_t* ids, int n_ids, int E, int K, LayerState st, int32_t* plan,
-                             int32_t* err, cudaStream_t s) {
+                             int32_t* err, unsigned long long* epoch, cudaStream_t s) {
   static bool carveout_set = false;  // keep room for a decode CTA on the same SM
   if (!carveout_set) {
     cudaFuncSetAttribute(residency_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                          (int)cudaSharedmemCarveoutMaxShared);
     carveout_set = true;
   }
-  residency_kernel<<<1, kThreads, 0, s>>>(ids, n_ids, E, K, st, plan, err);
+  residency_kernel<<<1, kThreads, 0, s>>>(ids, n_ids, E, K, st, plan, err, epoch);
   return cudaGetLastError();
 }
 

@@ -286,3 +286,29 @@ def test_host_side_fault_injection(pm, monkeypatch):
         if e >= 0:
             assert np.array_equal(cache.expert_cache_read_slot(0, s), L.store[e])
     cache.close()
+
+
+@pytest.mark.parametrize("E,H,I,T,k,ids_list,Ks", [
+    (16, 256, 128, 2, 4, [[3, 3, 3, 5], [3, 7, 3, 9]], [16, 4, 2]),
+    (128, 2048, 768, 1, 8, [[3, 3, 5, 6, 7, 8, 9, 3]], [40, 8]),
+])
+def test_expert_repeated_within_a_token(pm, E, H, I, T, k, ids_list, Ks):
+    """ids that name one expert several times for a token are a sum of repeated terms:
+    the decode path handles an expert with more pairs than tokens, at several K."""
+    L = hz.SyntheticLayer(0, E, H, I, seed=77)
+    rng = np.random.default_rng(77)
+    x_bits = gen.activations_bf16(rng, T, H)
+    ids_np = np.asarray(ids_list, dtype=np.int32)
+    w_np = rng.uniform(0.05, 1.0, size=(T, k)).astype(np.float32)
+    ref = L.oracle_y(x_bits, ids_np, w_np.astype(np.float64))
+    outs = []
+    for K in Ks:
+        cache = hz.make_cache([L], k, K, max_tokens=T)
+        y = cache.moe_paged_forward(0, hz.to_device_bf16(x_bits), torch.from_numpy(ids_np).cuda(),
+                                    torch.from_numpy(w_np).cuda())
+        torch.cuda.synchronize()
+        hz.assert_layer_close(hz.bf16_to_f64(y), ref, 0)
+        outs.append(y.clone())
+        cache.close()
+    for y in outs[1:]:
+        assert torch.equal(y.view(torch.int16), outs[0].view(torch.int16))
