@@ -122,6 +122,7 @@ struct pmoe_cache {
   int32_t* err_dev = nullptr;
   std::vector<cudaEvent_t> ev_plan, ev_layer_done, ev_ready;
   std::vector<int> staged, staged_waves, layer_used;
+  std::vector<int> pull_deferred;  // the staged step's wave-0 page-in is left to the fused decode kernel
   cudaEvent_t ev_ids = nullptr, ev_wave_done = nullptr, ev_stack = nullptr;
   Workspace ws{};
   void* ws_buf = nullptr;
@@ -249,7 +250,9 @@ int issue_copies(pmoe_cache* c, int layer, int wave) {
 int flush_staged(pmoe_cache* c, int layer) {
   if (!c->staged[layer]) return PMOE_OK;
   c->staged[layer] = 0;
-  for (int wv = 1; wv < c->staged_waves[layer]; ++wv) {
+  const int first = c->pull_deferred[layer] ? 0 : 1;
+  c->pull_deferred[layer] = 0;
+  for (int wv = first; wv < c->staged_waves[layer]; ++wv) {
     if (c->d.pagein_mode == PMOE_PAGEIN_COPY_ENGINE) {
       const int r = issue_copies(c, layer, wv);
       if (r != PMOE_OK) return r;
@@ -345,6 +348,7 @@ int expert_cache_create(const pmoe_cache_desc* desc, pmoe_cache** out) {
   c->ev_ready.assign(Lr, nullptr);
   c->staged.assign(Lr, 0);
   c->staged_waves.assign(Lr, 0);
+  c->pull_deferred.assign(Lr, 0);
   c->layer_used.assign(Lr, 0);
   int status = PMOE_OK;
 #define PMOE_TRY(call)              \
@@ -532,9 +536,11 @@ int expert_cache_reset(pmoe_cache* c, int layer) {
 namespace {
 
 // The residency step of `layer`, ordered after `ids_ready` (the ids' producer) and after
-// the layer's previous forward.
+// the layer's previous forward. defer_pull (SM-pull mode): leave the page-in of the
+// step's waves to the fused decode kernel, which copies each missing expert's bytes as
+// its chunks need them.
 int ensure_resident_impl(pmoe_cache* c, int layer, const int32_t* ids, int n_ids, cudaEvent_t ids_ready,
-                         int* waves_out);
+                         int* waves_out, bool defer_pull = false);
 
 }  // namespace
 
@@ -556,7 +562,7 @@ int expert_cache_ensure_resident(pmoe_cache* c, int layer, const int32_t* ids, i
 namespace {
 
 int ensure_resident_impl(pmoe_cache* c, int layer, const int32_t* ids, int n_ids, cudaEvent_t ids_ready,
-                         int* waves_out) {
+                         int* waves_out, bool defer_pull) {
   if (c == nullptr || layer < 0 || layer >= c->d.num_layers || n_ids < 0 ||
       n_ids > c->d.max_tokens * c->d.top_k || (n_ids > 0 && ids == nullptr))
     return PMOE_EINVAL;
@@ -612,9 +618,12 @@ int ensure_resident_impl(pmoe_cache* c, int layer, const int32_t* ids, int n_ids
     // the plan is on the device now: compute on the resident experts may start while the
     // pull kernel brings the missing ones
     PMOE_CUDA(cudaEventRecord(c->ev_plan[layer], c->copy_stream));
-    KernelMark km(c, PMOE_K_PULL, c->copy_stream);
-    PMOE_CUDA(launch_pull_pages(c->plan_dev[layer], c->d.num_experts, 0, c->host_store_dev[layer], c->stride,
-                                c->expert_bytes, c->arena[layer], c->err_dev, c->copy_stream));
+    c->pull_deferred[layer] = defer_pull ? 1 : 0;
+    if (!defer_pull) {
+      KernelMark km(c, PMOE_K_PULL, c->copy_stream);
+      PMOE_CUDA(launch_pull_pages(c->plan_dev[layer], c->d.num_experts, 0, c->host_store_dev[layer], c->stride,
+                                  c->expert_bytes, c->arena[layer], c->err_dev, c->copy_stream));
+    }
   }
   PMOE_CUDA(cudaEventRecord(c->ev_ready[layer], c->copy_stream));
   c->staged[layer] = 1;
@@ -638,16 +647,22 @@ int moe_paged_forward(pmoe_cache* c, int layer, const void* x, int T, const int3
   c->in_capture = stream_capturing(s);
   const int k = c->d.top_k, P = T * k, E = c->d.num_experts, H = c->d.hidden, I = c->d.intermediate;
   int status = PMOE_OK;
+  const bool tc = c->use_tc && T > kGemvMaxTokens;
+  const bool fused = !tc && decode_fused_supported(c->d.format, T, k, H, I, c->num_sms);
+  const bool ce = c->d.pagein_mode == PMOE_PAGEIN_COPY_ENGINE;
   if (!c->staged[layer]) {
-    const int r = expert_cache_ensure_resident(c, layer, ids, P, stream, nullptr);
+    // no step was staged ahead: plan it now; in SM-pull mode the fused decode kernel then
+    // pages the missing experts in itself, overlapping the host link with the resident
+    // experts' weight streaming
+    PMOE_CUDA(cudaEventRecord(c->ev_ids, s));
+    const int r = ensure_resident_impl(c, layer, ids, P, c->ev_ids, nullptr, fused && !ce);
     if (r == PMOE_EDEVICE) status = r;
     else if (r != PMOE_OK) return r;
   }
   c->staged[layer] = 0;
+  const bool pull_in_kernel = c->pull_deferred[layer] != 0;
+  c->pull_deferred[layer] = 0;
   const int nw = c->staged_waves[layer];
-  const bool tc = c->use_tc && T > kGemvMaxTokens;
-  const bool fused = !tc && decode_fused_supported(c->d.format, T, k, H, I, c->num_sms);
-  const bool ce = c->d.pagein_mode == PMOE_PAGEIN_COPY_ENGINE;
   // Copy-engine steps whose first wave has both resident and paged-in experts compute
   // the resident ones while the copies are still in flight (the plan lists them first).
   // (SM-pull mode: the host does not know the split, and launching both parts
@@ -678,7 +693,8 @@ int moe_paged_forward(pmoe_cache* c, int layer, const void* x, int T, const int3
       KernelMark km(c, PMOE_K_DECODE, s);
       PMOE_CUDA(launch_decode_fused(c->d.format, (const __nv_bfloat16*)x, ids, w, (const __nv_bfloat16*)residual,
                                     (__nv_bfloat16*)y, T, k, H, I, c->plan_dev[layer], E, wv, sub, fuse_combine,
-                                    c->ws, c->arena[layer], c->stride, c->err_dev, c->num_sms, s));
+                                    c->ws, c->arena[layer], c->host_store_dev[layer], pull_in_kernel ? 1 : 0,
+                                    c->stride, c->err_dev, c->num_sms, s));
     } else {
       {
         KernelMark km(c, PMOE_K_GATEUP, s);
@@ -704,7 +720,7 @@ int moe_paged_forward(pmoe_cache* c, int layer, const void* x, int T, const int3
     PMOE_CUDA(launch_gather_rows((const __nv_bfloat16*)x, c->ws.perm, P, k, H, c->ws.x_perm, s));
   }
   for (int wv = 0; wv < nw; ++wv) {
-    if (wv > 0) {
+    if (wv > 0 && !pull_in_kernel) {
       PMOE_CUDA(cudaEventRecord(c->ev_wave_done, s));
       PMOE_CUDA(cudaStreamWaitEvent(c->copy_stream, c->ev_wave_done, 0));
       if (ce) {

@@ -46,22 +46,33 @@ struct ChunkQ {
   float s, z;
 };
 
-template <int FMT>
+// COHERENT: the scales may have been written earlier in the same launch (an expert the
+// launch pages in itself), so they are read through L2 rather than the read-only path.
+template <int FMT, bool COHERENT = false>
 __device__ __forceinline__ ChunkQ chunk_q(const uint8_t* scales, int row, int c, int cols) {
   ChunkQ q{1.f, 0.f};
   if constexpr (FMT == PMOE_FP8_BLOCK128) {
-    const float* S = reinterpret_cast<const float*>(scales);
-    q.s = __ldg(S + (size_t)(row >> 7) * (cols >> 7) + ((c * 16) >> 7));
+    const float* S = reinterpret_cast<const float*>(scales) + (size_t)(row >> 7) * (cols >> 7) + ((c * 16) >> 7);
+    if constexpr (COHERENT) {
+      asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(q.s) : "l"(S));
+    } else {
+      q.s = __ldg(S);
+    }
   } else if constexpr (FMT == PMOE_INT4_GPTQ_G128) {
-    const __half2* SZ = reinterpret_cast<const __half2*>(scales);
-    const float2 sz = __half22float2(SZ[(size_t)row * (cols >> 7) + ((c * 32) >> 7)]);
+    const __half2* SZ = reinterpret_cast<const __half2*>(scales) + (size_t)row * (cols >> 7) + ((c * 32) >> 7);
+    uint32_t raw;
+    if constexpr (COHERENT) {
+      asm volatile("ld.global.cg.u32 %0, [%1];" : "=r"(raw) : "l"(SZ));
+    } else {
+      raw = *reinterpret_cast<const uint32_t*>(SZ);
+    }
+    const float2 sz = __half22float2(*reinterpret_cast<const __half2*>(&raw));
     q.s = sz.x;
     q.z = sz.y;
   }
   return q;
 }
 
-// sum over the chunk's elements of w_i * a_i, with a (bf16) read from `av` (EPC/8 uint4).
 // Where chunk_dot reads its activations from.
 enum : int { kSrcGlobal = 0, kSrcShared = 1, kSrcRegs = 2 };
 

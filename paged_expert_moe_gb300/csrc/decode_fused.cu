@@ -43,8 +43,10 @@ namespace {
 
 using namespace dec;
 
-constexpr int kDfConsumerWarps = 12;        // warps 0-11 consume, 12 produces, 13 fetches h
-constexpr int kDfThreads = (kDfConsumerWarps + 2) * 32;
+// 16 warps, four per SM sub-partition (whose register file then allows 128 per thread)
+constexpr int kDfConsumerWarps = 11;  // warps 0-10 consume, 11 produces, 12 fetches h, 13-15 page in
+constexpr int kDfPagerWarps = 3;
+constexpr int kDfThreads = (kDfConsumerWarps + 2 + kDfPagerWarps) * 32;
 constexpr int kDfSlots = 16;                // chunks in flight at most (one mbarrier pair each)
 constexpr int kDfMaxChunkBytes = 32 * 1024;  // weight bytes of one chunk
 constexpr int kDfMaxPairs = kDecodeMaxPairs;
@@ -96,7 +98,9 @@ struct DfArgs {
   int cg, cd;      // chunks per gate/up part and per down part
   const int32_t* plan;
   Workspace ws;
-  const uint8_t* arena;
+  uint8_t* arena;
+  const uint8_t* store;  // the layer's mapped host store (pull != 0)
+  int pull;              // page the wave's missing experts in during this launch
   size_t stride;
   ExpertLayout lay;
   int32_t* err;
@@ -178,6 +182,49 @@ __device__ __forceinline__ float2 gu_dot_bf16(uint4 wg, uint4 wu, uint4 xa) {
   }
   float2 r;
   asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(acc));
+  return r;
+}
+
+// Copy of two byte ranges (sizes multiples of 16) from src + off_i to dst + off_i by `nl`
+// cooperating lanes (this thread is lane vl of them), as one sequence with 16 16-byte
+// loads in flight per lane: the source is host memory across the link, so the bytes in
+// flight set the rate, and a whole chunk goes in one round trip.
+__device__ __forceinline__ void lanes_copy16x2(const uint8_t* src, uint8_t* dst, size_t off1, size_t bytes1,
+                                               size_t off2, size_t bytes2, int vl, int nl) {
+  constexpr int U = 10;
+  const size_t n1 = bytes1 / 16, n = n1 + bytes2 / 16;
+  for (size_t base = (size_t)vl; base < n; base += (size_t)nl * U) {
+    uint4 v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const size_t i = base + (size_t)u * nl;
+      if (i < n) v[u] = ld_stream(src + (i < n1 ? off1 + i * 16 : off2 + (i - n1) * 16));
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const size_t i = base + (size_t)u * nl;
+      if (i < n) *reinterpret_cast<uint4*>(dst + (i < n1 ? off1 + i * 16 : off2 + (i - n1) * 16)) = v[u];
+    }
+  }
+}
+// The same for a small range whose size and offset are multiples of 4 (scale rows).
+__device__ __forceinline__ void lanes_copy4(const uint8_t* src, uint8_t* dst, size_t off, size_t bytes, int vl,
+                                            int nl) {
+  for (size_t i = (size_t)vl * 4; i < bytes; i += (size_t)nl * 4)
+    *reinterpret_cast<uint32_t*>(dst + off + i) = *reinterpret_cast<const uint32_t*>(src + off + i);
+}
+__device__ __forceinline__ void pagers_sync() {
+  asm volatile("bar.sync 2, %0;" ::"n"(kDfPagerWarps * 32) : "memory");
+}
+// Barrier among the pager warps that ORs a predicate over them.
+__device__ __forceinline__ int pagers_any(int pred) {
+  int r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.s32 p, %1, 0;\n\tbar.red.or.pred q, 2, %2, p;\n\t"
+      "selp.s32 %0, 1, 0, q;\n\t}\n"
+      : "=r"(r)
+      : "r"(pred), "n"(kDfPagerWarps * 32)
+      : "memory");
   return r;
 }
 
@@ -295,6 +342,7 @@ __global__ void __launch_bounds__(kDfThreads, 1) decode_fused_kernel(const DfArg
   __shared__ __align__(8) uint64_t s_empty[kDfSlots];
   __shared__ int s_abort;
   __shared__ int s_placed;  // chunks placed in the ring so far
+  __shared__ int s_pulled;  // chunks whose bytes this CTA has paged in (missing experts)
 
   const unsigned R = (unsigned)a.ring_bytes;
   uint8_t* ring = dsm;
@@ -348,6 +396,7 @@ __global__ void __launch_bounds__(kDfThreads, 1) decode_fused_kernel(const DfArg
     }
     s_abort = 0;
     s_placed = 0;
+    s_pulled = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
@@ -358,6 +407,8 @@ __global__ void __launch_bounds__(kDfThreads, 1) decode_fused_kernel(const DfArg
   if (a.sub == 1) w1 = w0 + s_hdr[3];
   else if (a.sub == 2) w0 += s_hdr[3];
   const int D = w1 - w0;
+  // wave experts [n_hits, D) are paged in by this launch (the list puts resident ones first)
+  const int n_hits = (a.pull != 0 && a.sub == 0) ? min(s_hdr[3], D) : D;
   if (w0 != 0) {  // not the speculated list: load this wave's part of it
     if (tid < D) s_wl[tid] = make_int2(a.plan[L.wave_exp() + w0 + tid], a.plan[L.wave_slot() + w0 + tid]);
     __syncthreads();
@@ -485,6 +536,21 @@ __global__ void __launch_bounds__(kDfThreads, 1) decode_fused_kernel(const DfArg
         s_off[s] = (unsigned)off;
         head = (unsigned)off + need;
         uint64_t* fb = &s_full[s];
+        if (wbytes != 0 && cd.y >= n_hits) {
+          // an expert this launch pages in: wait until this CTA's pager has written the
+          // chunk's bytes into the slot
+          long long t1 = -1;
+          while (ld_acquire_shared(&s_pulled) <= k && !*abort_flag) {
+            if (t1 < 0) {
+              t1 = clock64();
+            } else if (clock64() - t1 > kDfWaitLimit) {
+              *abort_flag = 1;
+              atomicOr(a.err, kErrDecodeTimeout);
+            }
+            __nanosleep(128);
+          }
+          if (*abort_flag) break;
+        }
         DF_CHUNK(k, 0);
         if (wbytes == 0) {
           mb_arrive(fb);
@@ -594,6 +660,53 @@ __global__ void __launch_bounds__(kDfThreads, 1) decode_fused_kernel(const DfArg
       __syncwarp();
       if (lane == 0) mb_arrive(&s_hrdy[s]);
     }
+  } else if (warp >= kDfConsumerWarps + 2) {
+    // ---------------- pagers: for every chunk of an expert this launch pages in, copy the
+    // bytes the chunk reads (its weight rows and the scale rows they use) from the mapped
+    // host store into the expert's slot, in schedule order, then publish the progress.
+    // Every CTA copies what its own chunks read; together they fill the slot.
+    if (a.pull != 0) {
+      const int vl = tid - (kDfConsumerWarps + 2) * 32, nl = kDfPagerWarps * 32;
+      const int hb = a.H / 128, ib = a.I / 128;
+      for (int k = 0; k < n_chunks; ++k) {
+        const int4 cd = chunks[k];
+        if (cd.y < n_hits || cd.w == 0) continue;
+        if (pagers_any(*abort_flag)) break;  // every pager warp sees the same answer
+        const int4 we = s_we[cd.y];
+        const uint8_t* src = a.store + (size_t)we.x * a.stride;
+        uint8_t* dst = a.arena + (size_t)we.y * a.stride;
+        const int z = cd.z, n = cd.w;
+        if ((cd.x & 3) == 1) {
+          lanes_copy16x2(src, dst, a.lay.gu_w + (size_t)z * rbg, (size_t)n * rbg, a.lay.gu_w + (size_t)(a.I + z) * rbg,
+                         (size_t)n * rbg, vl, nl);
+          if constexpr (FMT == PMOE_FP8_BLOCK128) {
+            const size_t row = 4 * (size_t)hb;  // one block row of scales
+            lanes_copy4(src, dst, a.lay.gu_s + (size_t)(z >> 7) * row,
+                        (size_t)(((z + n - 1) >> 7) - (z >> 7) + 1) * row, vl, nl);
+            lanes_copy4(src, dst, a.lay.gu_s + (size_t)((a.I + z) >> 7) * row,
+                        (size_t)(((a.I + z + n - 1) >> 7) - ((a.I + z) >> 7) + 1) * row, vl, nl);
+          } else if constexpr (FMT == PMOE_INT4_GPTQ_G128) {
+            const size_t row = 4 * (size_t)hb;  // one row's (s, z) pairs
+            lanes_copy4(src, dst, a.lay.gu_s + (size_t)z * row, (size_t)n * row, vl, nl);
+            lanes_copy4(src, dst, a.lay.gu_s + (size_t)(a.I + z) * row, (size_t)n * row, vl, nl);
+          }
+        } else {
+          lanes_copy16x2(src, dst, a.lay.d_w + (size_t)z * rbd, (size_t)n * rbd, 0, 0, vl, nl);
+          if constexpr (FMT == PMOE_FP8_BLOCK128) {
+            const size_t row = 4 * (size_t)ib;
+            lanes_copy4(src, dst, a.lay.d_s + (size_t)(z >> 7) * row,
+                        (size_t)(((z + n - 1) >> 7) - (z >> 7) + 1) * row, vl, nl);
+          } else if constexpr (FMT == PMOE_INT4_GPTQ_G128) {
+            const size_t row = 4 * (size_t)ib;
+            lanes_copy4(src, dst, a.lay.d_s + (size_t)z * row, (size_t)n * row, vl, nl);
+          }
+        }
+        // the stores (generic proxy) are read next by bulk copies (async proxy)
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        pagers_sync();
+        if (vl == 0) asm volatile("st.release.cta.shared.u32 [%0], %1;" ::"r"(su32(&s_pulled)), "r"(k + 1) : "memory");
+      }
+    }
   } else {
     // ---------------- consumers (warps 0 .. kDfConsumerWarps-1): every warp walks every
     // chunk; the rows of the whole list are dealt to the warps round-robin (row i of the
@@ -654,8 +767,8 @@ __global__ void __launch_bounds__(kDfThreads, 1) decode_fused_kernel(const DfArg
               for (int c = 0; c < NCH1; ++c) {
                 const int idx = lane + 32 * c;
                 if (idx < nch1) {
-                  const ChunkQ qg = chunk_q<FMT>(ex + a.lay.gu_s, j, idx, a.H);
-                  const ChunkQ qu = chunk_q<FMT>(ex + a.lay.gu_s, a.I + j, idx, a.H);
+                  const ChunkQ qg = chunk_q<FMT, true>(ex + a.lay.gu_s, j, idx, a.H);
+                  const ChunkQ qu = chunk_q<FMT, true>(ex + a.lay.gu_s, a.I + j, idx, a.H);
                   g += chunk_dot<FMT, kSrcShared>(gw[c], xr + idx * (EPC / 8), qg);
                   u += chunk_dot<FMT, kSrcShared>(uw[c], xr + idx * (EPC / 8), qu);
                 }
@@ -686,7 +799,7 @@ __global__ void __launch_bounds__(kDfThreads, 1) decode_fused_kernel(const DfArg
             for (int c = 0; c < NCH2; ++c) {
               const int idx = lane + 32 * c;
               if (idx < nch2) {
-                const ChunkQ q = chunk_q<FMT>(ex + a.lay.d_s, n_out, idx, a.I);
+                const ChunkQ q = chunk_q<FMT, true>(ex + a.lay.d_s, n_out, idx, a.I);
                 if (pi < a.T) {
                   acc += chunk_dot<FMT, kSrcShared>(lds128(row + idx), hsv + (size_t)pi * (a.I / 8) + idx * (EPC / 8), q);
                 } else {
@@ -808,7 +921,8 @@ bool decode_fused_supported(int fmt, int T, int top_k, int H, int I, int num_sms
 cudaError_t launch_decode_fused(int fmt, const __nv_bfloat16* x, const int32_t* ids, const float* w,
                                 const __nv_bfloat16* residual, __nv_bfloat16* y, int T, int top_k, int H, int I,
                                 const int32_t* plan, int E, int wave, int sub, int fuse_combine, const Workspace& ws,
-                                const uint8_t* arena, size_t stride, int32_t* err, int num_sms, cudaStream_t s) {
+                                uint8_t* arena, const uint8_t* store, int pull, size_t stride, int32_t* err, int num_sms,
+                                cudaStream_t s) {
   DfGeom g;
   if (!df_geometry(fmt, T, top_k, H, I, num_sms, &g)) return cudaErrorInvalidValue;
   DfArgs a;
@@ -831,6 +945,8 @@ cudaError_t launch_decode_fused(int fmt, const __nv_bfloat16* x, const int32_t* 
   a.plan = plan;
   a.ws = ws;
   a.arena = arena;
+  a.store = store;
+  a.pull = (pull != 0 && store != nullptr) ? 1 : 0;
   a.stride = stride;
   a.lay = expert_layout(fmt, H, I);
   a.err = err;

@@ -91,7 +91,8 @@ bool decode_fused_supported(int fmt, int T, int top_k, int H, int I, int num_sms
 cudaError_t launch_decode_fused(int fmt, const __nv_bfloat16* x, const int32_t* ids, const float* w,
                                 const __nv_bfloat16* residual, __nv_bfloat16* y, int T, int top_k, int H, int I,
                                 const int32_t* plan, int E, int wave, int sub, int fuse_combine, const Workspace& ws,
-                                const uint8_t* arena, size_t stride, int32_t* err, int num_sms, cudaStream_t s);
+                                uint8_t* arena, const uint8_t* store, int pull, size_t stride, int32_t* err,
+                                int num_sms, cudaStream_t s);
 cudaError_t launch_pull_pages(const int32_t* plan, int E, int wave, const uint8_t* host_store_dev,
                               size_t stride, size_t expert_bytes, uint8_t* arena, int32_t* err,
                               cudaStream_t s);
