@@ -403,7 +403,7 @@ def run_ours(args):
     pm.load()
     store = make_store()
     hbm_peak, _, peak_kind = _peaks()
-    if args.section in ("prefill", "stack"):
+    if args.section in ("prefill", "stack", "decode_staged"):
         # one part of the bench alone (for profiling); one JSON line with that part
         out = {"metric": METRIC, "impl": "ours", "section": args.section}
         if args.section == "prefill":
@@ -411,9 +411,15 @@ def run_ours(args):
                 {"cold": run_prefill(pm, torch, store, args.prefill_steps, 2, local, cold=True),
                  "warm_all_resident": run_prefill(pm, torch, store, args.prefill_steps, 2, local, K=E, cold=False)},
                 hbm_peak, _peaks()[1])
-        else:
+        elif args.section == "stack":
             out["stack_int4"] = {f"B{B}_graph": run_stack(pm, torch, B, args.stack_steps, 3, local, mode=1, graph=True)
                                  for B in (1, 4)}
+        else:
+            # the decode kernel alone on resident weights (page-in staged ahead): the launches
+            # the roofline is measured on
+            r = run_decode(pm, torch, store, 1, args.steps, args.warmup, local, e2e=False, mode=1, stage=True)
+            out["decode_staged"] = {"ms_per_step": r["ms_per_step"],
+                                    "decode_kernel_us": r["kernel_times"]["decode"]["ms"] / args.steps * 1e3}
         if rank == 0:
             print(json.dumps(out))
         return
@@ -669,7 +675,7 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--prefill-steps", type=int, default=6)
     ap.add_argument("--stack-steps", type=int, default=60)
-    ap.add_argument("--section", default="all", choices=["all", "prefill", "stack"],
+    ap.add_argument("--section", default="all", choices=["all", "prefill", "stack", "decode_staged"],
                     help="run only one part (profiling); the default runs everything")
     args = ap.parse_args()
     if args.warmup < 3:
