@@ -773,8 +773,15 @@ int moe_paged_stack_forward(pmoe_cache* c, const void* x, int T, const int32_t* 
   // every layer's ids are ready once the work already on `stream` is done
   PMOE_CUDA(cudaEventRecord(c->ev_stack, s));
   int status = PMOE_OK;
+  // SM-pull decode: each layer's fused decode kernel pages its own missing experts in,
+  // overlapping the host link with that layer's resident weights (a separate pull
+  // kernel could not run beside it: the decode kernel holds every SM); the residency
+  // steps are still planned one layer ahead
+  const bool tc = c->use_tc && T > kGemvMaxTokens;
+  const bool defer = c->d.pagein_mode == PMOE_PAGEIN_SM_PULL && !tc &&
+                     decode_fused_supported(c->d.format, T, c->d.top_k, c->d.hidden, c->d.intermediate, c->num_sms);
   if (!c->staged[0]) {
-    const int r = ensure_resident_impl(c, 0, ids, P, c->ev_stack, nullptr);
+    const int r = ensure_resident_impl(c, 0, ids, P, c->ev_stack, nullptr, defer);
     if (r == PMOE_EDEVICE) status = r;
     else if (r != PMOE_OK) return r;
   }
@@ -789,7 +796,7 @@ int moe_paged_stack_forward(pmoe_cache* c, const void* x, int T, const int32_t* 
     if (l + 1 < L && !c->staged[l + 1]) {
       // plan and page in layer l+1 while layer l computes (the host's plan read-back in
       // copy-engine mode overlaps the kernels just enqueued)
-      r = ensure_resident_impl(c, l + 1, ids + (size_t)(l + 1) * P, P, c->ev_stack, nullptr);
+      r = ensure_resident_impl(c, l + 1, ids + (size_t)(l + 1) * P, P, c->ev_stack, nullptr, defer);
       if (r == PMOE_EDEVICE) status = r;
       else if (r != PMOE_OK) return r;
     }
