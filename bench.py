@@ -179,10 +179,11 @@ def aggregate(units_per_rank, time_s_per_rank):
 # --------------------------------------------------------------------------- our arm
 
 def run_decode(pm, torch, store, B, steps, warmup, device, timed_clock=None, e2e=True, mode=0, graph=False,
-               stage=False):
+               stage=False, fmt=0):
     trace, xs, logits, distinct = make_inputs(B)
     graph_launches = 0
-    cache = pm.ExpertCache(E, TOPK, H, I, K_SLOTS, fmt=pm.PMOE_BF16, max_tokens=B, device=device, pagein_mode=mode)
+    cache = pm.ExpertCache(E, TOPK, H, I, K_SLOTS, fmt=fmt, max_tokens=B, device=device, pagein_mode=mode)
+    ebytes = pm.pmoe_expert_bytes(fmt, H, I)  # every byte of an expert the decode kernel reads
     cache.load_layer(0, store)
     dev = torch.device("cuda", device)
     x_dev = [torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(dev) for x in xs]
@@ -255,7 +256,7 @@ def run_decode(pm, torch, store, B, steps, warmup, device, timed_clock=None, e2e
         "bytes_paged_per_step": (stats1["bytes_paged"] - stats0["bytes_paged"]) / steps,
         "gateup_weight_bytes": sum(d * 2 * I * H * 2 for d in d_steps),
         "down_weight_bytes": sum(d * H * I * 2 for d in d_steps),
-        "expert_weight_bytes": sum(d * 3 * I * H * 2 for d in d_steps),
+        "expert_weight_bytes": sum(d * ebytes for d in d_steps),
         "launches": (graph_launches * steps if graph else
                      sum(v["launches"] for k_, v in kt.items() if k_ not in ("copies", "pagein_copy")) + steps),
         "mode": ("SM-pull page-in inside the fused decode kernel, whole step replayed as one CUDA graph" if graph else
@@ -310,20 +311,23 @@ def measure_h2d(torch, dev, nbytes=9_437_184, reps=40):
 PREFILL_T, PREFILL_K = 2048, 92
 
 
-def run_prefill(pm, torch, store, steps, warmup, device, K=PREFILL_K, cold=True, n_inputs=3, mode=0):
-    """Config: 2048-token prefill, uniform routing; cold = the table is emptied before every step."""
+def run_prefill(pm, torch, store, steps, warmup, device, K=PREFILL_K, cold=True, n_inputs=3, mode=0, fmt=0,
+                T=None):
+    """Config: T-token prefill (2048 by default), uniform routing; cold = the table is emptied
+    before every step."""
+    T = PREFILL_T if T is None else T
     dev = torch.device("cuda", device)
-    rng = np.random.default_rng([SEED, 2048])
+    rng = np.random.default_rng([SEED, T])
     inputs = []
     for _ in range(n_inputs):
-        sets = gen.uniform_routing_sets(rng, PREFILL_T, E, TOPK)
-        inputs.append((torch.from_numpy(gen.activations_bf16(rng, PREFILL_T, H).view(np.int16)).view(torch.bfloat16).to(dev),
+        sets = gen.uniform_routing_sets(rng, T, E, TOPK)
+        inputs.append((torch.from_numpy(gen.activations_bf16(rng, T, H).view(np.int16)).view(torch.bfloat16).to(dev),
                        torch.from_numpy(gen.logits_for_sets(rng, sets, E)).to(dev)))
-    cache = pm.ExpertCache(E, TOPK, H, I, K, fmt=pm.PMOE_BF16, max_tokens=PREFILL_T, device=device, pagein_mode=mode)
+    cache = pm.ExpertCache(E, TOPK, H, I, K, fmt=fmt, max_tokens=T, device=device, pagein_mode=mode)
     cache.load_layer(0, store)
-    ids = torch.empty((PREFILL_T, TOPK), dtype=torch.int32, device=dev)
-    w = torch.empty((PREFILL_T, TOPK), dtype=torch.float32, device=dev)
-    y = torch.empty((PREFILL_T, H), dtype=torch.bfloat16, device=dev)
+    ids = torch.empty((T, TOPK), dtype=torch.int32, device=dev)
+    w = torch.empty((T, TOPK), dtype=torch.float32, device=dev)
+    y = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
     flush = L2Flush(dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -352,10 +356,10 @@ def run_prefill(pm, torch, store, steps, warmup, device, K=PREFILL_K, cold=True,
     kt = cache.expert_cache_kernel_times()
     s1 = cache.expert_cache_stats(0)
     cache.close()
-    P = PREFILL_T * TOPK
+    P = T * TOPK
     flops_gu = 2.0 * P * 2 * I * H * steps
     flops_d = 2.0 * P * H * I * steps
-    return {"ms_per_step": total_ms / steps, "tokens_per_s": PREFILL_T * steps / (total_ms / 1e3),
+    return {"T": T, "K": K, "ms_per_step": total_ms / steps, "tokens_per_s": T * steps / (total_ms / 1e3),
             "misses_per_step": (s1["misses"] - s0["misses"]) / steps,
             "waves_per_step": (s1["waves"] - s0["waves"]) / steps,
             "bytes_paged_per_step": (s1["bytes_paged"] - s0["bytes_paged"]) / steps,
@@ -403,6 +407,11 @@ def run_ours(args):
     pm.load()
     store = make_store()
     hbm_peak, _, peak_kind = _peaks()
+    if args.section == "fp8":
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "impl": "ours", "section": "fp8", "fp8": run_fp8(pm, torch, args, local,
+                                                                                                  hbm_peak)}))
+        return
     if args.section in ("prefill", "stack", "decode_staged"):
         # one part of the bench alone (for profiling); one JSON line with that part
         out = {"metric": METRIC, "impl": "ours", "section": args.section}
@@ -438,6 +447,7 @@ def run_ours(args):
     others = {}
     prefill = {}
     stack = {}
+    fp8 = None
     h2d = measure_h2d(torch, torch.device("cuda", local))
     if not args.headline_only:
         others["B1_sm_pull_staged_no_graph"] = timed
@@ -451,6 +461,7 @@ def run_ours(args):
         prefill["cold"] = run_prefill(pm, torch, store, args.prefill_steps, 2, local, cold=True)
         prefill["cold_sm_pull"] = run_prefill(pm, torch, store, args.prefill_steps, 2, local, cold=True, mode=1)
         prefill["warm_all_resident"] = run_prefill(pm, torch, store, args.prefill_steps, 2, local, K=E, cold=False)
+        fp8 = run_fp8(pm, torch, args, local, hbm_peak)
         for B in (1, 4):
             stack[f"B{B}"] = run_stack(pm, torch, B, args.stack_steps, 3, local)
             stack[f"B{B}_graph"] = run_stack(pm, torch, B, args.stack_steps, 3, local, mode=1, graph=True)
@@ -509,6 +520,7 @@ def run_ours(args):
                                             (kt["pull"]["ms"] / 1e3) / 1e9) if kt["pull"]["ms"] else None,
                       "decode_pagein_kind": "SM pull kernel (CUDA-event time on the copy stream)"},
         "prefill": _prefill_summary(prefill, hbm_peak, _peaks()[1]) if prefill else None,
+        "fp8": fp8,
         "stack_int4": ({"workload": "48-layer Qwen3-30B-A3B-shaped MoE stack (attention omitted), GPTQ-int4 g128 "
                                     "experts, K=26 slots/layer, p=0.8 reuse routing per layer, residual stream",
                         "hbm_roofline_tokens_per_s_B1": hbm_peak * 1e9 / (STACK_L * TOPK * 2_506_752),
@@ -521,6 +533,29 @@ def run_ours(args):
     if not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline_decode(1, budget_s=args.cpu_budget, store=store)
     print(json.dumps(out))
+
+
+def run_fp8(pm, torch, args, local, hbm_peak):
+    """The block-FP8 configuration: the same layer with e4m3 experts and fp32 128x128 scales,
+    K=40, decode B=1 over the p=0.8 reuse trace, plus a cold 512-token prefill."""
+    store = make_store(fmt=1)
+    ebytes = pm.pmoe_expert_bytes(1, H, I)
+    head = run_decode(pm, torch, store, 1, args.steps, args.warmup, local, e2e=False, mode=1, graph=True, fmt=1)
+    staged = run_decode(pm, torch, store, 1, args.steps, args.warmup, local, e2e=False, mode=1, stage=True, fmt=1)
+    kt = staged["kernel_times"]
+    dec_gbs = staged["expert_weight_bytes"] / (kt["decode"]["ms"] / 1e3) / 1e9
+    pre = run_prefill(pm, torch, store, args.prefill_steps, 2, local, K=40, cold=True, fmt=1, T=512)
+    flop = 2.0 * 512 * TOPK * 3 * H * I
+    return {"workload": "Qwen3-30B-A3B-shaped MoE layer, block-FP8 e4m3 experts (fp32 128x128 scales), K=40",
+            "expert_bytes": ebytes,
+            "decode_B1": {"tokens_per_s": head["tokens_per_s"], "ms_per_step": head["ms_per_step"],
+                          "misses_per_step": head["misses_per_step"], "mode": head["mode"],
+                          "decode_kernel_gbs": dec_gbs, "decode_kernel_hbm_frac": dec_gbs / hbm_peak,
+                          "decode_kernel_us": kt["decode"]["ms"] / args.steps * 1e3,
+                          "decode_kernel_measured_in": "page-in staged ahead by the pull kernel"},
+            "prefill_512_cold": dict(pre, FLOP_per_step=flop, weight_bytes_per_step=E * ebytes,
+                                     hbm_bound_tflops=flop / (E * ebytes / (hbm_peak * 1e9)) / 1e12,
+                                     note="FP8 weights are dequantised to bf16 in shared memory for kind::f16 MMAs")}
 
 
 STACK_L, STACK_K = 48, 26
@@ -675,7 +710,7 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--prefill-steps", type=int, default=6)
     ap.add_argument("--stack-steps", type=int, default=60)
-    ap.add_argument("--section", default="all", choices=["all", "prefill", "stack", "decode_staged"],
+    ap.add_argument("--section", default="all", choices=["all", "prefill", "stack", "decode_staged", "fp8"],
                     help="run only one part (profiling); the default runs everything")
     args = ap.parse_args()
     if args.warmup < 3:
