@@ -684,11 +684,11 @@ int moe_paged_forward(pmoe_cache* c, int layer, const void* x, int T, const int3
       {
         KernelMark km(c, PMOE_K_GATEUP, s);
         PMOE_CUDA(tc_gateup(c->d.format, c->maps[layer], c->ws_maps, c->plan_dev[layer], E, wv, sub, c->ws, I, H,
-                            c->arena[layer], c->stride, c->num_sms, c->err_dev, s));
+                            c->arena[layer], c->stride, c->num_sms, c->err_dev, tc_tile_n(T, k, E), s));
       }
       KernelMark km(c, PMOE_K_DOWN, s);
       PMOE_CUDA(tc_down(c->d.format, c->maps[layer], c->ws_maps, c->plan_dev[layer], E, wv, sub, c->ws, I, H,
-                        c->arena[layer], c->stride, c->num_sms, c->err_dev, s));
+                        c->arena[layer], c->stride, c->num_sms, c->err_dev, tc_tile_n(T, k, E), s));
     } else if (fused) {
       KernelMark km(c, PMOE_K_DECODE, s);
       PMOE_CUDA(launch_decode_fused(c->d.format, (const __nv_bfloat16*)x, ids, w, (const __nv_bfloat16*)residual,
@@ -713,7 +713,7 @@ int moe_paged_forward(pmoe_cache* c, int layer, const void* x, int T, const int3
   PMOE_CUDA(cudaStreamWaitEvent(s, split0 ? c->ev_plan[layer] : c->ev_ready[layer], 0));
   if (!fused) {  // the fused decode kernel groups the pairs itself
     KernelMark km(c, PMOE_K_GROUP, s);
-    PMOE_CUDA(launch_group(ids, P, E, c->plan_dev[layer], c->ws, tc ? kTcMaxN : 0, c->err_dev, s));
+    PMOE_CUDA(launch_group(ids, P, E, c->plan_dev[layer], c->ws, tc ? tc_tile_n(T, k, E) : 0, c->err_dev, s));
   }
   if (tc) {
     KernelMark km(c, PMOE_K_GATHER, s);

@@ -138,22 +138,29 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
-// Stage: A = 128 weight rows x 64 K (16 KB) + B = up to 256 pair rows x 64 K (32 KB).
+// Stage: A = 128 weight rows x 64 K (16 KB) + B = up to NMAX pair rows x 64 K (NMAX = 256:
+// 32 KB; NMAX = 64, used when a forward has few tokens per expert: 8 KB, which leaves room
+// for twice the stages and so hides twice the latency).
 // Gate/up A tiles hold 64 gate rows (TMEM lanes 0-63) then the matching 64 up rows
 // (lanes 64-127), so one M=128 MMA feeds both halves of SiLU*mul.
-template <int FMT>
+template <int FMT, int NMAX>
 struct TcCfg {
   static constexpr int kABytes = 128 * kBK * 2;            // bf16 A tile (MMA operand)
-  static constexpr int kBBytes = 256 * kBK * 2;            // bf16 B tile (up to 256 pairs)
+  static constexpr int kBBytes = NMAX * kBK * 2;           // bf16 B tile (up to NMAX pairs)
   // quantised A tile as loaded by TMA, before the converter warps dequantise it
   static constexpr int kQBytes = FMT == PMOE_FP8_BLOCK128 ? 128 * kBK : FMT == PMOE_INT4_GPTQ_G128 ? 128 * kBK / 2 : 0;
   static constexpr int kStageBytes = kABytes + kBBytes + kQBytes;
-  static constexpr int kStages = FMT == PMOE_FP8_BLOCK128 ? 3 : 4;
+  static constexpr int kStagingFloats = 128 * 17;
+  // quantised formats: each converter thread's row of scales (<= 16 per row), padded
+  static constexpr int kScaleWords = FMT == PMOE_BF16 ? 0 : 128 * 17;
+  static constexpr int kFixedBytes = kStagingFloats * 4 + kScaleWords * 4 + 1024 + 512;
+  static constexpr int kStagesFit = (220 * 1024 - kFixedBytes) / kStageBytes;
+  static constexpr int kStages = kStagesFit < 8 ? kStagesFit : 8;
   static constexpr int kAccCols = 256;   // one accumulator buffer (N <= 256 fp32 columns)
   static constexpr int kTmemCols = 512;  // two buffers: the epilogue of tile i overlaps the MMAs of tile i+1
-  static constexpr int kStagingFloats = 128 * 17;
-  static constexpr int kSmemBytes = kStages * kStageBytes + kStagingFloats * 4 + 1024 + 512;
+  static constexpr int kSmemBytes = kStages * kStageBytes + kFixedBytes;
   static constexpr int kThreads = FMT == PMOE_BF16 ? 192 : 320;  // + 4 converter warps
+  static_assert(kStages >= 2 && kSmemBytes <= 227 * 1024, "shared memory");
 };
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
@@ -174,17 +181,18 @@ __device__ __forceinline__ int epi_bar_or(int pred) {
 }
 
 // One persistent CTA per SM loops over (tile, m-tile) items of one wave.
-template <bool GATEUP, int FMT>
-__global__ void __launch_bounds__(TcCfg<FMT>::kThreads, 1)
+template <bool GATEUP, int FMT, int NMAX>
+__global__ void __launch_bounds__(TcCfg<FMT, NMAX>::kThreads, 1)
     tc_grouped_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_b,
                       const int32_t* __restrict__ plan, int E, int wave, int sub, Workspace ws, int I, int H,
                       const uint8_t* __restrict__ arena, size_t stride, ExpertLayout lay, int32_t* __restrict__ err) {
-  using C = TcCfg<FMT>;
+  using C = TcCfg<FMT, NMAX>;
   constexpr bool kQuant = FMT != PMOE_BF16;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   float* staging = reinterpret_cast<float*>(smem + C::kStages * C::kStageBytes);
-  uint64_t* full = reinterpret_cast<uint64_t*>(staging + C::kStagingFloats);
+  uint32_t* scale_cache = reinterpret_cast<uint32_t*>(staging + C::kStagingFloats);
+  uint64_t* full = reinterpret_cast<uint64_t*>(scale_cache + C::kScaleWords);
   uint64_t* empty = full + C::kStages;
   uint64_t* acc_full = empty + C::kStages;  // [2]
   uint64_t* acc_empty = acc_full + 2;       // [2]
@@ -337,6 +345,15 @@ __global__ void __launch_bounds__(TcCfg<FMT>::kThreads, 1)
       const int grow = GATEUP ? (r < 64 ? mt * 64 + r : I + mt * 64 + (r - 64)) : mt * 128 + r;
       const int cols = GATEUP ? H : I;
       const uint8_t* sc = ex + (GATEUP ? lay.gu_s : lay.d_s);
+      // this row's scales (block-FP8: one fp32 per 128-column block of its block row;
+      // int4: one (s, z) pair per group), read once per item instead of once per stage
+      const int nblk = cols >> 7;
+      const uint32_t* srow = reinterpret_cast<const uint32_t*>(sc) +
+                             (FMT == PMOE_FP8_BLOCK128 ? (size_t)(grow >> 7) * nblk : (size_t)grow * nblk);
+      uint32_t* my_sc = scale_cache + r * 17;
+      const bool cached = nblk <= 16;
+      if (cached)
+        for (int j = 0; j < nblk; ++j) my_sc[j] = __ldg(srow + j);
       for (int kb = 0; kb < n_kb; ++kb) {
         if (!mbar_wait(&full[s], ph, abort_flag, err)) {
           ok = false;
@@ -346,7 +363,7 @@ __global__ void __launch_bounds__(TcCfg<FMT>::kThreads, 1)
         uint4* arow = reinterpret_cast<uint4*>(st + r * 128);
         if (FMT == PMOE_FP8_BLOCK128) {
           const uint8_t* q = st + C::kABytes + C::kBBytes + r * kBK;
-          const float sv = reinterpret_cast<const float*>(sc)[(size_t)(grow >> 7) * (cols >> 7) + ((kb * kBK) >> 7)];
+          const float sv = __uint_as_float(cached ? my_sc[(kb * kBK) >> 7] : __ldg(srow + ((kb * kBK) >> 7)));
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             const uint2 v = *reinterpret_cast<const uint2*>(q + c * 8);
@@ -367,8 +384,8 @@ __global__ void __launch_bounds__(TcCfg<FMT>::kThreads, 1)
           }
         } else {
           const uint8_t* q = st + C::kABytes + C::kBBytes + r * (kBK / 2);
-          const float2 sz = __half22float2(
-              reinterpret_cast<const __half2*>(sc)[(size_t)grow * (cols >> 7) + ((kb * kBK) >> 7)]);
+          const uint32_t szw = cached ? my_sc[(kb * kBK) >> 7] : __ldg(srow + ((kb * kBK) >> 7));
+          const float2 sz = __half22float2(*reinterpret_cast<const __half2*>(&szw));
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             const uint32_t word = *reinterpret_cast<const uint32_t*>(q + c * 4);  // 8 nibbles, low first
@@ -480,21 +497,31 @@ int encode(CUtensorMap* m, void* base, int rank, const cuuint64_t* dims, const c
   return r == CUDA_SUCCESS ? PMOE_OK : PMOE_ECUDA;
 }
 
-template <bool GATEUP, int FMT>
-cudaError_t launch_tc(const CUtensorMap& mw, const CUtensorMap& mb, const int32_t* plan, int E, int wave, int sub,
-                      const Workspace& ws, int I, int H, const uint8_t* arena, size_t stride, int num_sms,
-                      int32_t* err, cudaStream_t s) {
-  using C = TcCfg<FMT>;
+template <bool GATEUP, int FMT, int NMAX>
+cudaError_t launch_tc_n(const CUtensorMap& mw, const CUtensorMap& mb, const int32_t* plan, int E, int wave, int sub,
+                        const Workspace& ws, int I, int H, const uint8_t* arena, size_t stride, int num_sms,
+                        int32_t* err, cudaStream_t s) {
+  using C = TcCfg<FMT, NMAX>;
   static bool attr_set = false;
   if (!attr_set) {
-    const cudaError_t e = cudaFuncSetAttribute(tc_grouped_kernel<GATEUP, FMT>,
+    const cudaError_t e = cudaFuncSetAttribute(tc_grouped_kernel<GATEUP, FMT, NMAX>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  tc_grouped_kernel<GATEUP, FMT><<<num_sms, C::kThreads, C::kSmemBytes, s>>>(
+  tc_grouped_kernel<GATEUP, FMT, NMAX><<<num_sms, C::kThreads, C::kSmemBytes, s>>>(
       mw, mb, plan, E, wave, sub, ws, I, H, arena, stride, expert_layout(FMT, H, I), err);
   return cudaGetLastError();
+}
+
+// tile_n: the pair cap the grouping used for this forward's tiles (kTcSmallN or kTcMaxN)
+template <bool GATEUP, int FMT>
+cudaError_t launch_tc(const CUtensorMap& mw, const CUtensorMap& mb, const int32_t* plan, int E, int wave, int sub,
+                      const Workspace& ws, int I, int H, const uint8_t* arena, size_t stride, int num_sms,
+                      int32_t* err, int tile_n, cudaStream_t s) {
+  if (tile_n <= kTcSmallN)
+    return launch_tc_n<GATEUP, FMT, kTcSmallN>(mw, mb, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, s);
+  return launch_tc_n<GATEUP, FMT, kTcMaxN>(mw, mb, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, s);
 }
 
 }  // namespace
@@ -553,24 +580,24 @@ int tc_make_act_maps(__nv_bfloat16* x_perm, __nv_bfloat16* h, size_t P, int H, i
 
 cudaError_t tc_gateup(int fmt, const TcMaps& wm, const TcMaps& am, const int32_t* plan, int E, int wave, int sub,
                       const Workspace& ws, int I, int H, const uint8_t* arena, size_t stride, int num_sms,
-                      int32_t* err, cudaStream_t s) {
+                      int32_t* err, int tile_n, cudaStream_t s) {
   if (fmt == PMOE_FP8_BLOCK128)
-    return launch_tc<true, PMOE_FP8_BLOCK128>(wm.gu, am.x, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, s);
+    return launch_tc<true, PMOE_FP8_BLOCK128>(wm.gu, am.x, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, tile_n, s);
   if (fmt == PMOE_INT4_GPTQ_G128)
-    return launch_tc<true, PMOE_INT4_GPTQ_G128>(wm.gu, am.x, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err,
+    return launch_tc<true, PMOE_INT4_GPTQ_G128>(wm.gu, am.x, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, tile_n,
                                                 s);
-  return launch_tc<true, PMOE_BF16>(wm.gu, am.x, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, s);
+  return launch_tc<true, PMOE_BF16>(wm.gu, am.x, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, tile_n, s);
 }
 
 cudaError_t tc_down(int fmt, const TcMaps& wm, const TcMaps& am, const int32_t* plan, int E, int wave, int sub,
                     const Workspace& ws, int I, int H, const uint8_t* arena, size_t stride, int num_sms, int32_t* err,
-                    cudaStream_t s) {
+                    int tile_n, cudaStream_t s) {
   if (fmt == PMOE_FP8_BLOCK128)
-    return launch_tc<false, PMOE_FP8_BLOCK128>(wm.d, am.h, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, s);
+    return launch_tc<false, PMOE_FP8_BLOCK128>(wm.d, am.h, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, tile_n, s);
   if (fmt == PMOE_INT4_GPTQ_G128)
-    return launch_tc<false, PMOE_INT4_GPTQ_G128>(wm.d, am.h, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err,
+    return launch_tc<false, PMOE_INT4_GPTQ_G128>(wm.d, am.h, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, tile_n,
                                                  s);
-  return launch_tc<false, PMOE_BF16>(wm.d, am.h, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, s);
+  return launch_tc<false, PMOE_BF16>(wm.d, am.h, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, tile_n, s);
 }
 
 }  // namespace pmoe

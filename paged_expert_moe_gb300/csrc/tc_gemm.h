@@ -7,7 +7,8 @@
 
 namespace pmoe {
 
-constexpr int kTcMaxN = 256;  // pairs per tile (MMA N)
+constexpr int kTcMaxN = 256;   // pairs per tile (MMA N)
+constexpr int kTcSmallN = 64;  // the cap for forwards with few tokens per expert (deeper TMA pipeline)
 
 struct TcMaps {
   CUtensorMap gu;  // gate/up rows of every slot: dims {H (bytes if quantised), 2I, K}
@@ -25,9 +26,15 @@ int tc_make_act_maps(__nv_bfloat16* x_perm, __nv_bfloat16* h, size_t P, int H, i
 // 2 = its experts paged in for this wave (tiles of the two parts are contiguous).
 cudaError_t tc_gateup(int fmt, const TcMaps& wm, const TcMaps& am, const int32_t* plan, int E, int wave, int sub,
                       const Workspace& ws, int I, int H, const uint8_t* arena, size_t stride, int num_sms,
-                      int32_t* err, cudaStream_t s);
+                      int32_t* err, int tile_n, cudaStream_t s);
 cudaError_t tc_down(int fmt, const TcMaps& wm, const TcMaps& am, const int32_t* plan, int E, int wave, int sub,
                     const Workspace& ws, int I, int H, const uint8_t* arena, size_t stride, int num_sms, int32_t* err,
-                    cudaStream_t s);
+                    int tile_n, cudaStream_t s);
+// The pair cap of a forward's tiles: small tiles (and a deeper pipeline) when the mean
+// pairs per expert is at most half of kTcSmallN; any cap is correct (an expert with more
+// pairs takes several tiles, which re-streams its weights).
+inline int tc_tile_n(int T, int top_k, int E) {
+  return (long long)T * top_k <= (long long)(kTcSmallN / 2) * E ? kTcSmallN : kTcMaxN;
+}
 
 }  // namespace pmoe
