@@ -312,3 +312,14 @@ def test_expert_repeated_within_a_token(pm, E, H, I, T, k, ids_list, Ks):
         cache.close()
     for y in outs[1:]:
         assert torch.equal(y.view(torch.int16), outs[0].view(torch.int16))
+
+
+@pytest.mark.parametrize("fmt,mode", [("bf16", 0), ("int4", 1)])
+def test_startup_independence_check(pm, fmt, mode):
+    """The library's start-up check (paged == unpaged, slots hold their experts' bytes)
+    passes on a small layer with more experts than slots."""
+    from paged_expert_moe_gb300 import preflight as pf
+    E, k, H, I, K = 16, 4, 256, 128, 5
+    L = hz.SyntheticLayer(pf.FORMATS[fmt], E, H, I, seed=90)
+    r = pf.independence_check(E, k, H, I, K, L.store, fmt=fmt, tokens=2, steps=5, seed=3, pagein_mode=mode)
+    assert r["outputs_equal"] and r["slot_mismatches"] == [] and r["misses"] > K and r["slots_checked"] == K
