@@ -162,6 +162,23 @@ PMOE_API int moe_router_topk(const float* logits, int T, int E, int top_k, int r
                     int32_t* ids_out, float* w_out, void* stream);
 
 /*
+ * moe_router_gemm_topk — the router's projection fused in front of moe_router_topk:
+ * logits[t][e] = sum_c x[t][c] * router_weight[e][c] (bf16 inputs, fp32 accumulation in a
+ * fixed order), then the selection and weights of moe_router_topk on those logits.
+ * The article's layer routes each token from its hidden state (section "What does Paged
+ * Experts actually do?", first paragraph); this call takes that hidden state directly.
+ *   x              device, bf16 [T][H], 16-byte aligned
+ *   router_weight  device, bf16 [E][H] (the gate projection, one row per expert), 16-byte aligned
+ *   logits_out     device, fp32 [T][E], or NULL when the logits are not wanted
+ *   ids_out        device, int32 [T][top_k]
+ *   w_out          device, fp32 [T][top_k]
+ * T = 0 enqueues nothing. H a multiple of 8, E in 1..1024, top_k in 1..min(E, 32), else
+ * PMOE_EINVAL; an H whose staging does not fit in shared memory gives PMOE_EUNSUPPORTED.
+ */
+PMOE_API int moe_router_gemm_topk(const void* x, const void* router_weight, int T, int H, int E, int top_k,
+                                  int renormalize, float* logits_out, int32_t* ids_out, float* w_out, void* stream);
+
+/*
  * expert_cache_create — build the paged-expert state for `num_layers` MoE layers:
  * a pinned host store of all E experts per layer, a device arena of K slots per
  * layer, a device LRU table per layer (all slots empty), a copy stream, events and

@@ -54,3 +54,19 @@ def router_topk(logits, top_k, renormalize=True):
         ids[t] = S
         w[t] = sel / sel.sum() if renormalize else sel
     return ids, w
+
+
+def router_logits(x, router_weight):
+    """The router's projection: logits[t, e] = sum_c x[t, c] * router_weight[e, c], float64.
+
+    router_weight holds one row per expert (E x H), the layer's gate projection.
+    """
+    return np.asarray(x, dtype=np.float64) @ np.asarray(router_weight, dtype=np.float64).T
+
+
+def router_gemm_topk(x, router_weight, top_k, renormalize=True):
+    """Route every token from its hidden state: (ids, w, logits) with router_topk applied
+    to router_logits(x, router_weight)."""
+    logits = router_logits(x, router_weight)
+    ids, w = router_topk(logits, top_k, renormalize)
+    return ids, w, logits

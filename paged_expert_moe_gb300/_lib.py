@@ -55,6 +55,7 @@ _SIGS = {
     "pmoe_last_error": ([], ctypes.c_char_p),
     "pmoe_expert_bytes": ([_I, _I, _I], ctypes.c_size_t),
     "moe_router_topk": ([_P, _I, _I, _I, _I, _P, _P, _P], _I),
+    "moe_router_gemm_topk": ([_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P], _I),
     "expert_cache_create": ([ctypes.POINTER(pmoe_cache_desc), ctypes.POINTER(_P)], _I),
     "expert_cache_destroy": ([_P], None),
     "expert_cache_host_store": ([_P, _I, ctypes.POINTER(_P), ctypes.POINTER(ctypes.c_size_t)], _I),
@@ -123,6 +124,26 @@ def moe_router_topk(logits, top_k, renormalize=True, ids_out=None, w_out=None, s
         w_out = torch.empty((T, top_k), dtype=torch.float32, device=logits.device)
     _check(lib.moe_router_topk(_ptr(logits), T, E, top_k, 1 if renormalize else 0, _ptr(ids_out), _ptr(w_out),
                                _stream_handle(stream)), "moe_router_topk")
+    return ids_out, w_out
+
+
+def moe_router_gemm_topk(x, router_weight, top_k, renormalize=True, ids_out=None, w_out=None, logits_out=None,
+                         stream=None):
+    """x: CUDA bf16 [T, H], router_weight: CUDA bf16 [E, H] -> (ids int32 [T, top_k],
+    w fp32 [T, top_k]); logits_out (fp32 [T, E]) is filled when given."""
+    import torch
+    lib = load()
+    T, H = x.shape
+    E = router_weight.shape[0]
+    assert x.dtype == torch.bfloat16 and router_weight.dtype == torch.bfloat16 and router_weight.shape[1] == H
+    assert x.is_cuda and x.is_contiguous() and router_weight.is_contiguous()
+    if ids_out is None:
+        ids_out = torch.empty((T, top_k), dtype=torch.int32, device=x.device)
+    if w_out is None:
+        w_out = torch.empty((T, top_k), dtype=torch.float32, device=x.device)
+    _check(lib.moe_router_gemm_topk(_ptr(x), _ptr(router_weight), T, H, E, top_k, 1 if renormalize else 0,
+                                    _ptr(logits_out), _ptr(ids_out), _ptr(w_out), _stream_handle(stream)),
+           "moe_router_gemm_topk")
     return ids_out, w_out
 
 

@@ -307,6 +307,20 @@ int moe_router_topk(const float* logits, int T, int E, int top_k, int renormaliz
   return PMOE_OK;
 }
 
+int moe_router_gemm_topk(const void* x, const void* router_weight, int T, int H, int E, int top_k, int renormalize,
+                         float* logits_out, int32_t* ids_out, float* w_out, void* stream) {
+  if (T < 0 || E < 1 || E > kMaxExperts || top_k < 1 || top_k > E || top_k > kMaxTopK || H < 8 || H % 8 != 0)
+    return PMOE_EINVAL;
+  if (T == 0) return PMOE_OK;
+  if (x == nullptr || router_weight == nullptr || ids_out == nullptr || w_out == nullptr) return PMOE_EINVAL;
+  if (reinterpret_cast<uintptr_t>(x) % 16 != 0 || reinterpret_cast<uintptr_t>(router_weight) % 16 != 0)
+    return PMOE_EINVAL;
+  if (router_gemm_smem(H, E) > 200 * 1024) return PMOE_EUNSUPPORTED;
+  PMOE_CUDA(launch_router_gemm_topk((const __nv_bfloat16*)x, (const __nv_bfloat16*)router_weight, T, H, E, top_k,
+                                    renormalize ? 1 : 0, logits_out, ids_out, w_out, (cudaStream_t)stream));
+  return PMOE_OK;
+}
+
 int expert_cache_create(const pmoe_cache_desc* desc, pmoe_cache** out) {
   if (desc == nullptr || out == nullptr) return PMOE_EINVAL;
   *out = nullptr;

@@ -72,6 +72,9 @@ struct Workspace {
 // Kernel launchers (each returns cudaError_t of the launch).
 cudaError_t launch_router_topk(const float* logits, int T, int E, int top_k, int renorm,
                                int32_t* ids, float* w, cudaStream_t s);
+size_t router_gemm_smem(int H, int E);
+cudaError_t launch_router_gemm_topk(const __nv_bfloat16* x, const __nv_bfloat16* wr, int T, int H, int E, int top_k,
+                                    int renorm, float* logits_out, int32_t* ids, float* w, cudaStream_t s);
 cudaError_t launch_residency(const int32_t* ids, int n_ids, int E, int K, LayerState st,
                              int32_t* plan, int32_t* err, unsigned long long* epoch, cudaStream_t s);
 cudaError_t launch_group(const int32_t* ids, int P, int E, const int32_t* plan, Workspace ws,

@@ -462,3 +462,45 @@ def test_planted_scale_transpose_is_caught(monkeypatch):
     monkeypatch.setattr(formats.np, "repeat", transposed_repeat)
     Wg, Wu, _ = formats.decode_expert(buf, 1, H, I)
     assert not np.array_equal(np.concatenate([Wg, Wu]), np.kron(sgu, np.ones((128, 128))))
+
+
+# ---------------------------------------------------------------- router projection
+
+def test_router_logits_of_a_one_hot_state_are_a_column():
+    # x = e_j picks column j of the (E x H) router weight: logits[e] = W[e, j]
+    from oracle import router as orouter
+    rng = np.random.default_rng(5)
+    E, H = 12, 20
+    W = rng.standard_normal((E, H))
+    for j in (0, 7, H - 1):
+        x = np.zeros((1, H))
+        x[0, j] = 1.0
+        assert np.array_equal(orouter.router_logits(x, W)[0], W[:, j])
+        ids, _, _ = orouter.router_gemm_topk(x, W, 3)
+        assert ids[0].tolist() == sorted(range(E), key=lambda e: (-W[e, j], e))[:3]
+
+
+def test_router_weights_ignore_a_feature_shared_by_all_experts():
+    # a constant input feature whose weight is the same for every expert shifts all
+    # logits of a token by the same amount: selection and (renormalised) weights stay
+    from oracle import router as orouter
+    rng = np.random.default_rng(6)
+    T, E, H, k = 5, 16, 24, 4
+    x = rng.standard_normal((T, H))
+    W = rng.standard_normal((E, H))
+    ids0, w0, _ = orouter.router_gemm_topk(x, W, k)
+    x1 = np.concatenate([x, np.ones((T, 1))], axis=1)
+    W1 = np.concatenate([W, np.full((E, 1), 0.75)], axis=1)
+    ids1, w1, lg1 = orouter.router_gemm_topk(x1, W1, k)
+    assert np.array_equal(ids0, ids1)
+    np.testing.assert_allclose(w0, w1, rtol=1e-6)
+    np.testing.assert_allclose(lg1 - orouter.router_logits(x, W), 0.75, atol=1e-12)
+
+
+def test_router_logits_are_linear_in_the_state():
+    from oracle import router as orouter
+    rng = np.random.default_rng(7)
+    W = rng.standard_normal((9, 11))
+    a, b = rng.standard_normal((3, 11)), rng.standard_normal((3, 11))
+    np.testing.assert_allclose(orouter.router_logits(a + 2 * b, W),
+                               orouter.router_logits(a, W) + 2 * orouter.router_logits(b, W), atol=1e-12)
