@@ -118,6 +118,7 @@ struct pmoe_cache {
   std::vector<int32_t*> plan_dev;
   int32_t* plan_host = nullptr;
   int32_t* state_buf = nullptr;
+  size_t state_stride = 0;  // bytes between consecutive layers' LRU states in state_buf
   int32_t* plan_buf = nullptr;
   int32_t* err_dev = nullptr;
   std::vector<cudaEvent_t> ev_plan, ev_layer_done, ev_ready;
@@ -418,6 +419,7 @@ int expert_cache_create(const pmoe_cache_desc* desc, pmoe_cache** out) {
   {
     // LRU state: per layer slot_of[E], expert_in[K], last_use[K], step[1], pad, counters (4 x u64)
     const size_t per = round_up((size_t)E + 2 * K + 2, 2) * 4 + 4 * 8;
+    c->state_stride = per;
     PMOE_TRY(cudaMalloc(&c->state_buf, per * Lr));
     PMOE_TRY(cudaMemset(c->state_buf, 0xFF, per * Lr));
     for (int l = 0; l < Lr; ++l) {
@@ -794,7 +796,29 @@ int moe_paged_stack_forward(pmoe_cache* c, const void* x, int T, const int32_t* 
   const bool tc = c->use_tc && T > kGemvMaxTokens;
   const bool defer = c->d.pagein_mode == PMOE_PAGEIN_SM_PULL && !tc &&
                      decode_fused_supported(c->d.format, T, c->d.top_k, c->d.hidden, c->d.intermediate, c->num_sms);
-  if (!c->staged[0]) {
+  bool none_staged = true;
+  for (int l = 0; l < L && none_staged; ++l) none_staged = !c->staged[l];
+  if (defer && none_staged && L > 1) {
+    // every layer's routing is known: plan all layers in one launch (one CTA per layer),
+    // each layer's decode kernel then pages its own missing experts in
+    cudaStream_t ps = c->copy_stream;
+    PMOE_CUDA(cudaStreamWaitEvent(ps, c->ev_stack, 0));
+    // (inside a captured graph each layer's previous forward precedes this by graph order)
+    if (!c->in_capture)
+      for (int l = 0; l < L; ++l) PMOE_CUDA(cudaStreamWaitEvent(ps, c->ev_layer_done[l], 0));
+    {
+      KernelMark km(c, PMOE_K_RESIDENCY, ps);
+      PMOE_CUDA(launch_residency_layers(ids, P, L, c->d.num_experts, c->d.num_slots, c->st[0], c->state_stride,
+                                        c->plan_dev[0], c->words, c->err_dev, c->ws.epoch, ps));
+    }
+    for (int l = 0; l < L; ++l) {
+      PMOE_CUDA(cudaEventRecord(c->ev_ready[l], ps));
+      c->layer_used[l] = 1;
+      c->staged[l] = 1;
+      c->staged_waves[l] = max_waves(c, P);
+      c->pull_deferred[l] = 1;
+    }
+  } else if (!c->staged[0]) {
     const int r = ensure_resident_impl(c, 0, ids, P, c->ev_stack, nullptr, defer);
     if (r == PMOE_EDEVICE) status = r;
     else if (r != PMOE_OK) return r;

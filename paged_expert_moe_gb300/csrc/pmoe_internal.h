@@ -72,6 +72,11 @@ struct Workspace {
 // Kernel launchers (each returns cudaError_t of the launch).
 cudaError_t launch_router_topk(const float* logits, int T, int E, int top_k, int renorm,
                                int32_t* ids, float* w, cudaStream_t s);
+// Layers 0..layers-1 at once; layer l's ids are ids[l * n_ids ...], its state lies
+// l * state_stride bytes after layer 0's, its plan l * plan_words words after plan0.
+cudaError_t launch_residency_layers(const int32_t* ids, int n_ids, int layers, int E, int K, LayerState st0,
+                                    size_t state_stride, int32_t* plan0, int plan_words, int32_t* err,
+                                    unsigned long long* epoch, cudaStream_t s);
 size_t router_gemm_smem(int H, int E);
 cudaError_t launch_router_gemm_topk(const __nv_bfloat16* x, const __nv_bfloat16* wr, int T, int H, int E, int top_k,
                                     int renorm, float* logits_out, int32_t* ids, float* w, cudaStream_t s);

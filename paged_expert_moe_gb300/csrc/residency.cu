@@ -51,10 +51,9 @@ __device__ int block_exclusive_scan(int v, int* s_warp, int* total) {
   return r;
 }
 
-__global__ void __launch_bounds__(kThreads) residency_kernel(const int32_t* __restrict__ ids, int n_ids, int E,
-                                                             int K, LayerState st, int32_t* __restrict__ plan,
-                                                             int32_t* __restrict__ err,
-                                                             unsigned long long* __restrict__ epoch) {
+__device__ __forceinline__ void residency_body(const int32_t* __restrict__ ids, int n_ids, int E, int K,
+                                               LayerState st, int32_t* __restrict__ plan, int32_t* __restrict__ err,
+                                               unsigned long long* __restrict__ epoch) {
   __shared__ int s_pend[kMaxExperts];
   __shared__ int s_slot_of[kMaxExperts];
   __shared__ int s_exp_in[kMaxExperts];
@@ -175,6 +174,31 @@ __global__ void __launch_bounds__(kThreads) residency_kernel(const int32_t* __re
   }
 }
 
+__global__ void __launch_bounds__(kThreads) residency_kernel(const int32_t* __restrict__ ids, int n_ids, int E,
+                                                             int K, LayerState st, int32_t* __restrict__ plan,
+                                                             int32_t* __restrict__ err,
+                                                             unsigned long long* __restrict__ epoch) {
+  residency_body(ids, n_ids, E, K, st, plan, err, epoch);
+}
+
+// Every layer of a stack at once: CTA l plans layer l (the layers' tables are independent,
+// and their states and plans lie at fixed strides from layer 0's).
+__global__ void __launch_bounds__(kThreads) residency_layers_kernel(const int32_t* __restrict__ ids, int n_ids,
+                                                                    int E, int K, LayerState st0, size_t state_stride,
+                                                                    int32_t* __restrict__ plan0, int plan_words,
+                                                                    int32_t* __restrict__ err,
+                                                                    unsigned long long* __restrict__ epoch) {
+  const int l = blockIdx.x;
+  const size_t d = state_stride * (size_t)l;
+  LayerState st;
+  st.slot_of = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(st0.slot_of) + d);
+  st.expert_in = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(st0.expert_in) + d);
+  st.last_use = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(st0.last_use) + d);
+  st.step = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(st0.step) + d);
+  st.counters = reinterpret_cast<unsigned long long*>(reinterpret_cast<uint8_t*>(st0.counters) + d);
+  residency_body(ids + (size_t)l * n_ids, n_ids, E, K, st, plan0 + (size_t)l * plan_words, err, epoch);
+}
+
 }  // namespace
 
 cudaError_t launch_residency(const int32_t* ids, int n_ids, int E, int K, LayerState st, int32_t* plan,
@@ -186,6 +210,20 @@ cudaError_t launch_residency(const int32_t* ids, int n_ids, int E, int K, LayerS
     carveout_set = true;
   }
   residency_kernel<<<1, kThreads, 0, s>>>(ids, n_ids, E, K, st, plan, err, epoch);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_residency_layers(const int32_t* ids, int n_ids, int layers, int E, int K, LayerState st0,
+                                    size_t state_stride, int32_t* plan0, int plan_words, int32_t* err,
+                                    unsigned long long* epoch, cudaStream_t s) {
+  static bool carveout_set = false;
+  if (!carveout_set) {
+    cudaFuncSetAttribute(residency_layers_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                         (int)cudaSharedmemCarveoutMaxShared);
+    carveout_set = true;
+  }
+  residency_layers_kernel<<<layers, kThreads, 0, s>>>(ids, n_ids, E, K, st0, state_stride, plan0, plan_words, err,
+                                                      epoch);
   return cudaGetLastError();
 }
 
