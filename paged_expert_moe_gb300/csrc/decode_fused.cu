@@ -325,6 +325,42 @@ __device__ __forceinline__ int ring_place(unsigned head, unsigned lo, bool empty
   return head + need <= lo ? (int)head : -1;
 }
 
+// Scales of a quantised chunk travel in the ring with its weight rows, so that the
+// consumers read them from shared memory instead of waiting on global loads per row.
+// A scale row covers one weight row (int4: the row's (s, z) per group of 128) or one
+// block row of 128 weight rows (FP8: the fp32 scale per 128x128 block). For rows
+// [r0, r0 + n) of a region whose scale rows are RS bytes apart, the copy spans the scale
+// rows they need, widened to 16-byte boundaries (the host requires the scale regions to
+// start and end on such boundaries); `first` is the byte offset of row r0's scale row in
+// the copy.
+struct ScaleSpan {
+  uint32_t src, bytes, first;  // src: byte offset in the expert
+};
+template <int FMT>
+__device__ __forceinline__ int scale_row(int r) {
+  return FMT == PMOE_FP8_BLOCK128 ? (r >> 7) : r;
+}
+template <int FMT>
+__device__ __forceinline__ ScaleSpan scale_span(size_t region, int RS, int r0, int n) {
+  const uint32_t b0 = (uint32_t)(region + (size_t)scale_row<FMT>(r0) * RS);
+  const uint32_t b1 = (uint32_t)(region + (size_t)(scale_row<FMT>(r0 + n - 1) + 1) * RS);
+  const uint32_t a0 = b0 & ~15u, a1 = (b1 + 15u) & ~15u;
+  return ScaleSpan{a0, a1 - a0, b0 - a0};
+}
+template <int FMT>
+__device__ __forceinline__ ChunkQ chunk_q_ring(const uint8_t* row_scales, int c) {
+  ChunkQ q{1.f, 0.f};
+  if constexpr (FMT == PMOE_FP8_BLOCK128) {
+    q.s = reinterpret_cast<const float*>(row_scales)[(c * 16) >> 7];
+  } else if constexpr (FMT == PMOE_INT4_GPTQ_G128) {
+    const uint32_t raw = reinterpret_cast<const uint32_t*>(row_scales)[(c * 32) >> 7];
+    const float2 sz = __half22float2(*reinterpret_cast<const __half2*>(&raw));
+    q.s = sz.x;
+    q.z = sz.y;
+  }
+  return q;
+}
+
 template <int FMT, int NCH1, int NCH2>
 __global__ void __launch_bounds__(kDfThreads, 1) decode_fused_kernel(const DfArgs a) {
   constexpr int EPC = Fmt<FMT>::EPC;
@@ -493,6 +529,7 @@ __global__ void __launch_bounds__(kDfThreads, 1) decode_fused_kernel(const DfArg
   if (tid == 0) DF_TRACE(1);
   const size_t rbg = (size_t)a.H * Fmt<FMT>::BPE2 / 2;  // one gate (or up) row
   const size_t rbd = (size_t)a.I * Fmt<FMT>::BPE2 / 2;  // one down row
+  const int rsg = (a.H / 128) * 4, rsd = (a.I / 128) * 4;  // one scale row of gate/up, of down
 
   if (warp == kDfConsumerWarps) {
     // ---------------- producer: lane 0 places every chunk in the byte ring as soon as
@@ -508,7 +545,18 @@ __global__ void __launch_bounds__(kDfThreads, 1) decode_fused_kernel(const DfArg
         const int4 we = s_we[cd.y];
         const unsigned wbytes = kind == 1 ? (unsigned)(2 * (size_t)cd.w * rbg) : (unsigned)((size_t)cd.w * rbd);
         const unsigned hbytes = (kind == 2 && cd.w > 0) ? (unsigned)(min(we.w - we.z, a.T) * a.I * 2) : 0u;
-        const unsigned need = (wbytes + hbytes + 127u) & ~127u;
+        ScaleSpan sp0{0, 0, 0}, sp1{0, 0, 0};
+        if constexpr (FMT != PMOE_BF16) {
+          if (cd.w > 0) {
+            if (kind == 1) {
+              sp0 = scale_span<FMT>(a.lay.gu_s, rsg, cd.z, cd.w);
+              sp1 = scale_span<FMT>(a.lay.gu_s, rsg, a.I + cd.z, cd.w);
+            } else {
+              sp0 = scale_span<FMT>(a.lay.d_s, rsd, cd.z, cd.w);
+            }
+          }
+        }
+        const unsigned need = (wbytes + hbytes + sp0.bytes + sp1.bytes + 127u) & ~127u;
         int off = -1;
         long long t0 = -1;
         while (true) {
@@ -557,13 +605,19 @@ __global__ void __launch_bounds__(kDfThreads, 1) decode_fused_kernel(const DfArg
         } else {
           const uint8_t* ex = a.arena + (size_t)we.y * a.stride;
           uint8_t* dst = ring + off;
-          mb_expect(fb, wbytes);
+          mb_expect(fb, wbytes + sp0.bytes + sp1.bytes);
           if (kind == 1) {
             const uint32_t half = wbytes / 2;
             bulk_g2s(dst, ex + a.lay.gu_w + (size_t)cd.z * rbg, half, fb);
             bulk_g2s(dst + half, ex + a.lay.gu_w + (size_t)(a.I + cd.z) * rbg, half, fb);
           } else {
             bulk_g2s(dst, ex + a.lay.d_w + (size_t)cd.z * rbd, wbytes, fb);
+          }
+          if constexpr (FMT != PMOE_BF16) {
+            // the scale rows go after the weights (and after a down chunk's h rows)
+            uint8_t* sdst = dst + wbytes + hbytes;
+            if (sp0.bytes != 0) bulk_g2s(sdst, ex + sp0.src, sp0.bytes, fb);
+            if (sp1.bytes != 0) bulk_g2s(sdst + sp0.bytes, ex + sp1.src, sp1.bytes, fb);
           }
         }
         asm volatile("st.release.cta.shared.u32 [%0], %1;" ::"r"(su32(&s_placed)), "r"(k + 1) : "memory");
@@ -731,7 +785,6 @@ __global__ void __launch_bounds__(kDfThreads, 1) decode_fused_kernel(const DfArg
       if (k == 0 && lane == 0 && warp == 0) DF_TRACE(2);
       if (warp == 0 && lane == 0) DF_CHUNK(k, 1);
       const int4 we = s_we[cd.y];
-      const uint8_t* ex = a.arena + (size_t)we.y * a.stride;
       const uint8_t* st = ring + s_off[s];
       bool ok = true;
       if (kind == 1) {
@@ -763,12 +816,19 @@ __global__ void __launch_bounds__(kDfThreads, 1) decode_fused_kernel(const DfArg
                 }
               }
             } else {
+              // this row pair's scale rows, in the ring after the chunk's weight rows
+              const ScaleSpan sg = scale_span<FMT>(a.lay.gu_s, rsg, cd.z, cd.w);
+              const ScaleSpan su = scale_span<FMT>(a.lay.gu_s, rsg, a.I + cd.z, cd.w);
+              const uint8_t* sgr = st + 2 * (size_t)cd.w * rbg + sg.first +
+                                   (size_t)(scale_row<FMT>(j) - scale_row<FMT>(cd.z)) * rsg;
+              const uint8_t* sur = st + 2 * (size_t)cd.w * rbg + sg.bytes + su.first +
+                                   (size_t)(scale_row<FMT>(a.I + j) - scale_row<FMT>(a.I + cd.z)) * rsg;
 #pragma unroll
               for (int c = 0; c < NCH1; ++c) {
                 const int idx = lane + 32 * c;
                 if (idx < nch1) {
-                  const ChunkQ qg = chunk_q<FMT, true>(ex + a.lay.gu_s, j, idx, a.H);
-                  const ChunkQ qu = chunk_q<FMT, true>(ex + a.lay.gu_s, a.I + j, idx, a.H);
+                  const ChunkQ qg = chunk_q_ring<FMT>(sgr, idx);
+                  const ChunkQ qu = chunk_q_ring<FMT>(sur, idx);
                   g += chunk_dot<FMT, kSrcShared>(gw[c], xr + idx * (EPC / 8), qg);
                   u += chunk_dot<FMT, kSrcShared>(uw[c], xr + idx * (EPC / 8), qu);
                 }
@@ -789,9 +849,14 @@ __global__ void __launch_bounds__(kDfThreads, 1) decode_fused_kernel(const DfArg
         // the fetcher stored the h rows of the expert's first T pairs after the W_d
         // rows; further pairs (an expert routed twice by one token) read theirs here
         const uint4* hsv = reinterpret_cast<const uint4*>(st + (size_t)cd.w * rbd);
+        const uint8_t* sdb = st + (size_t)cd.w * rbd + (size_t)min(we.w - we.z, a.T) * a.I * 2;
         for (int rr = first; rr < cd.w && ok; rr += kDfConsumerWarps) {
           const uint4* row = reinterpret_cast<const uint4*>(st + (size_t)rr * rbd);
           const int n_out = cd.z + rr;
+          const uint8_t* sdr = nullptr;
+          if constexpr (FMT != PMOE_BF16)
+            sdr = sdb + scale_span<FMT>(a.lay.d_s, rsd, cd.z, cd.w).first +
+                  (size_t)(scale_row<FMT>(n_out) - scale_row<FMT>(cd.z)) * rsd;
           for (int gp = we.z; gp < we.w && ok; ++gp) {
             const int pi = gp - we.z;
             float acc = 0.f;
@@ -799,7 +864,7 @@ __global__ void __launch_bounds__(kDfThreads, 1) decode_fused_kernel(const DfArg
             for (int c = 0; c < NCH2; ++c) {
               const int idx = lane + 32 * c;
               if (idx < nch2) {
-                const ChunkQ q = chunk_q<FMT, true>(ex + a.lay.d_s, n_out, idx, a.I);
+                const ChunkQ q = chunk_q_ring<FMT>(sdr, idx);
                 if (pi < a.T) {
                   acc += chunk_dot<FMT, kSrcShared>(lds128(row + idx), hsv + (size_t)pi * (a.I / 8) + idx * (EPC / 8), q);
                 } else {
@@ -893,8 +958,18 @@ bool df_geometry(int fmt, int T, int top_k, int H, int I, int G, DfGeom* g) {
   if (T > kDfMaxTokens) return false;
   g->fixed = (size_t)T * H * 2 + (size_t)kDfMaxPairs * kDfMaxRows * 4 + (size_t)kDfMaxTokens * kDfMaxRows * 2 +
              (size_t)kDfMaxChunks * sizeof(int4);
+  // a quantised chunk carries its scale rows, copied in 16-byte units: the scale regions
+  // must start and end on 16-byte boundaries
+  size_t scale_max = 0;
+  if (fmt != PMOE_BF16) {
+    if (H % 128 != 0 || I % 128 != 0) return false;
+    const ExpertLayout lay = expert_layout(fmt, H, I);
+    if (lay.gu_s % 16 != 0 || lay.d_s % 16 != 0 || lay.bytes % 16 != 0) return false;
+    const size_t rsg = (size_t)(H / 128) * 4, rsd = (size_t)(I / 128) * 4;
+    scale_max = 2 * ((size_t)(rj + 1) * rsg + 32) + (size_t)(kDfMaxRows + 1) * rsd + 32;
+  }
   // a down chunk also holds the h rows of up to T pairs
-  const size_t max_chunk = std::max((size_t)kDfMaxChunkBytes, (size_t)kDfMaxChunkBytes + (size_t)T * I * 2 + 128);
+  const size_t max_chunk = (size_t)kDfMaxChunkBytes + (size_t)T * I * 2 + 128 + scale_max;
   if (g->fixed + 2 * max_chunk > kDfSmemBudget) return false;
   g->ring = ((kDfSmemBudget - g->fixed) / 128) * 128;
   return true;
