@@ -392,6 +392,70 @@ __global__ void __launch_bounds__(kDfThreads, 1) decode_fused_kernel(const DfArg
   if (tid == 0) DF_TRACE(0);
   const PlanLayout L{a.E};
   const int P = a.T * a.top_k;
+  // The producer thread initialises the barriers and, for a launch that starts at wave
+  // 0, at once streams the first gate/up chunks of the wave's leading resident experts:
+  // their place in the schedule, their rows and their ring offsets follow from the plan
+  // header and slot list alone, so the copies are in flight while the block groups the
+  // pairs and builds the chunk list. The main loop carries on after them.
+  int early_n = 0;
+  unsigned early_head = 0;
+  if (warp == kDfConsumerWarps && lane == 0) {
+    for (int s = 0; s < kDfSlots; ++s) {
+      mb_init(&s_full[s], 1);
+      mb_init(&s_hrdy[s], 1);
+      mb_init(&s_empty[s], kDfConsumerWarps);
+    }
+    s_abort = 0;
+    s_pulled = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    const int nw = a.plan[kPlanWaves], ws0 = a.plan[L.wave_start() + a.wave];
+    const int ws1 = a.plan[L.wave_start() + a.wave + 1], hits = a.plan[L.wave_hits() + a.wave];
+    static_assert(kDfLag == 3, "the entry-time slot reads below cover the first three experts");
+    const int sl0 = a.plan[L.wave_slot()], sl1 = a.E > 1 ? a.plan[L.wave_slot() + 1] : -1;
+    const int sl2 = a.E > 2 ? a.plan[L.wave_slot() + 2] : -1;
+    const int D0 = ws1 - ws0;
+    if (a.wave < nw && ws0 == 0 && a.sub == 0 && D0 > 0 && D0 * (a.cg + a.cd) <= kDfMaxChunks) {
+      const int nh = a.pull != 0 ? min(hits, D0) : D0;
+      const DfSched sc0{D0, (int)gridDim.x, (int)blockIdx.x, a.I, a.H, a.cg, a.cd};
+      const size_t rbg0 = (size_t)a.H * Fmt<FMT>::BPE2 / 2;
+      const int rsg0 = (a.H / 128) * 4;
+      const unsigned R0 = (unsigned)a.ring_bytes;
+      for (int q = 0; q < min(kDfLag, D0) * a.cg && q < kDfSlots; ++q) {
+        const int4 cq = sched_entry(q, sc0);  // a gate/up chunk of wave expert q / cg
+        const int slot = cq.y == 0 ? sl0 : cq.y == 1 ? sl1 : sl2;
+        if (cq.y >= nh || slot < 0) break;  // (an expert paged in by this launch waits for the pagers)
+        const unsigned wbytes = (unsigned)(2 * (size_t)cq.w * rbg0);
+        ScaleSpan sp0{0, 0, 0}, sp1{0, 0, 0};
+        if constexpr (FMT != PMOE_BF16) {
+          if (cq.w > 0) {
+            sp0 = scale_span<FMT>(a.lay.gu_s, rsg0, cq.z, cq.w);
+            sp1 = scale_span<FMT>(a.lay.gu_s, rsg0, a.I + cq.z, cq.w);
+          }
+        }
+        const unsigned need = (wbytes + sp0.bytes + sp1.bytes + 127u) & ~127u;
+        if (early_head + need > R0) break;
+        s_off[q] = early_head;
+        uint64_t* fb = &s_full[q];
+        if (wbytes == 0) {
+          mb_arrive(fb);
+        } else {
+          const uint8_t* ex = a.arena + (size_t)slot * a.stride;
+          uint8_t* dst = ring + early_head;
+          mb_expect(fb, wbytes + sp0.bytes + sp1.bytes);
+          bulk_g2s(dst, ex + a.lay.gu_w + (size_t)cq.z * rbg0, wbytes / 2, fb);
+          bulk_g2s(dst + wbytes / 2, ex + a.lay.gu_w + (size_t)(a.I + cq.z) * rbg0, wbytes / 2, fb);
+          if constexpr (FMT != PMOE_BF16) {
+            if (sp0.bytes != 0) bulk_g2s(dst + wbytes, ex + sp0.src, sp0.bytes, fb);
+            if (sp1.bytes != 0) bulk_g2s(dst + wbytes + sp0.bytes, ex + sp1.src, sp1.bytes, fb);
+          }
+        }
+        DF_CHUNK(q, 0);
+        early_head += need;
+        ++early_n;
+      }
+    }
+    s_placed = early_n;  // (published by the block barrier below)
+  }
   const int r_lo = (int)((long long)a.H * blockIdx.x / gridDim.x);
   const int r_hi = (int)((long long)a.H * (blockIdx.x + 1) / gridDim.x);
   // One round of independent loads: the plan words, the ids, the first wave's list (read
@@ -423,17 +487,6 @@ __global__ void __launch_bounds__(kDfThreads, 1) decode_fused_kernel(const DfArg
       const int t = i / rows;
       res_s[t * kDfMaxRows + (i - t * rows)] = a.residual[(size_t)t * a.H + r_lo + (i - t * rows)];
     }
-  }
-  if (tid == 224) {
-    for (int s = 0; s < kDfSlots; ++s) {
-      mb_init(&s_full[s], 1);
-      mb_init(&s_hrdy[s], 1);
-      mb_init(&s_empty[s], kDfConsumerWarps);
-    }
-    s_abort = 0;
-    s_placed = 0;
-    s_pulled = 0;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
   if (tid == 0) DF_TRACE(7);
@@ -537,8 +590,8 @@ __global__ void __launch_bounds__(kDfThreads, 1) decode_fused_kernel(const DfArg
     // bulk copies. A down chunk also reserves room for the expert's h rows, which the
     // fetcher warp fills.
     if (lane == 0) {
-      unsigned head = 0;
-      int tail = 0, k = 0;
+      unsigned head = early_head;  // the chunks streamed at entry occupy [0, early_head)
+      int tail = 0, k = early_n;
       for (; k < n_chunks; ++k) {
         const int4 cd = chunks[k];
         const int kind = cd.x & 3;
