@@ -409,13 +409,15 @@ __global__ void __launch_bounds__(kDfThreads, 1) decode_fused_kernel(const DfArg
     s_pulled = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     const int nw = a.plan[kPlanWaves], ws0 = a.plan[L.wave_start() + a.wave];
-    const int ws1 = a.plan[L.wave_start() + a.wave + 1], hits = a.plan[L.wave_hits() + a.wave];
+    const int ws1 = a.plan[L.wave_start() + a.wave + 1];
     static_assert(kDfLag == 3, "the entry-time slot reads below cover the first three experts");
     const int sl0 = a.plan[L.wave_slot()], sl1 = a.E > 1 ? a.plan[L.wave_slot() + 1] : -1;
     const int sl2 = a.E > 2 ? a.plan[L.wave_slot() + 2] : -1;
     const int D0 = ws1 - ws0;
-    if (a.wave < nw && ws0 == 0 && a.sub == 0 && D0 > 0 && D0 * (a.cg + a.cd) <= kDfMaxChunks) {
-      const int nh = a.pull != 0 ? min(hits, D0) : D0;
+    // (not when this launch pages experts in: the block barrier below would hold the
+    // pager warps back while the producer issues, and the host link is the longer path)
+    if (a.pull == 0 && a.wave < nw && ws0 == 0 && a.sub == 0 && D0 > 0 && D0 * (a.cg + a.cd) <= kDfMaxChunks) {
+      const int nh = D0;  // (no page-in: every wave expert is resident)
       const DfSched sc0{D0, (int)gridDim.x, (int)blockIdx.x, a.I, a.H, a.cg, a.cd};
       const size_t rbg0 = (size_t)a.H * Fmt<FMT>::BPE2 / 2;
       const int rsg0 = (a.H / 128) * 4;
