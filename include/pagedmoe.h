@@ -227,6 +227,26 @@ PMOE_API int expert_cache_ensure_resident(pmoe_cache* cache, int layer, const in
                                  void* stream, int* waves_out);
 
 /*
+ * expert_cache_prefetch — page in a predicted expert set ahead of the layer's forward
+ * (the overlap of section "Why is it fast when experts keep crossing PCIe?": the
+ * next layer's experts cross the link while the current layer computes; here the
+ * set is a prediction, for a model whose next-layer routing is not yet known).
+ * ids: device int32 [n_ids], n_ids <= max_tokens * top_k, the predicted experts
+ * (repeats allowed). The call runs one residency step for them on `layer` (the
+ * same LRU step as for a forward: its hits, misses and waves are counted, and the
+ * experts are marked used at that step) and then the page-in of every wave, in
+ * order, on the copy stream; nothing is computed. It is ordered after the work on
+ * `stream` and after the layer's previous forward; the layer's next residency
+ * step, and so its forward, is ordered after this page-in. A staged
+ * ensure_resident that no forward consumed is completed first. Experts the
+ * prediction got right are hits in the forward that follows; a wrong prediction
+ * costs link time and slots, never a different result. Returns PMOE_EINVAL on bad
+ * arguments, PMOE_EUNSUPPORTED under stream capture of a copy-engine cache, else
+ * as ensure_resident.
+ */
+PMOE_API int expert_cache_prefetch(pmoe_cache* cache, int layer, const int32_t* ids, int n_ids, void* stream);
+
+/*
  * moe_paged_forward — the fused MoE over the slot table (section "What does Paged
  * Experts actually do?" item 3; section "Can paging change the model's outputs?").
  *   x         device, bf16 [T][H]

@@ -62,6 +62,7 @@ _SIGS = {
     "expert_cache_load_expert": ([_P, _I, _I, _P, ctypes.c_size_t], _I),
     "expert_cache_reset": ([_P, _I], _I),
     "expert_cache_ensure_resident": ([_P, _I, _P, _I, _P, ctypes.POINTER(_I)], _I),
+    "expert_cache_prefetch": ([_P, _I, _P, _I, _P], _I),
     "moe_paged_forward": ([_P, _I, _P, _I, _P, _P, _P, _P, _P], _I),
     "expert_cache_stats": ([_P, _I, ctypes.POINTER(pmoe_stats)], _I),
     "expert_cache_slot_table": ([_P, _I, _P, _P], _I),
@@ -216,6 +217,10 @@ class ExpertCache:
                                                    _stream_handle(stream), ctypes.byref(waves)),
                "expert_cache_ensure_resident")
         return waves.value
+
+    def expert_cache_prefetch(self, layer, ids, stream=None):
+        _check(load().expert_cache_prefetch(self.handle, layer, _ptr(ids), ids.numel(), _stream_handle(stream)),
+               "expert_cache_prefetch")
 
     def moe_paged_forward(self, layer, x, ids, w, y=None, residual=None, stream=None):
         import torch

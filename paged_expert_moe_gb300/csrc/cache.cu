@@ -573,6 +573,21 @@ int expert_cache_ensure_resident(pmoe_cache* c, int layer, const int32_t* ids, i
   return ensure_resident_impl(c, layer, ids, n_ids, c->ev_ids, waves_out);
 }
 
+int expert_cache_prefetch(pmoe_cache* c, int layer, const int32_t* ids, int n_ids, void* stream) {
+  if (c == nullptr || layer < 0 || layer >= c->d.num_layers || n_ids < 0 ||
+      n_ids > c->d.max_tokens * c->d.top_k || (n_ids > 0 && ids == nullptr))
+    return PMOE_EINVAL;
+  PMOE_CUDA(cudaSetDevice(c->d.device));
+  c->in_capture = stream_capturing((cudaStream_t)stream);
+  PMOE_CUDA(cudaEventRecord(c->ev_ids, (cudaStream_t)stream));
+  // one residency step for the predicted ids (an LRU step like any other), then the
+  // page-in of every wave, in order, on the copy stream; nothing is computed
+  const int r = ensure_resident_impl(c, layer, ids, n_ids, c->ev_ids, nullptr);
+  if (r != PMOE_OK && r != PMOE_EDEVICE) return r;
+  const int f = flush_staged(c, layer);
+  return f != PMOE_OK ? f : r;
+}
+
 }  // extern "C"
 
 namespace {

@@ -370,6 +370,23 @@ def test_single_wave_rule_and_batch_cap():
             assert U <= 8 * B
 
 
+def test_lru_prefetch_of_the_own_set_moves_every_miss_into_the_prefetch():
+    """A step preceded by a step for the same set (a perfect prefetch) has no misses
+    when the set fits in K. Stepping every set twice only relabels the LRU clock in the
+    same order, so the total misses and the final table equal those of stepping each
+    set once."""
+    rng = np.random.default_rng(17)
+    E, K, k = 64, 12, 4
+    once, twice = lru.LayerLRU(E, K), lru.LayerLRU(E, K)
+    for _ in range(300):
+        ids = [int(e) for e in rng.choice(E, size=2 * k, replace=True)]
+        once.step(ids)
+        twice.step(ids)
+        assert twice.step(ids)["n_misses"] == 0
+    assert twice.misses == once.misses
+    assert twice.expert_in == once.expert_in
+
+
 def test_lru_evicts_only_least_recent_experts():
     """Invariant: in single-wave steps, no resident expert is older than an evicted one."""
     rng = np.random.default_rng(18)
