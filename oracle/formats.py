@@ -23,6 +23,13 @@ layout contract, independently of the CUDA code:
       SZ_gu fp16 [2I][H/128][2]   (scale, zero) per output row and input group
       SZ_d  fp16 [H][I/128][2]
       w[n, c] = (q[n, c] - z[n, c//128]) * s[n, c//128]
+  MXFP4 (format 3), H and I multiples of 128; the OCP microscaling layout: 32 inputs
+  share one power-of-two scale
+      Q_gu  u8 [2I][H/2]   FP4 E2M1 codes, element c of a row: byte c//2, low nibble if c even
+      Q_d   u8 [H][I/2]
+      X_gu  u8 [2I][H/32]  E8M0 scale per output row and block of 32 inputs
+      X_d   u8 [H][I/32]
+      w[n, c] = e2m1(q[n, c]) * 2^(X[n, c//32] - 127)
 
 All sections are packed back to back in the order listed, with no padding.
 TEST INFRASTRUCTURE ONLY (see the package docstring).
@@ -30,7 +37,7 @@ TEST INFRASTRUCTURE ONLY (see the package docstring).
 
 import numpy as np
 
-BF16, FP8_BLOCK128, INT4_GPTQ_G128 = 0, 1, 2
+BF16, FP8_BLOCK128, INT4_GPTQ_G128, MXFP4 = 0, 1, 2, 3
 
 
 def expert_nbytes(fmt, H, I):
@@ -42,6 +49,8 @@ def expert_nbytes(fmt, H, I):
         return n_w + 4 * ((2 * I // 128) * (H // 128) + (H // 128) * (I // 128))
     if fmt == INT4_GPTQ_G128:
         return n_w // 2 + 4 * ((2 * I) * (H // 128) + H * (I // 128))
+    if fmt == MXFP4:
+        return n_w // 2 + (2 * I) * (H // 32) + H * (I // 32)
     raise ValueError("unknown format")
 
 
@@ -68,6 +77,31 @@ def e4m3_value(code):
 
 
 E4M3_TABLE = np.array([e4m3_value(c) for c in range(256)], dtype=np.float64)
+
+
+def e2m1_value(code):
+    """Value of one FP4 E2M1 code (the OCP microscaling element type), from its fields.
+
+    1 sign bit, 2 exponent bits with bias 1, 1 mantissa bit; exponent 0 is subnormal
+    (m/2); there is no infinity or NaN.
+    """
+    s = -1.0 if code & 0x8 else 1.0
+    e = (code >> 1) & 0x3
+    m = code & 0x1
+    if e == 0:
+        return s * (m / 2.0)
+    return s * (1.0 + m / 2.0) * 2.0 ** (e - 1)
+
+
+E2M1_TABLE = np.array([e2m1_value(c) for c in range(16)], dtype=np.float64)
+
+
+def e8m0_value(byte):
+    """Value of one E8M0 scale: 2^(byte - 127); 0xFF is NaN."""
+    return float("nan") if byte == 0xFF else 2.0 ** (int(byte) - 127)
+
+
+E8M0_TABLE = np.array([e8m0_value(b) for b in range(256)], dtype=np.float64)
 
 
 def _take(buf, off, nbytes):
@@ -104,6 +138,13 @@ def decode_expert(buf, fmt, H, I):
         szd, off = _take(buf, off, 4 * H * (I // 128))
         Wgu = _int4_rows(qgu, szgu, 2 * I, H)
         Wd = _int4_rows(qd, szd, H, I)
+    elif fmt == MXFP4:
+        qgu, off = _take(buf, off, I * H)
+        qd, off = _take(buf, off, H * I // 2)
+        xgu, off = _take(buf, off, 2 * I * (H // 32))
+        xd, off = _take(buf, off, H * (I // 32))
+        Wgu = _mxfp4_rows(qgu, xgu, 2 * I, H)
+        Wd = _mxfp4_rows(qd, xd, H, I)
     else:
         raise ValueError("unknown format")
     if off != buf.size:
@@ -121,3 +162,13 @@ def _int4_rows(qbytes, szbytes, n_rows, n_cols):
     s = np.repeat(sz[:, :, 0], 128, axis=1)
     z = np.repeat(sz[:, :, 1], 128, axis=1)
     return (nib - z) * s
+
+
+def _mxfp4_rows(qbytes, xbytes, n_rows, n_cols):
+    """MXFP4 rows: E2M1 nibbles (low first), one E8M0 scale per (row, block of 32)."""
+    q = qbytes.reshape(n_rows, n_cols // 2)
+    codes = np.empty((n_rows, n_cols), dtype=np.uint8)
+    codes[:, 0::2] = q & 0x0F
+    codes[:, 1::2] = q >> 4
+    x = E8M0_TABLE[xbytes.reshape(n_rows, n_cols // 32)]
+    return E2M1_TABLE[codes] * np.repeat(x, 32, axis=1)

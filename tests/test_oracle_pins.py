@@ -271,6 +271,79 @@ def test_quantised_generators_round_trip_within_their_grids():
     assert (np.abs(got - wgu) <= 0.5 * step * 1.01 + 1e-7).all()
 
 
+def test_e8m0_scales_match_torch_for_every_byte():
+    """The MXFP4 scale byte against torch's float8_e8m0fnu cast (a library routine)."""
+    ref = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e8m0fnu).to(torch.float64).numpy()
+    got = formats.E8M0_TABLE
+    both_nan = np.isnan(ref) & np.isnan(got)
+    assert both_nan[255] and not both_nan[:255].any()
+    np.testing.assert_array_equal(got[:255], ref[:255])
+
+
+def test_e2m1_grid_properties_and_generator_round_trip():
+    """FP4 E2M1: the positive codes are strictly increasing, the sign bit negates, the
+    largest value is 6 and the smallest step 0.5. The generator's own grid (a literal
+    list) quantises every oracle value back to its code, and a midpoint to the code with
+    the even mantissa, so the two restatements agree."""
+    t = formats.E2M1_TABLE
+    assert (np.diff(t[:8]) > 0).all() and t[0] == 0.0
+    np.testing.assert_array_equal(t[8:], -t[:8])
+    assert t[7] == 6.0 and t[1] == 0.5
+    # one block of 32 holding every positive and negative grid value, amax 6: scale 2^0
+    vals = np.concatenate([t[:8], t[9:], t[:8], t[9:], [6.0, -6.0]])[:32].astype(np.float32)
+    packed, x = gen._mxfp4_block_quant(vals.reshape(1, 32))
+    assert x.tolist() == [[127]]
+    codes = np.empty(32, np.uint8)
+    codes[0::2] = packed[0] & 0xF
+    codes[1::2] = packed[0] >> 4
+    np.testing.assert_array_equal(t[codes], vals)
+    # midpoints between neighbours: ties go to the even mantissa (codes 0, 2, 2, 4, 4, 6, 6)
+    mids = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0] + [6.0] * 25, np.float32)
+    packed, x = gen._mxfp4_block_quant(mids.reshape(1, 32))
+    codes[0::2] = packed[0] & 0xF
+    codes[1::2] = packed[0] >> 4
+    assert codes[:7].tolist() == [0, 2, 2, 4, 4, 6, 6]
+
+
+def test_mxfp4_nibble_order_and_block_indexing():
+    """Hand-built MXFP4 expert: byte 0x32 holds codes 2 (low, 1.0) then 3 (high, 1.5);
+    scale byte 128 doubles, 126 halves, one byte per row and block of 32."""
+    H, I = 128, 128
+    qgu = np.zeros((2 * I, H // 2), np.uint8)
+    qgu[0, 0] = 0x32
+    qgu[7, 16] = 0xF9  # row 7: element 32 = code 9 (-0.5), element 33 = code 15 (-6)
+    qd = np.zeros((H, I // 2), np.uint8)
+    qd[4, 63] = 0x70  # row 4: element 126 = 0, element 127 = code 7 (6)
+    xgu = np.full((2 * I, H // 32), 127, np.uint8)
+    xgu[7, 1] = 128
+    xd = np.full((H, I // 32), 127, np.uint8)
+    xd[4, 3] = 126
+    buf = np.concatenate([qgu.ravel(), qd.ravel(), xgu.ravel(), xd.ravel()])
+    Wg, Wu, Wd = formats.decode_expert(buf, 3, H, I)
+    assert Wg[0, 0] == 1.0 and Wg[0, 1] == 1.5 and Wg[0, 2] == 0.0
+    assert Wg[7, 32] == -0.5 * 2.0 and Wg[7, 33] == -6.0 * 2.0 and Wg[7, 31] == 0.0
+    assert Wd[4, 127] == 6.0 * 0.5 and Wd[4, 126] == 0.0
+    assert formats.expert_nbytes(3, 2048, 768) == 2506752
+
+
+def test_mxfp4_generator_error_bound():
+    """Per block of 32, with scale X = 2^(floor(log2 amax) - 2): an element below 6X is
+    off by at most half a grid step (X at most, X/4 below 2X) and one at or above 6X
+    becomes +-6X (the recipe's saturation)."""
+    H, I = 256, 128
+    rng = np.random.default_rng([14, 0, 0, 3])
+    wgu = rng.standard_normal((2 * I, H), dtype=np.float32) * np.float32(0.02)
+    Wg, Wu, _ = formats.decode_expert(gen.expert_bytes(3, H, I, 14), 3, H, I)
+    got = np.concatenate([Wg, Wu])
+    g = wgu.reshape(2 * I, H // 32, 32)
+    X = np.repeat(2.0 ** (np.floor(np.log2(np.abs(g).max(axis=2))) - 2), 32, axis=1)
+    a = np.abs(wgu)
+    sat = a >= 6 * X
+    assert (got[sat] == np.sign(wgu[sat]) * 6 * X[sat]).all()
+    half_step = np.where(a < 2 * X, 0.25 * X, np.where(a < 4 * X, 0.5 * X, X))
+    assert (np.abs(got - wgu)[~sat] <= half_step[~sat] * 1.0001).all()
+
+
 def test_bf16_decode_matches_torch_bfloat16():
     rng = np.random.default_rng(13)
     H, I = 128, 64

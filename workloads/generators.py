@@ -1,6 +1,6 @@
 """Seeded generators: activations, router logits with a guaranteed top-k gap, routing
 traces (uniform and previous-step reuse), and expert weights encoded in the
-library's byte layouts (bf16, block-FP8 e4m3, GPTQ-style int4 group 128).
+library's byte layouts (bf16, block-FP8 e4m3, GPTQ-style int4 group 128, MXFP4).
 
 Every expert is drawn from its own counter-style seed (seed, layer, expert,
 format), so any expert can be regenerated alone, on any machine.
@@ -96,6 +96,8 @@ def expert_nbytes(fmt, H, I):
         return n_w + 4 * ((2 * I // 128) * (H // 128) + (H // 128) * (I // 128))
     if fmt == 2:
         return n_w // 2 + 4 * ((2 * I) * (H // 128) + H * (I // 128))
+    if fmt == 3:
+        return n_w // 2 + (2 * I) * (H // 32) + H * (I // 32)
     raise ValueError("unknown format")
 
 
@@ -139,6 +141,33 @@ def _int4_group_quant(w):
     return packed, sz
 
 
+_E2M1_MAGS = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0], dtype=np.float32)
+_E2M1_MIDS = (_E2M1_MAGS[1:] + _E2M1_MAGS[:-1]) / 2
+
+
+def _mxfp4_block_quant(w):
+    """[R, C] float32 -> (packed E2M1 codes [R, C/2] uint8, E8M0 scales [R, C/32] uint8).
+
+    The OCP microscaling recipe per (row, block of 32 columns): shared exponent
+    floor(log2(amax)) - 2 (2 = the largest E2M1 exponent), scale 2^that; each element
+    divided by the scale and rounded to the nearest E2M1 value, ties to the even
+    mantissa, saturating at 6. An all-zero block gets scale 1 and zero codes.
+    """
+    R, C = w.shape
+    g = w.reshape(R, C // 32, 32).astype(np.float32)
+    amax = np.abs(g).max(axis=2)
+    e = np.where(amax > 0, np.floor(np.log2(np.where(amax > 0, amax, 1.0))) - 2, 0).astype(np.int32)
+    e = np.clip(e, -127, 127)
+    scale = np.ldexp(np.float32(1.0), e).astype(np.float32)
+    a = np.abs(g) / scale[:, :, None]
+    lo = np.searchsorted(_E2M1_MIDS, a, side="left")
+    hi = np.searchsorted(_E2M1_MIDS, a, side="right")
+    idx = np.where(lo == hi, lo, np.where(lo % 2 == 0, lo, hi))  # on a midpoint: the even code
+    codes = (idx | np.where(g < 0, 8, 0)).astype(np.uint8).reshape(R, C)
+    packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+    return packed, (e + 127).astype(np.uint8)
+
+
 def expert_bytes(fmt, H, I, seed, layer=0, expert=0, std=0.02):
     """One expert in the byte layout of `fmt`, drawn from N(0, std) master weights.
 
@@ -158,6 +187,10 @@ def expert_bytes(fmt, H, I, seed, layer=0, expert=0, std=0.02):
         qgu, szgu = _int4_group_quant(wgu)
         qd, szd = _int4_group_quant(wd)
         parts = [qgu.ravel(), qd.ravel(), szgu.view(np.uint8).ravel(), szd.view(np.uint8).ravel()]
+    elif fmt == 3:
+        qgu, xgu = _mxfp4_block_quant(wgu)
+        qd, xd = _mxfp4_block_quant(wd)
+        parts = [qgu.ravel(), qd.ravel(), xgu.ravel(), xd.ravel()]
     else:
         raise ValueError("unknown format")
     out = np.concatenate(parts)
