@@ -42,7 +42,16 @@
  *                        SZ_gu fp16 [2I][H/128][2], SZ_d fp16 [H][I/128][2]
  *                        ((scale, zero) per output row and group of 128 inputs);
  *                        w = (q - z) * s
- * FP8 and int4 need H and I multiples of 128; bf16 needs multiples of 8 (and,
+ *   PMOE_MXFP4           Q_gu u8 [2I][H/2], Q_d u8 [H][I/2] (FP4 E2M1 codes, element
+ *                        c of a row in byte c/2, low nibble for even c),
+ *                        X_gu u8 [2I][H/32], X_d u8 [H][I/32] (E8M0 scale per output
+ *                        row and block of 32 inputs); w = e2m1(q) * 2^(X - 127)
+ *                        (the OCP microscaling layout; the formats of section "What
+ *                        does Paged Experts actually do?", PR #45787). Decode batches
+ *                        only: a cache with MXFP4 experts takes max_tokens <= 8
+ *                        (PMOE_EUNSUPPORTED otherwise; the prefill path has no FP4
+ *                        converter).
+ * FP8, int4 and MXFP4 need H and I multiples of 128; bf16 needs multiples of 8 (and,
  * for the tensor-core prefill path, H a multiple of 128 and I of 128).
  *
  * Activations x, residual and y are bf16 [T][H] row-major; router logits fp32
@@ -78,7 +87,8 @@ typedef enum {
 typedef enum {
   PMOE_BF16 = 0,
   PMOE_FP8_BLOCK128 = 1,
-  PMOE_INT4_GPTQ_G128 = 2
+  PMOE_INT4_GPTQ_G128 = 2,
+  PMOE_MXFP4 = 3
 } pmoe_format;
 
 typedef enum {

@@ -1,6 +1,7 @@
 // Device helpers shared by the decode kernels: streaming loads, bf16 unpacking, the
 // per-format dequantisation of one 16-byte weight chunk (bf16 / block-FP8 e4m3 with
-// fp32 128x128 scales / GPTQ int4 g128 with fp16 scale and zero), warp reductions.
+// fp32 128x128 scales / GPTQ int4 g128 with fp16 scale and zero / MXFP4: E2M1 codes with
+// an E8M0 scale per 32 inputs), warp reductions.
 #pragma once
 
 #include "pmoe_internal.h"
@@ -40,6 +41,20 @@ template <int FMT> struct Fmt;
 template <> struct Fmt<PMOE_BF16> { static constexpr int EPC = 8; static constexpr int BPE2 = 4; };
 template <> struct Fmt<PMOE_FP8_BLOCK128> { static constexpr int EPC = 16; static constexpr int BPE2 = 2; };
 template <> struct Fmt<PMOE_INT4_GPTQ_G128> { static constexpr int EPC = 32; static constexpr int BPE2 = 1; };
+template <> struct Fmt<PMOE_MXFP4> { static constexpr int EPC = 32; static constexpr int BPE2 = 1; };
+
+// FP4 E2M1 code (low 4 bits of c) -> fp32, from the fields: 1 sign bit, 2 exponent bits
+// with bias 1, 1 mantissa bit; exponent 0 is subnormal (m/2). The fp32 bit pattern of a
+// normal value puts exponent e - 1 + 127 in bits 23.. and the mantissa bit at bit 22.
+__device__ __forceinline__ float e2m1_f32(uint32_t c) {
+  const uint32_t mag = c & 7u;
+  const uint32_t bits = mag < 2u ? (mag ? 0x3f000000u : 0u) : ((((mag >> 1) + 126u) << 23) | ((mag & 1u) << 22));
+  return __uint_as_float(bits | ((c & 8u) << 28));
+}
+// E8M0 scale byte -> 2^(b - 127) as fp32 (b = 0 is the subnormal 2^-127)
+__device__ __forceinline__ float e8m0_f32(uint32_t b) {
+  return b ? __uint_as_float(b << 23) : __uint_as_float(0x00400000u);
+}
 
 // Per-chunk dequantisation parameters of row `row` (of a [rows][cols] matrix), chunk `c`.
 struct ChunkQ {
@@ -58,6 +73,16 @@ __device__ __forceinline__ ChunkQ chunk_q(const uint8_t* scales, int row, int c,
     } else {
       q.s = __ldg(S);
     }
+  } else if constexpr (FMT == PMOE_MXFP4) {
+    // one scale byte per row and block of 32 inputs: chunk c is exactly block c
+    const uint8_t* X = scales + (size_t)row * (cols >> 5) + c;
+    uint32_t b;
+    if constexpr (COHERENT) {
+      asm volatile("ld.global.cg.u8 %0, [%1];" : "=r"(b) : "l"(X));
+    } else {
+      b = __ldg(X);
+    }
+    q.s = e8m0_f32(b);
   } else if constexpr (FMT == PMOE_INT4_GPTQ_G128) {
     const __half2* SZ = reinterpret_cast<const __half2*>(scales) + (size_t)row * (cols >> 7) + ((c * 32) >> 7);
     uint32_t raw;
@@ -112,6 +137,21 @@ __device__ __forceinline__ float chunk_dot(uint4 w, const uint4* av, ChunkQ q) {
         acc = fmaf(f0.y, bf_hi(a0), acc);
         acc = fmaf(f1.x, bf_lo(a1), acc);
         acc = fmaf(f1.y, bf_hi(a1), acc);
+      }
+    }
+    return acc * q.s;
+  } else if constexpr (FMT == PMOE_MXFP4) {
+    const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+    float acc = 0.f;
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      const uint4 a = load_act<FMT, SRC>(av + h);
+      const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
+      const uint32_t word = wv[h];  // 8 codes = elements 8h .. 8h+7, low nibble first
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        acc = fmaf(e2m1_f32(word >> (8 * k)), bf_lo(aw[k]), acc);
+        acc = fmaf(e2m1_f32(word >> (8 * k + 4)), bf_hi(aw[k]), acc);
       }
     }
     return acc * q.s;

@@ -352,6 +352,8 @@ __device__ __forceinline__ ChunkQ chunk_q_ring(const uint8_t* row_scales, int c)
   ChunkQ q{1.f, 0.f};
   if constexpr (FMT == PMOE_FP8_BLOCK128) {
     q.s = reinterpret_cast<const float*>(row_scales)[(c * 16) >> 7];
+  } else if constexpr (FMT == PMOE_MXFP4) {
+    q.s = e8m0_f32(row_scales[c]);  // one byte per block of 32 inputs: chunk c is block c
   } else if constexpr (FMT == PMOE_INT4_GPTQ_G128) {
     const uint32_t raw = reinterpret_cast<const uint32_t*>(row_scales)[(c * 32) >> 7];
     const float2 sz = __half22float2(*reinterpret_cast<const __half2*>(&raw));
@@ -794,8 +796,8 @@ __global__ void __launch_bounds__(kDfThreads, 1) decode_fused_kernel(const DfArg
                         (size_t)(((z + n - 1) >> 7) - (z >> 7) + 1) * row, vl, nl);
             lanes_copy4(src, dst, a.lay.gu_s + (size_t)((a.I + z) >> 7) * row,
                         (size_t)(((a.I + z + n - 1) >> 7) - ((a.I + z) >> 7) + 1) * row, vl, nl);
-          } else if constexpr (FMT == PMOE_INT4_GPTQ_G128) {
-            const size_t row = 4 * (size_t)hb;  // one row's (s, z) pairs
+          } else if constexpr (FMT == PMOE_INT4_GPTQ_G128 || FMT == PMOE_MXFP4) {
+            const size_t row = 4 * (size_t)hb;  // one row's scale bytes: (s, z) pairs, or E8M0 per 32 inputs
             lanes_copy4(src, dst, a.lay.gu_s + (size_t)z * row, (size_t)n * row, vl, nl);
             lanes_copy4(src, dst, a.lay.gu_s + (size_t)(a.I + z) * row, (size_t)n * row, vl, nl);
           }
@@ -805,7 +807,7 @@ __global__ void __launch_bounds__(kDfThreads, 1) decode_fused_kernel(const DfArg
             const size_t row = 4 * (size_t)ib;
             lanes_copy4(src, dst, a.lay.d_s + (size_t)(z >> 7) * row,
                         (size_t)(((z + n - 1) >> 7) - (z >> 7) + 1) * row, vl, nl);
-          } else if constexpr (FMT == PMOE_INT4_GPTQ_G128) {
+          } else if constexpr (FMT == PMOE_INT4_GPTQ_G128 || FMT == PMOE_MXFP4) {
             const size_t row = 4 * (size_t)ib;
             lanes_copy4(src, dst, a.lay.d_s + (size_t)z * row, (size_t)n * row, vl, nl);
           }
@@ -1093,6 +1095,9 @@ cudaError_t launch_decode_fused(int fmt, const __nv_bfloat16* x, const int32_t* 
   } else if (fmt == PMOE_INT4_GPTQ_G128) {
     if (nch1 <= 32 * 2 && nch2 <= 32 * 1) PMOE_DF(PMOE_INT4_GPTQ_G128, 2, 1);
     if (nch1 <= 32 * 4 && nch2 <= 32 * 2) PMOE_DF(PMOE_INT4_GPTQ_G128, 4, 2);
+  } else if (fmt == PMOE_MXFP4) {
+    if (nch1 <= 32 * 2 && nch2 <= 32 * 1) PMOE_DF(PMOE_MXFP4, 2, 1);
+    if (nch1 <= 32 * 4 && nch2 <= 32 * 2) PMOE_DF(PMOE_MXFP4, 4, 2);
   }
 #undef PMOE_DF
   return cudaErrorInvalidValue;

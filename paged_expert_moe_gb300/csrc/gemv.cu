@@ -261,6 +261,12 @@ ExpertLayout expert_layout(int fmt, int H, int I) {
     l.gu_s = n_gu + n_d;
     l.d_s = l.gu_s + 4 * (size_t)(2 * I / 128) * (H / 128);
     l.bytes = l.d_s + 4 * (size_t)(H / 128) * (I / 128);
+  } else if (fmt == PMOE_MXFP4) {
+    l.gu_w = 0;
+    l.d_w = n_gu / 2;
+    l.gu_s = l.d_w + n_d / 2;
+    l.d_s = l.gu_s + (size_t)(2 * I) * (H / 32);  // one E8M0 byte per row and 32 inputs
+    l.bytes = l.d_s + (size_t)H * (I / 32);
   } else {
     l.gu_w = 0;
     l.d_w = n_gu / 2;
@@ -289,6 +295,10 @@ cudaError_t launch_gemv_gateup(int fmt, const __nv_bfloat16* x, int T, int top_k
     const int nch = H / 32;
     if (nch <= 32 * 2) return gateup_t<PMOE_INT4_GPTQ_G128, 2, 4>(x, T, top_k, H, I, plan, E, wave, ws, arena, stride, lay, grid, s);
     if (nch <= 32 * 4) return gateup_t<PMOE_INT4_GPTQ_G128, 4, 4>(x, T, top_k, H, I, plan, E, wave, ws, arena, stride, lay, grid, s);
+  } else if (fmt == PMOE_MXFP4) {
+    const int nch = H / 32;
+    if (nch <= 32 * 2) return gateup_t<PMOE_MXFP4, 2, 4>(x, T, top_k, H, I, plan, E, wave, ws, arena, stride, lay, grid, s);
+    if (nch <= 32 * 4) return gateup_t<PMOE_MXFP4, 4, 4>(x, T, top_k, H, I, plan, E, wave, ws, arena, stride, lay, grid, s);
   }
   return cudaErrorInvalidValue;
 }
@@ -310,6 +320,10 @@ cudaError_t launch_gemv_down(int fmt, int H, int I, const int32_t* plan, int E, 
     const int nch = I / 32;
     if (nch <= 32 * 1) return down_t<PMOE_INT4_GPTQ_G128, 1, 8>(H, I, plan, E, wave, ws, arena, stride, lay, grid, s);
     if (nch <= 32 * 2) return down_t<PMOE_INT4_GPTQ_G128, 2, 4>(H, I, plan, E, wave, ws, arena, stride, lay, grid, s);
+  } else if (fmt == PMOE_MXFP4) {
+    const int nch = I / 32;
+    if (nch <= 32 * 1) return down_t<PMOE_MXFP4, 1, 8>(H, I, plan, E, wave, ws, arena, stride, lay, grid, s);
+    if (nch <= 32 * 2) return down_t<PMOE_MXFP4, 2, 4>(H, I, plan, E, wave, ws, arena, stride, lay, grid, s);
   }
   return cudaErrorInvalidValue;
 }

@@ -204,6 +204,23 @@ def test_decode_fp8_layer(pm):
     _decode_case(pm, 1, 128, 40, 1, 8, seed=21)
 
 
+@pytest.mark.parametrize("B,mode", [(1, 0), (2, 1), (4, 1)])
+def test_decode_mxfp4_layer(pm, B, mode):
+    """MXFP4 experts (E2M1 codes, E8M0 scale per 32 inputs), Qwen3 shape with 64 experts;
+    B=4 at K=24 runs several waves in some steps; SM-pull mode pages the scale rows in
+    with the weights."""
+    _decode_case(pm, 3, 64, 24, B, 8, seed=41 + B, mode=mode)
+
+
+def test_mxfp4_cache_is_decode_only(pm):
+    """The prefill path has no FP4 converter: a cache that could see more than 8 tokens is
+    refused at creation."""
+    with pytest.raises(pm.PmoeError) as ei:
+        pm.ExpertCache(64, 8, 2048, 768, 24, fmt=pm.PMOE_MXFP4, max_tokens=16)
+    assert ei.value.status == pm.PMOE_EUNSUPPORTED
+    pm.ExpertCache(64, 8, 2048, 768, 24, fmt=pm.PMOE_MXFP4, max_tokens=8).close()
+
+
 @pytest.mark.parametrize("B", [1, 4])
 def test_decode_int4_layer(pm, B):
     """B=4 at K=26 exceeds K // top_k = 3: some steps run several waves."""
