@@ -412,6 +412,11 @@ def run_ours(args):
             print(json.dumps({"metric": METRIC, "impl": "ours", "section": "fp8", "fp8": run_fp8(pm, torch, args, local,
                                                                                                   hbm_peak)}))
         return
+    if args.section == "mxfp4":
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "impl": "ours", "section": "mxfp4",
+                              "mxfp4": run_mxfp4(pm, torch, args, local, hbm_peak)}))
+        return
     if args.section in ("prefill", "stack", "decode_staged"):
         # one part of the bench alone (for profiling); one JSON line with that part
         out = {"metric": METRIC, "impl": "ours", "section": args.section}
@@ -448,6 +453,7 @@ def run_ours(args):
     prefill = {}
     stack = {}
     fp8 = None
+    mxfp4 = None
     h2d = measure_h2d(torch, torch.device("cuda", local))
     if not args.headline_only:
         others["B1_sm_pull_staged_no_graph"] = timed
@@ -462,6 +468,7 @@ def run_ours(args):
         prefill["cold_sm_pull"] = run_prefill(pm, torch, store, args.prefill_steps, 2, local, cold=True, mode=1)
         prefill["warm_all_resident"] = run_prefill(pm, torch, store, args.prefill_steps, 2, local, K=E, cold=False)
         fp8 = run_fp8(pm, torch, args, local, hbm_peak)
+        mxfp4 = run_mxfp4(pm, torch, args, local, hbm_peak)
         for B in (1, 4):
             stack[f"B{B}"] = run_stack(pm, torch, B, args.stack_steps, 3, local)
             stack[f"B{B}_graph"] = run_stack(pm, torch, B, args.stack_steps, 3, local, mode=1, graph=True)
@@ -521,6 +528,7 @@ def run_ours(args):
                       "decode_pagein_kind": "SM pull kernel (CUDA-event time on the copy stream)"},
         "prefill": _prefill_summary(prefill, hbm_peak, _peaks()[1]) if prefill else None,
         "fp8": fp8,
+        "mxfp4": mxfp4,
         "stack_int4": ({"workload": "48-layer Qwen3-30B-A3B-shaped MoE stack (attention omitted), GPTQ-int4 g128 "
                                     "experts, K=26 slots/layer, p=0.8 reuse routing per layer, residual stream",
                         "hbm_roofline_tokens_per_s_B1": hbm_peak * 1e9 / (STACK_L * TOPK * 2_506_752),
@@ -556,6 +564,24 @@ def run_fp8(pm, torch, args, local, hbm_peak):
             "prefill_512_cold": dict(pre, FLOP_per_step=flop, weight_bytes_per_step=E * ebytes,
                                      hbm_bound_tflops=flop / (E * ebytes / (hbm_peak * 1e9)) / 1e12,
                                      note="FP8 weights are dequantised to bf16 in shared memory for kind::f16 MMAs")}
+
+
+def run_mxfp4(pm, torch, args, local, hbm_peak):
+    """MXFP4 experts (E2M1 codes, an E8M0 scale per 32 inputs): the same layer, K=40,
+    decode B=1 over the p=0.8 reuse trace (MXFP4 caches are decode-only)."""
+    store = make_store(fmt=3)
+    ebytes = pm.pmoe_expert_bytes(3, H, I)
+    head = run_decode(pm, torch, store, 1, args.steps, args.warmup, local, e2e=False, mode=1, graph=True, fmt=3)
+    staged = run_decode(pm, torch, store, 1, args.steps, args.warmup, local, e2e=False, mode=1, stage=True, fmt=3)
+    kt = staged["kernel_times"]
+    dec_gbs = staged["expert_weight_bytes"] / (kt["decode"]["ms"] / 1e3) / 1e9
+    return {"workload": "Qwen3-30B-A3B-shaped MoE layer, MXFP4 experts (E2M1, E8M0 scale per 32 inputs), K=40",
+            "expert_bytes": ebytes,
+            "decode_B1": {"tokens_per_s": head["tokens_per_s"], "ms_per_step": head["ms_per_step"],
+                          "misses_per_step": head["misses_per_step"], "mode": head["mode"],
+                          "decode_kernel_gbs": dec_gbs, "decode_kernel_hbm_frac": dec_gbs / hbm_peak,
+                          "decode_kernel_us": kt["decode"]["ms"] / args.steps * 1e3,
+                          "decode_kernel_measured_in": "page-in staged ahead by the pull kernel"}}
 
 
 STACK_L, STACK_K = 48, 26
@@ -710,7 +736,7 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--prefill-steps", type=int, default=6)
     ap.add_argument("--stack-steps", type=int, default=60)
-    ap.add_argument("--section", default="all", choices=["all", "prefill", "stack", "decode_staged", "fp8"],
+    ap.add_argument("--section", default="all", choices=["all", "prefill", "stack", "decode_staged", "fp8", "mxfp4"],
                     help="run only one part (profiling); the default runs everything")
     args = ap.parse_args()
     if args.warmup < 3:

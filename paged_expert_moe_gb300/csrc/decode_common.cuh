@@ -7,6 +7,7 @@
 #include "pmoe_internal.h"
 
 #include <cuda_fp16.h>
+#include <cuda_fp4.h>
 #include <cuda_fp8.h>
 
 namespace pmoe {
@@ -43,14 +44,6 @@ template <> struct Fmt<PMOE_FP8_BLOCK128> { static constexpr int EPC = 16; stati
 template <> struct Fmt<PMOE_INT4_GPTQ_G128> { static constexpr int EPC = 32; static constexpr int BPE2 = 1; };
 template <> struct Fmt<PMOE_MXFP4> { static constexpr int EPC = 32; static constexpr int BPE2 = 1; };
 
-// FP4 E2M1 code (low 4 bits of c) -> fp32, from the fields: 1 sign bit, 2 exponent bits
-// with bias 1, 1 mantissa bit; exponent 0 is subnormal (m/2). The fp32 bit pattern of a
-// normal value puts exponent e - 1 + 127 in bits 23.. and the mantissa bit at bit 22.
-__device__ __forceinline__ float e2m1_f32(uint32_t c) {
-  const uint32_t mag = c & 7u;
-  const uint32_t bits = mag < 2u ? (mag ? 0x3f000000u : 0u) : ((((mag >> 1) + 126u) << 23) | ((mag & 1u) << 22));
-  return __uint_as_float(bits | ((c & 8u) << 28));
-}
 // E8M0 scale byte -> 2^(b - 127) as fp32 (b = 0 is the subnormal 2^-127)
 __device__ __forceinline__ float e8m0_f32(uint32_t b) {
   return b ? __uint_as_float(b << 23) : __uint_as_float(0x00400000u);
@@ -150,8 +143,11 @@ __device__ __forceinline__ float chunk_dot(uint4 w, const uint4* av, ChunkQ q) {
       const uint32_t word = wv[h];  // 8 codes = elements 8h .. 8h+7, low nibble first
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        acc = fmaf(e2m1_f32(word >> (8 * k)), bf_lo(aw[k]), acc);
-        acc = fmaf(e2m1_f32(word >> (8 * k + 4)), bf_hi(aw[k]), acc);
+        // one byte = two E2M1 codes -> two fp16 values (exact), low nibble first
+        const __half2_raw pr = __nv_cvt_fp4x2_to_halfraw2((__nv_fp4x2_storage_t)((word >> (8 * k)) & 0xffu), __NV_E2M1);
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&pr));
+        acc = fmaf(f.x, bf_lo(aw[k]), acc);
+        acc = fmaf(f.y, bf_hi(aw[k]), acc);
       }
     }
     return acc * q.s;
