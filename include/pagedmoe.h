@@ -46,6 +46,8 @@
  *                        c of a row in byte c/2, low nibble for even c),
  *                        X_gu u8 [2I][H/32], X_d u8 [H][I/32] (E8M0 scale per output
  *                        row and block of 32 inputs); w = e2m1(q) * 2^(X - 127)
+ *                        (X = 0xFF, NaN in the format, is read as 2^128: keep
+ *                        stores free of NaN scales)
  *                        (the OCP microscaling layout; the formats of section "What
  *                        does Paged Experts actually do?", PR #45787). Decode batches
  *                        only: a cache with MXFP4 experts takes max_tokens <= 8
