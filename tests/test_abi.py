@@ -34,8 +34,18 @@ def test_expert_sizes_from_the_library():
     assert pm.pmoe_expert_bytes(pm.PMOE_BF16, 2048, 768) == 9_437_184
     assert pm.pmoe_expert_bytes(pm.PMOE_FP8_BLOCK128, 2048, 768) == 4_719_744
     assert pm.pmoe_expert_bytes(pm.PMOE_INT4_GPTQ_G128, 2048, 768) == 2_506_752
+    assert pm.pmoe_expert_bytes(pm.PMOE_MXFP4, 2048, 768) == 2_506_752
     assert pm.pmoe_expert_bytes(pm.PMOE_FP8_BLOCK128, 200, 768) == 0
+    assert pm.pmoe_expert_bytes(pm.PMOE_MXFP4, 200, 768) == 0
     assert pm.pmoe_expert_bytes(7, 2048, 768) == 0
+
+
+@pytest.mark.parametrize("H,I", [(2048, 768), (128, 128), (4096, 1536), (1024, 256)])
+def test_library_expert_sizes_equal_the_oracle_layout(H, I):
+    import paged_expert_moe_gb300 as pm
+    from oracle import formats
+    for fmt in (pm.PMOE_BF16, pm.PMOE_FP8_BLOCK128, pm.PMOE_INT4_GPTQ_G128, pm.PMOE_MXFP4):
+        assert pm.pmoe_expert_bytes(fmt, H, I) == formats.expert_nbytes(fmt, H, I), (fmt, H, I)
 
 
 @pytest.mark.parametrize("desc", [
@@ -65,6 +75,16 @@ def test_create_rejects_unsupported_formats():
                                 format=pm.PMOE_INT4_GPTQ_G128, max_tokens=4, pagein_mode=0, device=0)
     h = ctypes.c_void_p()
     assert lib.expert_cache_create(ctypes.byref(d), ctypes.byref(h)) == pm.PMOE_EUNSUPPORTED
+
+
+def test_create_refuses_mxfp4_beyond_decode_batches():
+    import paged_expert_moe_gb300 as pm
+    lib = pm.load()
+    d = pm._lib.pmoe_cache_desc(num_experts=8, top_k=2, hidden=128, intermediate=128, num_slots=4, num_layers=1,
+                                format=pm.PMOE_MXFP4, max_tokens=16, pagein_mode=0, device=0)
+    h = ctypes.c_void_p()
+    assert lib.expert_cache_create(ctypes.byref(d), ctypes.byref(h)) == pm.PMOE_EUNSUPPORTED
+    assert not h.value
 
 
 def test_router_argument_checks_need_no_gpu():
