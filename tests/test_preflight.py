@@ -61,6 +61,9 @@ def test_sizing_from_the_library_layout():
     assert i4.arena_bytes == 26 * i4.slot_stride * 48 and i4.host_store_bytes == 128 * i4.slot_stride * 48
     assert i4.slots_fit == min(128, int(8e9 // (i4.slot_stride * 48)))
     assert bf.batch_cap == 5 and i4.batch_cap == 3
+    # MXFP4: packed E2M1 codes + one E8M0 byte per output row and block of 32 inputs
+    mx = pf.size(128, 8, 48, 26, "mxfp4", 2048, 768)
+    assert mx.expert_bytes == 2_359_296 + 1536 * 64 + 2048 * 24 == 2_506_752
 
 
 def test_cli_prints_the_three_lines(capsys):
