@@ -329,25 +329,38 @@ PMOE_API int expert_cache_kernel_times(pmoe_cache* cache, pmoe_kernel_times* out
  * no counterpart of this call; it exists for callers that cannot call cudaMalloc:
  * code running inside another framework's memory pool or allocator hooks, real-time
  * loops that must never enter the driver's allocator, and embedders whose device
- * memory is budgeted up front. It computes what moe_paged_forward computes for the
- * same tokens when every routed expert is resident, with the same kernels.
- *   experts   device: expert slots of pmoe_expert_bytes(format, H, I) bytes each,
- *             `stride` bytes apart (stride a multiple of 16)
- *   slot_of   device int32 [E]: slot of each expert in `experts`, or NULL when
- *             expert e sits in slot e; an expert with slot -1 contributes nothing
- *   x, residual, y, ids, w: as in moe_paged_forward (residual may be NULL)
+ * memory is budgeted up front. For the same tokens it computes the layer that
+ * moe_paged_forward computes when every routed expert is resident (same arithmetic
+ * order per pair, through the library's two-kernel GEMV decode); the outputs agree
+ * within the layer tolerances (bf16 and int4: relative Frobenius 1e-2; block FP8:
+ * 3e-2), not necessarily bit for bit.
+ *   experts   device: n_slots expert slots of pmoe_expert_bytes(format, H, I) bytes
+ *             each, `stride` bytes apart (stride a multiple of 16); 16-byte aligned
+ *   n_slots   slots in `experts`; at least E when slot_of is NULL
+ *   slot_of   device int32 [E]: slot of each expert in `experts`, or NULL when expert
+ *             e sits in slot e. A routed expert with slot -1 contributes nothing; any
+ *             other slot outside [0, n_slots) is an error: the expert is skipped and
+ *             error bit 4 is set
+ *   x, residual, y, ids, w: as in moe_paged_forward (residual may be NULL); x,
+ *             residual and y 16-byte aligned, ids and w 4-byte aligned
+ *   err_out   device int32 or NULL: after the call's kernels (stream-ordered) it
+ *             receives the call's device error bits: 0 = none, 1 = an id outside
+ *             [0, E) was skipped, 4 = an expert's slot was outside [0, n_slots)
  * Limits: E <= 1024, T <= 8, T * top_k <= 64, and the intermediates must fit the
  * library's fixed 2 MiB static device scratch ((P*(2I + 4H)) bytes plus small
- * tables, P = T * top_k); larger requests return PMOE_EINVAL with nothing enqueued.
+ * tables, P = T * top_k); larger requests, misaligned pointers and bad arguments
+ * return PMOE_EINVAL with nothing enqueued.
  * The first call on each device (with that device current) looks up the scratch
- * address once; make it before any stream capture. All calls share the one scratch
- * array: calls that overlap on the GPU race on it, so serialise them (one stream).
- * Invalid expert ids are skipped on the device. Nothing is synchronised.
+ * address once; with lazy module loading that also loads the library's device code
+ * holding the scratch, so this first call may allocate inside the driver: make it
+ * during warm-up, before any stream capture. All calls share the one scratch array,
+ * which keeps the last call's contents: calls that overlap on the GPU race on it, so
+ * serialise them (one stream). Nothing is synchronised.
  */
-PMOE_API int moe_decode_forward_noalloc(const void* experts, size_t stride, const int32_t* slot_of, int E,
-                                        int top_k, int H, int I, int format, const void* x, int T,
+PMOE_API int moe_decode_forward_noalloc(const void* experts, size_t stride, int n_slots, const int32_t* slot_of,
+                                        int E, int top_k, int H, int I, int format, const void* x, int T,
                                         const int32_t* ids, const float* w, const void* residual, void* y,
-                                        void* stream);
+                                        int32_t* err_out, void* stream);
 
 #ifdef __cplusplus
 }

@@ -69,7 +69,8 @@ _SIGS = {
     "expert_cache_read_slot": ([_P, _I, _I, _P, ctypes.c_size_t], _I),
     "expert_cache_set_timing": ([_P, _I], _I),
     "expert_cache_kernel_times": ([_P, ctypes.POINTER(pmoe_kernel_times)], _I),
-    "moe_decode_forward_noalloc": ([_P, ctypes.c_size_t, _P, _I, _I, _I, _I, _I, _P, _I, _P, _P, _P, _P, _P], _I),
+    "moe_decode_forward_noalloc": ([_P, ctypes.c_size_t, _I, _P, _I, _I, _I, _I, _I, _P, _I, _P, _P, _P, _P, _P,
+                                    _P], _I),
     "moe_paged_stack_forward": ([_P, _P, _I, _P, _P, _P, _P, _P], _I),
 }
 EXPORTED = tuple(_SIGS)
@@ -149,15 +150,32 @@ def moe_router_gemm_topk(x, router_weight, top_k, renormalize=True, ids_out=None
 
 
 def moe_decode_forward_noalloc(experts, stride, E, top_k, H, I, fmt, x, ids, w, y=None, slot_of=None,
-                               residual=None, stream=None):
+                               residual=None, err_out=None, n_slots=None, stream=None):
     """Decode MoE over experts already in device memory; allocates no device memory
     (the library uses a fixed static scratch). experts: CUDA uint8 tensor holding the
-    expert slots `stride` bytes apart; x: bf16 [T, H]; returns y."""
+    expert slots `stride` bytes apart (n_slots defaults to all of them); x: bf16 [T, H];
+    ids int32 / w fp32 [T, top_k]; slot_of: int32 [E] or None; err_out: int32 [1] that
+    receives the call's device error bits, or None. Returns y."""
     import torch
+    T = x.shape[0]
+    assert experts.is_cuda and experts.dtype == torch.uint8 and experts.is_contiguous()
+    assert x.is_cuda and x.dtype == torch.bfloat16 and x.is_contiguous() and x.shape == (T, H)
+    assert ids.is_cuda and ids.dtype == torch.int32 and ids.is_contiguous() and tuple(ids.shape) == (T, top_k)
+    assert w.is_cuda and w.dtype == torch.float32 and w.is_contiguous() and tuple(w.shape) == (T, top_k)
+    if slot_of is not None:
+        assert slot_of.is_cuda and slot_of.dtype == torch.int32 and slot_of.is_contiguous() and slot_of.numel() == E
+    if residual is not None:
+        assert residual.is_cuda and residual.dtype == torch.bfloat16 and residual.is_contiguous()
+        assert residual.shape == x.shape
+    if err_out is not None:
+        assert err_out.is_cuda and err_out.dtype == torch.int32 and err_out.numel() >= 1
+    if n_slots is None:
+        n_slots = experts.numel() // stride
     if y is None:
         y = torch.empty_like(x)
-    _check(load().moe_decode_forward_noalloc(_ptr(experts), stride, _ptr(slot_of), E, top_k, H, I, fmt, _ptr(x),
-                                             x.shape[0], _ptr(ids), _ptr(w), _ptr(residual), _ptr(y),
+    assert y.is_cuda and y.dtype == torch.bfloat16 and y.is_contiguous() and y.shape == x.shape
+    _check(load().moe_decode_forward_noalloc(_ptr(experts), stride, n_slots, _ptr(slot_of), E, top_k, H, I, fmt,
+                                             _ptr(x), T, _ptr(ids), _ptr(w), _ptr(residual), _ptr(y), _ptr(err_out),
                                              _stream_handle(stream)), "moe_decode_forward_noalloc")
     return y
 

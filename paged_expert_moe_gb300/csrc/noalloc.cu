@@ -12,11 +12,14 @@
 // Host code never names g_noalloc_scratch as an address: in host code that name is a
 // host-side stand-in, and a kernel given it would fault or read the wrong memory.
 // The first call on each device, with that device current, looks the device
-// address up once with cudaGetSymbolAddress and keeps it; make that first call
-// before any stream capture. Every call shares the one array, which keeps the
-// last call's contents: calls that overlap on the GPU (different streams, or
-// different host threads on one device) race on it and must be serialised by the
-// caller. The per-call error word at the start of the array is cleared each call.
+// address up once with cudaGetSymbolAddress and keeps it; with lazy module loading
+// that lookup is also what loads this file's device code and its array, so the
+// first call can enter the driver's allocator: make it during warm-up, before any
+// stream capture. Every call shares the one array, which keeps the last call's
+// contents: calls that overlap on the GPU (different streams, or different host
+// threads on one device) race on it and must be serialised by the caller. The
+// per-call error word at the start of the array is cleared each call and, when the
+// caller passes err_out, copied there after the call's kernels.
 #include "pmoe_internal.h"
 
 #include <mutex>
@@ -68,11 +71,17 @@ ScratchMap scratch_map(int E, int P, int H, int I) {
   return m;
 }
 
+// Slot of a routed expert: slot_of[e], or e when there is no map. -1 marks an expert
+// the caller holds no slot for; any other value outside [0, n_slots) is an error.
+__device__ __forceinline__ int expert_slot(const int32_t* __restrict__ slot_of, int e) {
+  return slot_of != nullptr ? slot_of[e] : e;
+}
+
 // One-wave plan for experts that are all resident: the distinct routed ids in
-// ascending order with their slots (slot_of[e], or e when slot_of is NULL). An
-// expert with no slot (slot_of[e] < 0) is left out of the plan and flagged.
+// ascending order with their slots. An expert without a valid slot is left out of
+// the plan; a slot other than -1 outside [0, n_slots) is also flagged.
 __global__ void __launch_bounds__(1024) resident_plan_kernel(const int32_t* __restrict__ ids, int P, int E,
-                                                             const int32_t* __restrict__ slot_of,
+                                                             const int32_t* __restrict__ slot_of, int n_slots,
                                                              int32_t* __restrict__ plan, int32_t* __restrict__ err) {
   __shared__ int s_used[kMaxExperts];
   __shared__ int s_scan[kMaxExperts];
@@ -87,9 +96,9 @@ __global__ void __launch_bounds__(1024) resident_plan_kernel(const int32_t* __re
   }
   __syncthreads();
   int used = (tid < E) ? s_used[tid] : 0;
-  const int slot = (used && slot_of != nullptr) ? slot_of[tid] : tid;
-  if (used && slot < 0) {
-    atomicOr(err, kErrBadSlot);
+  const int slot = used ? expert_slot(slot_of, tid) : -1;
+  if (used && (slot < 0 || slot >= n_slots)) {
+    if (slot != -1) atomicOr(err, kErrBadSlot);
     used = 0;
   }
   s_scan[tid] = used;
@@ -123,14 +132,19 @@ __global__ void __launch_bounds__(1024) resident_plan_kernel(const int32_t* __re
   }
 }
 
-// Pairs whose expert has no slot are left out of the combine (pos = -1).
+// Pairs whose expert has no valid slot are left out of the combine (pos = -1).
 __global__ void drop_unslotted_kernel(const int32_t* __restrict__ ids, int P, int E,
-                                      const int32_t* __restrict__ slot_of, Workspace ws) {
+                                      const int32_t* __restrict__ slot_of, int n_slots, Workspace ws) {
   for (int p = threadIdx.x; p < P; p += blockDim.x) {
     const int e = ids[p];
-    if (e >= 0 && e < E && slot_of[e] < 0) ws.pos[p] = -1;
+    if (e < 0 || e >= E) continue;
+    const int slot = expert_slot(slot_of, e);
+    if (slot < 0 || slot >= n_slots) ws.pos[p] = -1;
   }
 }
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+bool aligned4(const void* p) { return ((uintptr_t)p & 3u) == 0; }
 
 int setup_device(int dev, DeviceSetup** out) {
   if (dev < 0 || dev >= kMaxDevices) return PMOE_EUNSUPPORTED;
@@ -151,11 +165,12 @@ int setup_device(int dev, DeviceSetup** out) {
 
 using namespace pmoe;
 
-extern "C" int moe_decode_forward_noalloc(const void* experts, size_t stride, const int32_t* slot_of, int E,
-                                          int top_k, int H, int I, int format, const void* x, int T,
+extern "C" int moe_decode_forward_noalloc(const void* experts, size_t stride, int n_slots, const int32_t* slot_of,
+                                          int E, int top_k, int H, int I, int format, const void* x, int T,
                                           const int32_t* ids, const float* w, const void* residual, void* y,
-                                          void* stream) {
+                                          int32_t* err_out, void* stream) {
   if (E < 1 || E > kMaxExperts || top_k < 1 || top_k > E || T < 0 || T > kGemvMaxTokens) return PMOE_EINVAL;
+  if (n_slots < 1 || (slot_of == nullptr && n_slots < E)) return PMOE_EINVAL;
   if (H <= 0 || I <= 0 || H % 8 != 0 || I % 8 != 0 || H > 4096 || I > 1536) return PMOE_EINVAL;
   if (format != PMOE_BF16 && format != PMOE_FP8_BLOCK128 && format != PMOE_INT4_GPTQ_G128 && format != PMOE_MXFP4)
     return PMOE_EUNSUPPORTED;
@@ -166,8 +181,12 @@ extern "C" int moe_decode_forward_noalloc(const void* experts, size_t stride, co
   if (P > kNoallocMaxPairs) return PMOE_EINVAL;  // larger steps: use moe_paged_forward
   const ScratchMap m = scratch_map(E, P, H, I);
   if (m.total > kNoallocScratchBytes) return PMOE_EINVAL;  // the static scratch is 2 MiB
-  if (T == 0) return PMOE_OK;
-  if (experts == nullptr || x == nullptr || ids == nullptr || w == nullptr || y == nullptr || x == y)
+  if (T > 0 && (experts == nullptr || x == nullptr || ids == nullptr || w == nullptr || y == nullptr || x == y))
+    return PMOE_EINVAL;
+  // the kernels move experts, x, residual and y in 16-byte vectors
+  if (!aligned16(experts) || !aligned16(x) || !aligned16(y) || (residual != nullptr && !aligned16(residual)) ||
+      !aligned4(ids) || !aligned4(w) || (slot_of != nullptr && !aligned4(slot_of)) ||
+      (err_out != nullptr && !aligned4(err_out)))
     return PMOE_EINVAL;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PMOE_ECUDA;
@@ -186,20 +205,25 @@ extern "C" int moe_decode_forward_noalloc(const void* experts, size_t stride, co
   ws.h = (__nv_bfloat16*)(base + m.h);
   ws.o_part = (float*)(base + m.o_part);
   if (cudaMemsetAsync(err, 0, 4, s) != cudaSuccess) return PMOE_ECUDA;
-  resident_plan_kernel<<<1, 1024, 0, s>>>(ids, P, E, slot_of, plan, err);
-  if (cudaGetLastError() != cudaSuccess) return PMOE_ECUDA;
-  if (launch_group(ids, P, E, plan, ws, 0, err, s) != cudaSuccess) return PMOE_ECUDA;
-  if (slot_of != nullptr) {
-    drop_unslotted_kernel<<<1, 128, 0, s>>>(ids, P, E, slot_of, ws);
+  if (T > 0) {
+    resident_plan_kernel<<<1, 1024, 0, s>>>(ids, P, E, slot_of, n_slots, plan, err);
     if (cudaGetLastError() != cudaSuccess) return PMOE_ECUDA;
+    if (launch_group(ids, P, E, plan, ws, 0, err, s) != cudaSuccess) return PMOE_ECUDA;
+    if (slot_of != nullptr || n_slots < E) {
+      drop_unslotted_kernel<<<1, 128, 0, s>>>(ids, P, E, slot_of, n_slots, ws);
+      if (cudaGetLastError() != cudaSuccess) return PMOE_ECUDA;
+    }
+    const uint8_t* arena = (const uint8_t*)experts;
+    if (launch_gemv_gateup(format, (const __nv_bfloat16*)x, T, top_k, H, I, plan, E, 0, ws, arena, stride,
+                           ds->num_sms, s) != cudaSuccess)
+      return PMOE_ECUDA;
+    if (launch_gemv_down(format, H, I, plan, E, 0, ws, arena, stride, ds->num_sms, s) != cudaSuccess)
+      return PMOE_ECUDA;
+    if (launch_combine(ws, w, (const __nv_bfloat16*)residual, (__nv_bfloat16*)y, T, top_k, H, s) != cudaSuccess)
+      return PMOE_ECUDA;
   }
-  const uint8_t* arena = (const uint8_t*)experts;
-  if (launch_gemv_gateup(format, (const __nv_bfloat16*)x, T, top_k, H, I, plan, E, 0, ws, arena, stride,
-                         ds->num_sms, s) != cudaSuccess)
-    return PMOE_ECUDA;
-  if (launch_gemv_down(format, H, I, plan, E, 0, ws, arena, stride, ds->num_sms, s) != cudaSuccess)
-    return PMOE_ECUDA;
-  if (launch_combine(ws, w, (const __nv_bfloat16*)residual, (__nv_bfloat16*)y, T, top_k, H, s) != cudaSuccess)
+  // the call's device error bits, for a caller that wants them (stream-ordered)
+  if (err_out != nullptr && cudaMemcpyAsync(err_out, err, 4, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
     return PMOE_ECUDA;
   return PMOE_OK;
 }

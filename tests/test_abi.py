@@ -108,3 +108,32 @@ def test_null_cache_calls_are_rejected():
     assert lib.expert_cache_ensure_resident(nul, 0, nul, 1, nul, None) == pm.PMOE_EINVAL
     assert lib.expert_cache_reset(nul, 0) == pm.PMOE_EINVAL
     lib.expert_cache_destroy(nul)
+
+
+def test_noalloc_argument_checks_need_no_gpu():
+    """The allocation-free decode call refuses bad sizes, slot counts and misaligned
+    pointers on the host, before any CUDA call."""
+    import paged_expert_moe_gb300 as pm
+    lib = pm.load()
+    nul = ctypes.c_void_p(0)
+    p = ctypes.c_void_p
+    H, I, E, k = 256, 128, 16, 4
+    stride = pm.pmoe_expert_bytes(pm.PMOE_BF16, H, I)
+
+    def call(experts=0x10000, stride=stride, n_slots=E, slot_of=0, T=2, x=0x20000, ids=0x30000, w=0x40000,
+             residual=0, y=0x50000, err=0):
+        return lib.moe_decode_forward_noalloc(p(experts), stride, n_slots, p(slot_of), E, k, H, I, pm.PMOE_BF16,
+                                              p(x), T, p(ids), p(w), p(residual), p(y), p(err), nul)
+
+    assert call(T=9) == pm.PMOE_EINVAL              # beyond the static scratch's token limit
+    assert call(n_slots=E - 1) == pm.PMOE_EINVAL    # no slot map and fewer slots than experts
+    assert call(n_slots=0, slot_of=0x60000) == pm.PMOE_EINVAL
+    assert call(stride=stride - 16) == pm.PMOE_EINVAL
+    assert call(x=0x20008) == pm.PMOE_EINVAL        # x, y, experts, residual: 16-byte aligned
+    assert call(y=0x50004) == pm.PMOE_EINVAL
+    assert call(experts=0x10008) == pm.PMOE_EINVAL
+    assert call(residual=0x70002) == pm.PMOE_EINVAL
+    assert call(ids=0x30002) == pm.PMOE_EINVAL      # ids, w, slot_of, err_out: 4-byte aligned
+    assert call(err=0x80001) == pm.PMOE_EINVAL
+    assert call(x=0x20000, y=0x20000) == pm.PMOE_EINVAL  # y aliases x
+    assert call(ids=0) == pm.PMOE_EINVAL

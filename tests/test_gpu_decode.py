@@ -188,28 +188,39 @@ def _decode_case(pm, fmt, E, K, B, n_steps, seed, mode=0, fast_int4=False, check
     return L, steps, ys
 
 
+def _assert_bitwise_equal_to_all_resident(L, steps, ys, B, mode=0):
+    """Paging never changes the result (section "Can paging change the model's outputs?"):
+    the same steps with every expert resident (K = E) give the same bits."""
+    cache = hz.make_cache([L], 8, L.E, max_tokens=B, mode=mode)
+    ys_full = _run_steps(cache, steps)
+    cache.close()
+    for i, (a, b) in enumerate(zip(ys, ys_full)):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16)), f"step {i} differs from K={L.E}"
+
+
 @pytest.mark.parametrize("B", [1, 2, 4])
 def test_decode_bf16_qwen3_layer(pm, B):
     """Qwen3-30B-A3B-shaped layer, bf16, K=40, p=0.8 reuse routing; against the oracle
     and bit for bit against K=128 (everything resident)."""
     L, steps, ys = _decode_case(pm, 0, 128, 40, B, 10, seed=10 + B)
-    cache = hz.make_cache([L], 8, 128, max_tokens=B)
-    ys_full = _run_steps(cache, steps)
-    cache.close()
-    for a, b in zip(ys, ys_full):
-        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    _assert_bitwise_equal_to_all_resident(L, steps, ys, B)
 
 
-def test_decode_fp8_layer(pm):
-    _decode_case(pm, 1, 128, 40, 1, 8, seed=21)
+@pytest.mark.parametrize("B,K,mode", [(1, 40, 0), (4, 26, 1)])
+def test_decode_fp8_layer(pm, B, K, mode):
+    """Block-FP8 experts: against the oracle, and bit for bit against K=128; B=4 at K=26
+    runs several waves in some steps."""
+    L, steps, ys = _decode_case(pm, 1, 128, K, B, 8, seed=21 + B, mode=mode)
+    _assert_bitwise_equal_to_all_resident(L, steps, ys, B, mode=mode)
 
 
 @pytest.mark.parametrize("B,mode", [(1, 0), (2, 1), (4, 1)])
 def test_decode_mxfp4_layer(pm, B, mode):
     """MXFP4 experts (E2M1 codes, E8M0 scale per 32 inputs), Qwen3 shape with 64 experts;
     B=4 at K=24 runs several waves in some steps; SM-pull mode pages the scale rows in
-    with the weights."""
-    _decode_case(pm, 3, 64, 24, B, 8, seed=41 + B, mode=mode)
+    with the weights. Bit for bit equal to K=64 (everything resident)."""
+    L, steps, ys = _decode_case(pm, 3, 64, 24, B, 8, seed=41 + B, mode=mode)
+    _assert_bitwise_equal_to_all_resident(L, steps, ys, B, mode=mode)
 
 
 def test_mxfp4_cache_is_decode_only(pm):
@@ -221,10 +232,12 @@ def test_mxfp4_cache_is_decode_only(pm):
     pm.ExpertCache(64, 8, 2048, 768, 24, fmt=pm.PMOE_MXFP4, max_tokens=8).close()
 
 
-@pytest.mark.parametrize("B", [1, 4])
-def test_decode_int4_layer(pm, B):
-    """B=4 at K=26 exceeds K // top_k = 3: some steps run several waves."""
-    _decode_case(pm, 2, 128, 26, B, 8, seed=31 + B)
+@pytest.mark.parametrize("B,K", [(1, 40), (4, 26)])
+def test_decode_int4_layer(pm, B, K):
+    """B=4 at K=26 exceeds K // top_k = 3: some steps run several waves. Bit for bit
+    equal to K=128 (everything resident)."""
+    L, steps, ys = _decode_case(pm, 2, 128, K, B, 8, seed=31 + B)
+    _assert_bitwise_equal_to_all_resident(L, steps, ys, B)
 
 
 def test_sm_pull_mode_is_bitwise_identical_to_copy_engine(pm):

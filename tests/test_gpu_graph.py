@@ -28,6 +28,10 @@ def pm():
 
 @pytest.mark.parametrize("B", [1, 4])
 def test_captured_decode_step_matches_uncaptured(pm, B):
+    """The headline configuration (E=128, K=40, SM-pull page-in inside the decode kernel,
+    the step replayed as one graph): every replayed step equals the uncaptured run bit
+    for bit and the oracle within the bf16 tolerances."""
+    from oracle import router as orouter
     E, k, H, I, K, steps = 128, 8, 2048, 768, 40, 12
     L = hz.SyntheticLayer(0, E, H, I, seed=700)
     rng = np.random.default_rng(700 + B)
@@ -56,6 +60,9 @@ def test_captured_decode_step_matches_uncaptured(pm, B):
         g.replay()
         torch.cuda.synchronize()
         assert torch.equal(y_s.view(torch.int16), ys_ref[i].view(torch.int16)), f"step {i}"
+        ids_o, w_o = orouter.router_topk(logits, k)
+        assert np.array_equal(ids_s.cpu().numpy(), ids_o), f"step {i}: routing"
+        hz.assert_layer_close(hz.bf16_to_f64(y_s), L.oracle_y(x_bits, ids_o, w_o), 0)
     assert cache.expert_cache_stats(0) == ref.expert_cache_stats(0)
     assert cache.expert_cache_slot_table(0)[0].tolist() == ref.expert_cache_slot_table(0)[0].tolist()
     cache.close()

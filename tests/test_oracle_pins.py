@@ -176,6 +176,36 @@ def test_stack_activation_count_is_layers_times_top_k():
     assert n == 384 == preflight.activations_per_token(48, 8)
 
 
+def test_residual_stack_with_zero_down_projections_returns_its_input():
+    """With every W_d = 0 each layer adds nothing to the residual stream, so the stack is
+    the identity on x (a dropped residual would return 0, a doubled one 2^L x)."""
+    rng = np.random.default_rng(11)
+    H, I, E, k, L = 12, 6, 5, 2, 3
+    Ws = [_dense_weights(rng, H, I) for _ in range(E)]
+    zeroed = [(Wg, Wu, np.zeros_like(Wd)) for Wg, Wu, Wd in Ws]
+    x = rng.standard_normal((4, H))
+    layers = []
+    for _ in range(L):
+        ids, w = router.router_topk(rng.standard_normal((4, E)).astype(np.float32), k)
+        layers.append((ids, w, lambda e: zeroed[e]))
+    h, n = moe.moe_stack(x, layers, residual=True)
+    assert np.array_equal(h, x) and n == 4 * k * L
+
+
+def test_residual_stack_matches_a_hand_built_two_layer_decoder():
+    """Two layers with one expert each (k = 1, weight 1): h1 = x + MLP_0(x), h2 = h1 +
+    MLP_1(h1), every MLP from torch.nn.functional (a decoder block's residual add)."""
+    rng = np.random.default_rng(12)
+    H, I = 16, 8
+    W0, W1 = _dense_weights(rng, H, I, 0.3), _dense_weights(rng, H, I, 0.3)
+    x = rng.standard_normal((3, H))
+    one = (np.zeros((3, 1), np.int32), np.ones((3, 1)))
+    h, n = moe.moe_stack(x, [(*one, lambda e: W0), (*one, lambda e: W1)], residual=True)
+    h1 = x + _torch_swiglu(x, *W0)
+    np.testing.assert_allclose(h, h1 + _torch_swiglu(h1, *W1), rtol=1e-12, atol=1e-14)
+    assert n == 6
+
+
 # ----------------------------------------------------------------------------- formats
 
 def test_expert_sizes_match_the_layout_closed_forms():

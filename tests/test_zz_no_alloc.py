@@ -1,15 +1,17 @@
-"""The allocation-free decode entry point, against moe_paged_forward.
+"""The allocation-free decode entry point, against the oracle and moe_paged_forward.
 
 moe_decode_forward_noalloc serves callers that cannot call cudaMalloc (code inside
 another framework's memory pool or allocator hooks, real-time loops that must not
 enter the driver's allocator, embedders with a fixed device-memory budget): it keeps
-its intermediates in the library's fixed static device scratch. This file runs last
-(pytest collects it after the others) and also passes on its own in a fresh process.
+its intermediates in the library's fixed static device scratch. Every case makes two
+calls in a row on that shared scratch. This file runs last (pytest collects it after
+the others) and also passes on its own in a fresh process.
 """
 
 import numpy as np
 import pytest
 
+from oracle import router as orouter
 from tests import _harness as hz
 from workloads import generators as gen
 
@@ -28,61 +30,98 @@ def pm():
 
 def _experts_on_device(store, stride, order=None):
     E, nb = store.shape
-    buf = np.zeros((E, stride), np.uint8)
-    for slot in range(E):
+    n = E if order is None else len(order)
+    buf = np.zeros((n, stride), np.uint8)
+    for slot in range(n):
         e = slot if order is None else order[slot]
         buf[slot, :nb] = store[e]
     return torch.from_numpy(buf).cuda()
 
 
-@pytest.mark.parametrize("fmt", [0, 2])
-def test_noalloc_matches_paged_forward_on_two_calls(pm, fmt):
+@pytest.mark.parametrize("fmt", [0, 1, 2, 3])
+def test_noalloc_matches_oracle_and_paged_forward_on_two_calls(pm, fmt):
+    """Qwen3 shape (H=2048, I=768), 32 experts, 4 tokens, every format: each of two calls
+    in a row is within the layer tolerance of the oracle and of moe_paged_forward, and
+    reports no device error."""
     E, k, H, I, T = 32, 8, 2048, 768, 4
-    L = hz.SyntheticLayer(fmt, E, H, I, seed=77)
+    L = hz.SyntheticLayer(fmt, E, H, I, seed=77 + fmt)
     nb = pm.pmoe_expert_bytes(fmt, H, I)
     stride = (nb + 4095) // 4096 * 4096
     experts = _experts_on_device(L.store, stride)
     cache = hz.make_cache([L], k, E, max_tokens=T)
-    rng = np.random.default_rng(78)
+    err = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    rng = np.random.default_rng(78 + fmt)
     for call in range(2):
         sets = gen.uniform_routing_sets(rng, T, E, k)
         x_bits, logits = hz.step_inputs(rng, sets, E, H)
         x = hz.to_device_bf16(x_bits)
         ids, w = pm.moe_router_topk(torch.from_numpy(logits).cuda(), k)
-        y_ref = cache.moe_paged_forward(0, x, ids, w)
-        y = pm.moe_decode_forward_noalloc(experts, stride, E, k, H, I, fmt, x, ids, w)
+        y_paged = cache.moe_paged_forward(0, x, ids, w)
+        y = pm.moe_decode_forward_noalloc(experts, stride, E, k, H, I, fmt, x, ids, w, err_out=err)
         torch.cuda.synchronize()
-        hz.assert_layer_close(hz.bf16_to_f64(y), hz.bf16_to_f64(y_ref), fmt)
+        assert int(err.item()) == 0, f"call {call}: device error bits {int(err.item())}"
+        ids_o, w_o = orouter.router_topk(logits, k)
+        hz.assert_layer_close(hz.bf16_to_f64(y), L.oracle_y(x_bits, ids_o, w_o), fmt)
+        hz.assert_layer_close(hz.bf16_to_f64(y), hz.bf16_to_f64(y_paged), fmt)
     cache.close()
 
 
-def test_noalloc_with_a_slot_map_and_limits(pm):
+def test_noalloc_slot_map_absent_and_out_of_range_slots(pm):
+    """A permuted slot map over fewer slots than experts: an expert with slot -1 and an
+    expert whose slot lies past the last slot both contribute nothing (the oracle with
+    their weighted terms removed); only the second raises the bad-slot error bit."""
     E, k, H, I, T = 16, 4, 256, 128, 2
     L = hz.SyntheticLayer(0, E, H, I, seed=79)
     nb = pm.pmoe_expert_bytes(0, H, I)
     stride = nb
-    order = np.random.default_rng(80).permutation(E)  # slot s holds expert order[s]
+    rng = np.random.default_rng(80)
+    n_slots = E - 2
+    order = rng.permutation(E)[:n_slots]  # slot s holds expert order[s]
     experts = _experts_on_device(L.store, stride, order)
-    slot_of = torch.tensor(np.argsort(order).astype(np.int32)).cuda()
-    cache = hz.make_cache([L], k, E, max_tokens=T)
-    rng = np.random.default_rng(81)
+    slot_np = np.full(E, -1, np.int32)
+    slot_np[order] = np.arange(n_slots, dtype=np.int32)
+    absent = [e for e in range(E) if slot_np[e] < 0]
+    assert len(absent) == 2
+    bad = absent[1]
+    slot_np[bad] = n_slots  # one past the end of `experts`: must be refused on the device
+    slot_of = torch.from_numpy(slot_np).cuda()
+    err = torch.full((1,), -1, dtype=torch.int32, device="cuda")
     for call in range(2):
         sets = gen.uniform_routing_sets(rng, T, E, k)
+        others = [int(e) for e in rng.permutation([e for e in range(E) if e not in absent])[:k - 2]]
+        sets[0] = [absent[0], bad] + others  # token 0 routes to both slotless experts
         x_bits, logits = hz.step_inputs(rng, sets, E, H)
         x = hz.to_device_bf16(x_bits)
         ids, w = pm.moe_router_topk(torch.from_numpy(logits).cuda(), k)
-        y_ref = cache.moe_paged_forward(0, x, ids, w)
-        y = pm.moe_decode_forward_noalloc(experts, stride, E, k, H, I, 0, x, ids, w, slot_of=slot_of)
+        y = pm.moe_decode_forward_noalloc(experts, stride, E, k, H, I, 0, x, ids, w, slot_of=slot_of,
+                                          n_slots=n_slots, err_out=err)
         torch.cuda.synchronize()
-        hz.assert_layer_close(hz.bf16_to_f64(y), hz.bf16_to_f64(y_ref), 0)
-    cache.close()
-    # beyond the static scratch's limits: rejected before anything is enqueued
+        assert int(err.item()) == 4, f"call {call}: device error bits {int(err.item())}"
+        ids_o, w_o = orouter.router_topk(logits, k)
+        assert absent[0] in ids_o[0] and bad in ids_o[0]
+        w_kept = np.where(np.isin(ids_o, absent), 0.0, w_o)
+        hz.assert_layer_close(hz.bf16_to_f64(y), L.oracle_y(x_bits, ids_o, w_kept), 0)
+
+
+def test_noalloc_rejects_requests_beyond_its_limits(pm):
+    E, k, H, I = 16, 4, 256, 128
+    L = hz.SyntheticLayer(0, E, H, I, seed=81)
+    stride = pm.pmoe_expert_bytes(0, H, I)
+    experts = _experts_on_device(L.store, stride)
     x9 = torch.zeros((9, H), dtype=torch.bfloat16, device="cuda")
     ids9 = torch.zeros((9, k), dtype=torch.int32, device="cuda")
     w9 = torch.zeros((9, k), dtype=torch.float32, device="cuda")
-    with pytest.raises(pm.PmoeError) as ei:
-        pm.moe_decode_forward_noalloc(experts, stride, E, k, H, I, 0, x9, ids9, w9)
-    assert ei.value.status == pm.PMOE_EINVAL
-    with pytest.raises(pm.PmoeError) as ei:
-        pm.moe_decode_forward_noalloc(experts, stride - 16, E, k, H, I, 0, x9[:1], ids9[:1], w9[:1])
-    assert ei.value.status == pm.PMOE_EINVAL
+
+    def status(**kw):
+        with pytest.raises(pm.PmoeError) as ei:
+            args = dict(experts=experts, stride=stride, E=E, top_k=k, H=H, I=I, fmt=0, x=x9[:1], ids=ids9[:1],
+                        w=w9[:1])
+            args.update(kw)
+            pm.moe_decode_forward_noalloc(**args)
+        return ei.value.status
+
+    assert status(x=x9, ids=ids9, w=w9) == pm.PMOE_EINVAL  # T > 8: beyond the static scratch
+    assert status(stride=stride - 16) == pm.PMOE_EINVAL  # a slot shorter than one expert
+    assert status(n_slots=E - 1) == pm.PMOE_EINVAL  # no slot map, fewer slots than experts
+    xm = torch.zeros((2 * H + 8,), dtype=torch.bfloat16, device="cuda")[1:H + 1].view(1, H)
+    assert status(x=xm) == pm.PMOE_EINVAL  # x not 16-byte aligned
