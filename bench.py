@@ -453,12 +453,13 @@ def run_prefill_sweep(pm, torch, args, local, hbm_peak, tc_peak):
     bf16 tokens, 1024 at 16384): all experts resident (the GEMMs alone), bf16 and block FP8."""
     out = {}
     sizes = [int(t) for t in args.prefill_tokens.split(",") if t.strip()]
-    for fmt, name, bpe in ((0, "bf16", 2), (1, "fp8", 1)):
+    for fmt, name, bpe in ((0, "bf16", 2), (1, "fp8", 1), (3, "mxfp4", 0.5)):
         store = make_store(fmt=fmt)
         runs = {f"T{T}_warm_all_resident": run_prefill(pm, torch, store, args.prefill_steps, 2, local, K=E, cold=False,
                                                        fmt=fmt, T=T, n_inputs=2) for T in sizes}
         out[name] = _prefill_summary(runs, hbm_peak, tc_peak, wbytes_per_elem=bpe)
     out["fp8"]["note"] = "FP8 weights are dequantised to bf16 in shared memory for kind::f16 MMAs"
+    out["mxfp4"]["note"] = "MXFP4 weights (E2M1 x E8M0, exact in bf16) are dequantised in shared memory for kind::f16 MMAs"
     return out
 
 
@@ -486,7 +487,7 @@ def _summary(out):
         sm[f"prefill2048_{name}_tok_s"] = r3(g(out, "prefill", name, "tokens_per_s"))
         sm[f"prefill2048_{name}_gemm_tflops"] = r3(g(out, "prefill", name, "gemm_tflops"))
         sm[f"prefill2048_{name}_bound_frac"] = r3(g(out, "prefill", name, "bound_frac"))
-    for fmt in ("bf16", "fp8"):
+    for fmt in ("bf16", "fp8", "mxfp4"):
         for k_, v in (g(out, "prefill_sweep", fmt) or {}).items():
             if isinstance(v, dict) and "gemm_tflops" in v:
                 sm[f"prefill_{fmt}_{k_}"] = {"gemm_tflops": r3(v["gemm_tflops"]), "tensor_frac": r3(v["tensor_frac"]),
@@ -497,6 +498,7 @@ def _summary(out):
     sm["fp8_prefill512_gemm_tflops"] = r3(g(out, "fp8", "prefill_512_cold", "gemm_tflops"))
     sm["mxfp4_decode_B1_tok_s"] = r3(g(out, "mxfp4", "decode_B1", "tokens_per_s"))
     sm["mxfp4_decode_kernel_hbm_frac"] = r3(g(out, "mxfp4", "decode_B1", "decode_kernel_hbm_frac"))
+    sm["mxfp4_prefill512_gemm_tflops"] = r3(g(out, "mxfp4", "prefill_512_cold", "gemm_tflops"))
     for k_ in ("B1", "B1_graph", "B4", "B4_graph"):
         sm[f"stack_int4_{k_}_tok_s"] = r3(g(out, "stack_int4", k_, "tokens_per_s"))
         ov = g(out, "stack_int4", k_, "overlap")
@@ -702,20 +704,26 @@ def run_fp8(pm, torch, args, local, hbm_peak):
 
 def run_mxfp4(pm, torch, args, local, hbm_peak):
     """MXFP4 experts (E2M1 codes, an E8M0 scale per 32 inputs): the same layer, K=40,
-    decode B=1 over the p=0.8 reuse trace (MXFP4 caches are decode-only)."""
+    decode B=1 over the p=0.8 reuse trace, plus a cold 512-token prefill."""
     store = make_store(fmt=3)
     ebytes = pm.pmoe_expert_bytes(3, H, I)
     head = run_decode(pm, torch, store, 1, args.steps, args.warmup, local, e2e=False, mode=1, graph=True, fmt=3)
     staged = run_decode(pm, torch, store, 1, args.steps, args.warmup, local, e2e=False, mode=1, stage=True, fmt=3)
     kt = staged["kernel_times"]
     dec_gbs = staged["expert_weight_bytes"] / (kt["decode"]["ms"] / 1e3) / 1e9
+    pre = run_prefill(pm, torch, store, args.prefill_steps, 2, local, K=40, cold=True, fmt=3, T=512)
+    flop = 2.0 * 512 * TOPK * 3 * H * I
     return {"workload": "Qwen3-30B-A3B-shaped MoE layer, MXFP4 experts (E2M1, E8M0 scale per 32 inputs), K=40",
             "expert_bytes": ebytes,
             "decode_B1": {"tokens_per_s": head["tokens_per_s"], "ms_per_step": head["ms_per_step"],
                           "misses_per_step": head["misses_per_step"], "mode": head["mode"],
                           "decode_kernel_gbs": dec_gbs, "decode_kernel_hbm_frac": dec_gbs / hbm_peak,
                           "decode_kernel_us": kt["decode"]["ms"] / args.steps * 1e3,
-                          "decode_kernel_measured_in": "page-in staged ahead by the pull kernel"}}
+                          "decode_kernel_measured_in": "page-in staged ahead by the pull kernel"},
+            "prefill_512_cold": dict(pre, FLOP_per_step=flop, weight_bytes_per_step=E * ebytes,
+                                     hbm_bound_tflops=flop / (E * ebytes / (hbm_peak * 1e9)) / 1e12,
+                                     note="E2M1 x E8M0 weights are dequantised (exactly) to bf16 in shared memory "
+                                          "for kind::f16 MMAs")}
 
 
 STACK_L, STACK_K = 48, 26

@@ -49,10 +49,9 @@
  *                        (X = 0xFF, NaN in the format, is read as 2^128: keep
  *                        stores free of NaN scales)
  *                        (the OCP microscaling layout; the formats of section "What
- *                        does Paged Experts actually do?", PR #45787). Decode batches
- *                        only: a cache with MXFP4 experts takes max_tokens <= 8
- *                        (PMOE_EUNSUPPORTED otherwise; the prefill path has no FP4
- *                        converter).
+ *                        does Paged Experts actually do?", PR #45787). E2M1 times an
+ *                        E8M0 scale is exact in bf16 (scales 2^-126 .. 2^125), so the
+ *                        prefill path dequantises these weights without rounding.
  * FP8, int4 and MXFP4 need H and I multiples of 128; bf16 needs multiples of 8 (and,
  * for the tensor-core prefill path, H a multiple of 128 and I of 128).
  *

@@ -336,8 +336,6 @@ int expert_cache_create(const pmoe_cache_desc* desc, pmoe_cache** out) {
   {
     const int v = validate_shape(d.format, d.hidden, d.intermediate);
     if (v != PMOE_OK) return v;
-    // MXFP4 experts run in the decode kernels only (the prefill path has no FP4 converter)
-    if (d.format == PMOE_MXFP4 && d.max_tokens > kGemvMaxTokens) return PMOE_EUNSUPPORTED;
   }
   PMOE_CUDA(cudaSetDevice(d.device));
   cudaDeviceProp prop;

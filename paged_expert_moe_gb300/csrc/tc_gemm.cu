@@ -25,6 +25,7 @@
 
 #include <cuda.h>
 #include <cuda_fp16.h>
+#include <cuda_fp4.h>
 #include <cuda_fp8.h>
 #include <cstdio>
 
@@ -148,10 +149,12 @@ struct TcCfg {
   static constexpr int kABytes = 128 * kBK * 2;            // bf16 A tile (MMA operand)
   static constexpr int kBBytes = NMAX * kBK * 2;           // bf16 B tile (up to NMAX pairs)
   // quantised A tile as loaded by TMA, before the converter warps dequantise it
-  static constexpr int kQBytes = FMT == PMOE_FP8_BLOCK128 ? 128 * kBK : FMT == PMOE_INT4_GPTQ_G128 ? 128 * kBK / 2 : 0;
+  static constexpr int kQBytes = FMT == PMOE_FP8_BLOCK128                           ? 128 * kBK
+                                 : (FMT == PMOE_INT4_GPTQ_G128 || FMT == PMOE_MXFP4) ? 128 * kBK / 2
+                                                                                     : 0;
   static constexpr int kStageBytes = kABytes + kBBytes + kQBytes;
   static constexpr int kStagingFloats = 128 * 17;
-  // quantised formats: each converter thread's row of scales (<= 16 per row), padded
+  // quantised formats: each converter thread's row of scales (<= 16 words per row), padded
   static constexpr int kScaleWords = FMT == PMOE_BF16 ? 0 : 128 * 17;
   static constexpr int kFixedBytes = kStagingFloats * 4 + kScaleWords * 4 + 1024 + 512;
   static constexpr int kStagesFit = (220 * 1024 - kFixedBytes) / kStageBytes;
@@ -332,8 +335,9 @@ __global__ void __launch_bounds__(TcCfg<FMT, NMAX>::kThreads, 1)
   } else if (kQuant && warp >= 6) {
     // ---------------- converters: warps 6..9, thread r owns row r of the A tile. Each
     // quantised row (64 K values) is dequantised with its scale (block-FP8: the fp32
-    // scale of its 128x128 block; int4: (q - z) * s of its group of 128) to bf16 and
-    // written in the 128-byte-swizzled K-major layout TMA would have produced.
+    // scale of its 128x128 block; int4: (q - z) * s of its group of 128; MXFP4: the E2M1
+    // value times 2^(X - 127) of its block of 32, exact in bf16) to bf16 and written in
+    // the 128-byte-swizzled K-major layout TMA would have produced.
     const int r = threadIdx.x - 192;
     int s = 0;
     uint32_t ph = 0;
@@ -346,7 +350,8 @@ __global__ void __launch_bounds__(TcCfg<FMT, NMAX>::kThreads, 1)
       const int cols = GATEUP ? H : I;
       const uint8_t* sc = ex + (GATEUP ? lay.gu_s : lay.d_s);
       // this row's scales (block-FP8: one fp32 per 128-column block of its block row;
-      // int4: one (s, z) pair per group), read once per item instead of once per stage
+      // int4: one (s, z) pair per group; MXFP4: one E8M0 byte per 32 columns, four to a
+      // word), read once per item instead of once per stage
       const int nblk = cols >> 7;
       const uint32_t* srow = reinterpret_cast<const uint32_t*>(sc) +
                              (FMT == PMOE_FP8_BLOCK128 ? (size_t)(grow >> 7) * nblk : (size_t)grow * nblk);
@@ -379,6 +384,27 @@ __global__ void __launch_bounds__(TcCfg<FMT, NMAX>::kThreads, 1)
               const __nv_bfloat162 b1 = __floats2bfloat162_rn(f1.x * sv, f1.y * sv);
               out[2 * h] = *reinterpret_cast<const uint32_t*>(&b0);
               out[2 * h + 1] = *reinterpret_cast<const uint32_t*>(&b1);
+            }
+            arow[c ^ (r & 7)] = make_uint4(out[0], out[1], out[2], out[3]);
+          }
+        } else if (FMT == PMOE_MXFP4) {
+          // 64 codes = two blocks of 32, each with its own E8M0 byte
+          const uint8_t* q = st + C::kABytes + C::kBBytes + r * (kBK / 2);
+          const uint32_t xw = cached ? my_sc[(kb * kBK) >> 7] : __ldg(srow + ((kb * kBK) >> 7));
+          const int xb = ((kb * kBK) >> 5) & 3;  // first of the stage's two scale bytes in the word
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint32_t word = *reinterpret_cast<const uint32_t*>(q + c * 4);  // 8 codes, low nibble first
+            const uint32_t xbyte = (xw >> (8 * (xb + (c >> 2)))) & 0xffu;
+            const float sv = xbyte ? __uint_as_float(xbyte << 23) : __uint_as_float(0x00400000u);
+            uint32_t out[4];
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              const __half2_raw pr =
+                  __nv_cvt_fp4x2_to_halfraw2((__nv_fp4x2_storage_t)((word >> (8 * h)) & 0xffu), __NV_E2M1);
+              const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&pr));
+              const __nv_bfloat162 bv = __floats2bfloat162_rn(f.x * sv, f.y * sv);
+              out[h] = *reinterpret_cast<const uint32_t*>(&bv);
             }
             arow[c ^ (r & 7)] = make_uint4(out[0], out[1], out[2], out[3]);
           }
@@ -545,8 +571,8 @@ int tc_make_weight_maps(uint8_t* arena, size_t stride, int K, int H, int I, int 
     const cuuint32_t box[3] = {(cuuint32_t)kBK, 128, 1};
     return encode(&out->d, arena + lay.d_w, 3, dims, strides, box) == PMOE_OK ? PMOE_OK : PMOE_ECUDA;
   }
-  if (fmt != PMOE_FP8_BLOCK128 && fmt != PMOE_INT4_GPTQ_G128) return PMOE_EUNSUPPORTED;
-  // quantised weights are loaded as bytes (one e4m3 or two int4 per byte), unswizzled
+  if (fmt != PMOE_FP8_BLOCK128 && fmt != PMOE_INT4_GPTQ_G128 && fmt != PMOE_MXFP4) return PMOE_EUNSUPPORTED;
+  // quantised weights are loaded as bytes (one e4m3, or two int4 / E2M1 codes, per byte), unswizzled
   const cuuint64_t hb = fmt == PMOE_FP8_BLOCK128 ? (cuuint64_t)H : (cuuint64_t)H / 2;
   const cuuint64_t ib = fmt == PMOE_FP8_BLOCK128 ? (cuuint64_t)I : (cuuint64_t)I / 2;
   const cuuint32_t kbb = fmt == PMOE_FP8_BLOCK128 ? (cuuint32_t)kBK : (cuuint32_t)kBK / 2;
@@ -586,6 +612,8 @@ cudaError_t tc_gateup(int fmt, const TcMaps& wm, const TcMaps& am, const int32_t
   if (fmt == PMOE_INT4_GPTQ_G128)
     return launch_tc<true, PMOE_INT4_GPTQ_G128>(wm.gu, am.x, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, tile_n,
                                                 s);
+  if (fmt == PMOE_MXFP4)
+    return launch_tc<true, PMOE_MXFP4>(wm.gu, am.x, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, tile_n, s);
   return launch_tc<true, PMOE_BF16>(wm.gu, am.x, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, tile_n, s);
 }
 
@@ -597,6 +625,8 @@ cudaError_t tc_down(int fmt, const TcMaps& wm, const TcMaps& am, const int32_t* 
   if (fmt == PMOE_INT4_GPTQ_G128)
     return launch_tc<false, PMOE_INT4_GPTQ_G128>(wm.d, am.h, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, tile_n,
                                                  s);
+  if (fmt == PMOE_MXFP4)
+    return launch_tc<false, PMOE_MXFP4>(wm.d, am.h, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, tile_n, s);
   return launch_tc<false, PMOE_BF16>(wm.d, am.h, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, tile_n, s);
 }
 

@@ -77,14 +77,15 @@ def test_create_rejects_unsupported_formats():
     assert lib.expert_cache_create(ctypes.byref(d), ctypes.byref(h)) == pm.PMOE_EUNSUPPORTED
 
 
-def test_create_refuses_mxfp4_beyond_decode_batches():
+def test_create_refuses_mxfp4_shapes_off_the_128_grid():
     import paged_expert_moe_gb300 as pm
     lib = pm.load()
-    d = pm._lib.pmoe_cache_desc(num_experts=8, top_k=2, hidden=128, intermediate=128, num_slots=4, num_layers=1,
-                                format=pm.PMOE_MXFP4, max_tokens=16, pagein_mode=0, device=0)
-    h = ctypes.c_void_p()
-    assert lib.expert_cache_create(ctypes.byref(d), ctypes.byref(h)) == pm.PMOE_EUNSUPPORTED
-    assert not h.value
+    for hidden, inter in ((192, 128), (128, 200)):
+        d = pm._lib.pmoe_cache_desc(num_experts=8, top_k=2, hidden=hidden, intermediate=inter, num_slots=4,
+                                    num_layers=1, format=pm.PMOE_MXFP4, max_tokens=16, pagein_mode=0, device=0)
+        h = ctypes.c_void_p()
+        assert lib.expert_cache_create(ctypes.byref(d), ctypes.byref(h)) == pm.PMOE_EUNSUPPORTED
+        assert not h.value
 
 
 def test_router_argument_checks_need_no_gpu():

@@ -223,15 +223,6 @@ def test_decode_mxfp4_layer(pm, B, mode):
     _assert_bitwise_equal_to_all_resident(L, steps, ys, B, mode=mode)
 
 
-def test_mxfp4_cache_is_decode_only(pm):
-    """The prefill path has no FP4 converter: a cache that could see more than 8 tokens is
-    refused at creation."""
-    with pytest.raises(pm.PmoeError) as ei:
-        pm.ExpertCache(64, 8, 2048, 768, 24, fmt=pm.PMOE_MXFP4, max_tokens=16)
-    assert ei.value.status == pm.PMOE_EUNSUPPORTED
-    pm.ExpertCache(64, 8, 2048, 768, 24, fmt=pm.PMOE_MXFP4, max_tokens=8).close()
-
-
 @pytest.mark.parametrize("B,K", [(1, 40), (4, 26)])
 def test_decode_int4_layer(pm, B, K):
     """B=4 at K=26 exceeds K // top_k = 3: some steps run several waves. Bit for bit

@@ -46,9 +46,11 @@ def _forward(cache, x_bits, logits, k):
 
 
 @pytest.mark.parametrize("T,skew,fmt", [(300, True, 0), (9, False, 0), (64, False, 0), (1000, False, 0),
-                                        (300, True, 1), (64, False, 1), (300, True, 2), (64, False, 2)])
+                                        (300, True, 1), (64, False, 1), (300, True, 2), (64, False, 2),
+                                        (300, True, 3), (64, False, 3)])
 def test_prefill_small_layer_parity_and_bitwise_k_invariance(pm, T, skew, fmt):
-    """bf16, block-FP8 (dequantised in shared memory) and GPTQ-int4 prefill tiles."""
+    """bf16, block-FP8, GPTQ-int4 and MXFP4 prefill tiles (the quantised formats are
+    dequantised to bf16 in shared memory)."""
     E, k, H, I = 16, 4, 256, 384
     L = hz.SyntheticLayer(fmt, E, H, I, seed=200 + T)
     rng = np.random.default_rng(200 + T)
@@ -109,11 +111,13 @@ def test_gemv_and_tensor_core_paths_agree_at_the_boundary(pm):
         hz.assert_layer_close(hz.bf16_to_f64(y), L.oracle_y(x_bits, ids, w), 0)
 
 
-def test_prefill_fp8_512_tokens_k40(pm):
-    """Block-FP8 Qwen3-30B-A3B layer, 512-token prefill, K=40 (several waves): sampled tokens
-    against the oracle (rel-Frobenius 3e-2) and all outputs bit for bit against K=128."""
+@pytest.mark.parametrize("fmt", [1, 3])
+def test_prefill_quantised_512_tokens_k40(pm, fmt):
+    """Block-FP8 (rel-Frobenius 3e-2) and MXFP4 (the bf16 tolerances: E2M1 times an E8M0
+    scale is exact in bf16) Qwen3-30B-A3B layers, 512-token prefill, K=40 (several waves):
+    sampled tokens against the oracle and all outputs bit for bit against K=128."""
     E, k, H, I, T = 128, 8, 2048, 768, 512
-    L = hz.SyntheticLayer(1, E, H, I, seed=500)
+    L = hz.SyntheticLayer(fmt, E, H, I, seed=500)
     rng = np.random.default_rng(500)
     sets = gen.uniform_routing_sets(rng, T, E, k)
     x_bits, logits = hz.step_inputs(rng, sets, E, H)
@@ -130,4 +134,4 @@ def test_prefill_fp8_512_tokens_k40(pm):
     assert torch.equal(y40.view(torch.int16), y128.view(torch.int16))
     sample = np.random.default_rng(501).choice(T, size=16, replace=False)
     ids, w = orouter.router_topk(logits[sample], k)
-    hz.assert_layer_close(hz.bf16_to_f64(y40)[sample], L.oracle_y(x_bits[sample], ids, w), 1)
+    hz.assert_layer_close(hz.bf16_to_f64(y40)[sample], L.oracle_y(x_bits[sample], ids, w), fmt)
