@@ -536,8 +536,7 @@ def run_ours(args):
         elif args.section == "prefill_sweep":
             out["prefill_sweep"] = run_prefill_sweep(pm, torch, args, local, hbm_peak, tc_peak)
         elif args.section == "stack":
-            out["stack_int4"] = {f"B{B}_graph": run_stack(pm, torch, B, args.stack_steps, 3, local, mode=1, graph=True)
-                                 for B in (1, 4)}
+            out["stack_int4"] = run_stack_section(pm, torch, args, local, measure_h2d(torch, torch.device("cuda", local)))
         else:
             # the decode kernel alone on resident weights (page-in staged ahead): the launches
             # the roofline is measured on
@@ -573,6 +572,7 @@ def run_ours(args):
     sweep = None
     h2d = measure_h2d(torch, torch.device("cuda", local))
     if not args.headline_only:
+        stack = run_stack_section(pm, torch, args, local, h2d)
         others["B1_sm_pull_staged_no_graph"] = timed
         others["B1_sm_pull_in_kernel_no_graph"] = run_decode(pm, torch, store, 1, args.steps, args.warmup, local,
                                                              e2e=False, mode=1)
@@ -589,19 +589,6 @@ def run_ours(args):
         sweep = run_prefill_sweep(pm, torch, args, local, hbm_peak, tc_peak)
         fp8 = run_fp8(pm, torch, args, local, hbm_peak)
         mxfp4 = run_mxfp4(pm, torch, args, local, hbm_peak)
-        for B in (1, 4):
-            stack[f"B{B}"] = run_stack(pm, torch, B, args.stack_steps, 3, local, h2d_gbs=h2d)
-            g_run = run_stack(pm, torch, B, args.stack_steps, 3, local, mode=1, graph=True, h2d_gbs=h2d)
-            # the same steps with every expert resident (K = E): the compute alone, against
-            # which the in-kernel page-in's overlap with the weight streaming is measured
-            res_run = run_stack(pm, torch, B, args.stack_steps, 3, local, mode=1, graph=True, K=E)
-            t_link, t_res = g_run["overlap"]["link_ms_per_step"], res_run["ms_per_step"]
-            g_run["overlap"].update({"resident_only_ms_per_step": t_res,
-                                     "overlap_frac": _overlap(t_link, t_res, g_run["ms_per_step"]),
-                                     "method": "page-in inside the decode kernels: (t_link + t_resident - t_step) / "
-                                               "min(...), t_link = paged bytes / pinned H2D GB/s, t_resident = the "
-                                               "same steps with K = E (no misses)"})
-            stack[f"B{B}_graph"] = g_run
     job_ms = reduce_max(head["total_ms"], ws, torch.device("cuda", local))
     value = ws * 1 * args.steps / (job_ms / 1e3)
     if rank != 0:
@@ -738,17 +725,66 @@ def _overlap(t_a, t_b, t_step):
     return float(min(1.0, max(0.0, (t_a + t_b - t_step) / lo)))
 
 
-def run_stack(pm, torch, B, steps, warmup, device, mode=0, layers=STACK_L, K=STACK_K, graph=False, h2d_gbs=None):
-    """48-layer MoE stack, GPTQ-int4 experts, K=26 slots per layer, decode batch B, each
-    layer with its own p=0.8 reuse routing; h_{l+1} = h_l + moe_l(h_l) through
-    moe_paged_stack_forward (next layer's page-in overlapped with the current layer)."""
+def run_stack_section(pm, torch, args, local, h2d):
+    """Config 5 in both page-in modes at B=1 and B=4: SM-pull in graphs, the same steps with
+    every expert resident (the compute alone, for the overlap fraction), and copy engine."""
+    stack = {}
+    pull = make_stack_cache(pm, torch, local, mode=1)
+    runs = {B: run_stack(pm, torch, B, args.stack_steps, 3, local, graph=True, h2d_gbs=h2d, cache=pull)
+            for B in (1, 4)}
+    pull.close()
+    res = make_stack_cache(pm, torch, local, mode=1, K=E)
+    res_runs = {B: run_stack(pm, torch, B, args.stack_steps, 3, local, graph=True, cache=res) for B in (1, 4)}
+    res.close()
+    for B in (1, 4):
+        g_run, t_res = runs[B], res_runs[B]["ms_per_step"]
+        t_link = g_run["overlap"]["link_ms_per_step"]
+        g_run["overlap"].update({"resident_only_ms_per_step": t_res,
+                                 "overlap_frac": _overlap(t_link, t_res, g_run["ms_per_step"]),
+                                 "method": "page-in inside the decode kernels: (t_link + t_resident - t_step) / "
+                                           "min(...), t_link = paged bytes / pinned H2D GB/s, t_resident = the "
+                                           "same steps with K = E (no misses)"})
+        stack[f"B{B}_graph"] = g_run
+    ce = make_stack_cache(pm, torch, local, mode=0)
+    for B in (1, 4):
+        stack[f"B{B}"] = run_stack(pm, torch, B, args.stack_steps, 3, local, h2d_gbs=h2d, cache=ce)
+    ce.close()
+    return stack
+
+
+def make_stack_cache(pm, torch, device, mode=0, layers=STACK_L, K=STACK_K, max_tokens=4):
+    """One pinned 15 GB host store for every run on it (repeated pinning of 15 GB slows
+    later host-link reads on the same box). K = E: every expert of every layer paged in
+    ahead, so later steps miss nothing."""
     dev = torch.device("cuda", device)
-    cache = pm.ExpertCache(E, TOPK, H, I, K, num_layers=layers, fmt=pm.PMOE_INT4_GPTQ_G128, max_tokens=B,
+    cache = pm.ExpertCache(E, TOPK, H, I, K, num_layers=layers, fmt=pm.PMOE_INT4_GPTQ_G128, max_tokens=max_tokens,
                            device=device, pagein_mode=mode)
     for l in range(layers):
         gen.layer_store(2, H, I, E, SEED, layer=l, fast=True, out=cache.host_store(l))
-    if TOUCH_STORE and K != E:
+    if K == E:
+        n = min(E, max_tokens * TOPK)
+        for l in range(layers):
+            for e0 in range(0, E, n):
+                cache.expert_cache_prefetch(l, torch.arange(e0, min(E, e0 + n), dtype=torch.int32, device=dev))
+        torch.cuda.synchronize(dev)
+    elif TOUCH_STORE:
         touch_store(torch, cache, layers, dev)
+    return cache
+
+
+def run_stack(pm, torch, B, steps, warmup, device, mode=0, layers=STACK_L, K=STACK_K, graph=False, h2d_gbs=None,
+              cache=None):
+    """48-layer MoE stack, GPTQ-int4 experts, K=26 slots per layer, decode batch B, each
+    layer with its own p=0.8 reuse routing; h_{l+1} = h_l + moe_l(h_l) through
+    moe_paged_stack_forward (next layer's page-in overlapped with the current layer).
+    A run on a K < E cache empties its tables first (each run starts cold)."""
+    dev = torch.device("cuda", device)
+    own = cache is None
+    if own:
+        cache = make_stack_cache(pm, torch, device, mode, layers, K, max_tokens=B)
+    elif cache.K != E:
+        cache.expert_cache_reset(-1)
+    mode, K, layers = (1 if cache.desc.pagein_mode else 0), cache.K, cache.layers
     rng = np.random.default_rng([SEED, 48, B])
     traces = [gen.reuse_routing_trace(rng, E, TOPK, B, TRACE_STEPS) for _ in range(layers)]
     n_inputs = min(TRACE_STEPS, warmup + steps)
@@ -763,14 +799,6 @@ def run_stack(pm, torch, B, steps, warmup, device, mode=0, layers=STACK_L, K=STA
     work = torch.empty((B, H), dtype=torch.bfloat16, device=dev)
     flush = L2Flush(dev)
     stream = torch.cuda.current_stream(dev)
-    if K == E:
-        # every expert of every layer paged in ahead (prefetch steps of at most B*top_k ids);
-        # with K = E nothing is evicted afterwards, so the timed steps miss nothing
-        n = min(E, B * TOPK)
-        for l in range(layers):
-            for e0 in range(0, E, n):
-                cache.expert_cache_prefetch(l, torch.arange(e0, min(E, e0 + n), dtype=torch.int32, device=dev))
-        torch.cuda.synchronize(dev)
 
     if graph:
         x_s = torch.empty((B, H), dtype=torch.bfloat16, device=dev)
@@ -808,7 +836,9 @@ def run_stack(pm, torch, B, steps, warmup, device, mode=0, layers=STACK_L, K=STA
     total_ms = float(sum(a.elapsed_time(b) for a, b in evs))
     kt = cache.expert_cache_kernel_times()
     s1 = cache.expert_cache_stats(-1)
-    cache.close()
+    cache.expert_cache_set_timing(False)
+    if own:
+        cache.close()
     nb = pm.pmoe_expert_bytes(pm.PMOE_INT4_GPTQ_G128, H, I)
     wbytes = sum(distinct[si] for si in ids_used) * nb
     dec_ms = kt["decode"]["ms"]

@@ -415,10 +415,12 @@ __global__ void __launch_bounds__(kDfThreads, 1) decode_fused_kernel(const DfArg
     static_assert(kDfLag == 3, "the entry-time slot reads below cover the first three experts");
     const int sl0 = a.plan[L.wave_slot()], sl1 = a.E > 1 ? a.plan[L.wave_slot() + 1] : -1;
     const int sl2 = a.E > 2 ? a.plan[L.wave_slot() + 2] : -1;
+    const int hits0 = a.plan[L.wave_hits() + a.wave];  // the wave's experts resident before this launch
     const int D0 = ws1 - ws0;
     // (not when this launch pages experts in: the block barrier below would hold the
     // pager warps back while the producer issues, and the host link is the longer path)
-    if (a.pull == 0 && a.wave < nw && ws0 == 0 && a.sub == 0 && D0 > 0 && D0 * (a.cg + a.cd) <= kDfMaxChunks) {
+    if ((a.pull == 0 || hits0 >= D0) && a.wave < nw && ws0 == 0 && a.sub == 0 && D0 > 0 &&
+        D0 * (a.cg + a.cd) <= kDfMaxChunks) {
       const int nh = D0;  // (no page-in: every wave expert is resident)
       const DfSched sc0{D0, (int)gridDim.x, (int)blockIdx.x, a.I, a.H, a.cg, a.cd};
       const size_t rbg0 = (size_t)a.H * Fmt<FMT>::BPE2 / 2;

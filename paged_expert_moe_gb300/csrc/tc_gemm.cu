@@ -146,24 +146,38 @@ __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.
 // (lanes 64-127), so one M=128 MMA feeds both halves of SiLU*mul.
 template <int FMT, int NMAX>
 struct TcCfg {
+  static constexpr bool kQuant = FMT != PMOE_BF16;
   static constexpr int kABytes = 128 * kBK * 2;            // bf16 A tile (MMA operand)
   static constexpr int kBBytes = NMAX * kBK * 2;           // bf16 B tile (up to NMAX pairs)
   // quantised A tile as loaded by TMA, before the converter warps dequantise it
   static constexpr int kQBytes = FMT == PMOE_FP8_BLOCK128                           ? 128 * kBK
                                  : (FMT == PMOE_INT4_GPTQ_G128 || FMT == PMOE_MXFP4) ? 128 * kBK / 2
                                                                                      : 0;
-  static constexpr int kStageBytes = kABytes + kBBytes + kQBytes;
   static constexpr int kStagingFloats = 128 * 17;
   // quantised formats: each converter thread's row of scales (<= 16 words per row), padded
-  static constexpr int kScaleWords = FMT == PMOE_BF16 ? 0 : 128 * 17;
-  static constexpr int kFixedBytes = kStagingFloats * 4 + kScaleWords * 4 + 1024 + 512;
-  static constexpr int kStagesFit = (220 * 1024 - kFixedBytes) / kStageBytes;
-  static constexpr int kStages = kStagesFit < 8 ? kStagesFit : 8;
+  static constexpr int kScaleWords = kQuant ? 128 * 17 : 0;
+  static constexpr int kFixedBytes = kStagingFloats * 4 + kScaleWords * 4 + 1024 + 1024;
+  static constexpr int kBudget = 220 * 1024 - kFixedBytes;
+  // bf16: stages of (A + B) as deep as fit, at most 8
+  static constexpr int kStagesFit = kBudget / (kABytes + kBBytes);
+  static constexpr int kStages = kQuant ? 0 : (kStagesFit < 8 ? kStagesFit : 8);
+  // quantised: three rings. The raw weight tiles stream from HBM and set the pace, so
+  // they get most of the memory (deep: many tiles in flight); the converted bf16 A tiles
+  // only bridge the converters and the MMAs (shallow); the activation tiles (B) sit in
+  // between.
+  static constexpr int kAStages = kQuant ? (NMAX > 64 ? 2 : 3) : 0;
+  static constexpr int kBStages = kQuant ? (NMAX > 64 ? 3 : 6) : 0;
+  static constexpr int kQFit = kQuant ? (kBudget - kAStages * kABytes - kBStages * kBBytes) / kQBytes : 0;
+  static constexpr int kQStages = kQFit < 24 ? kQFit : 24;
+  static constexpr int kRingBytes =
+      kQuant ? kAStages * kABytes + kBStages * kBBytes + kQStages * kQBytes : kStages * (kABytes + kBBytes);
   static constexpr int kAccCols = 256;   // one accumulator buffer (N <= 256 fp32 columns)
   static constexpr int kTmemCols = 512;  // two buffers: the epilogue of tile i overlaps the MMAs of tile i+1
-  static constexpr int kSmemBytes = kStages * kStageBytes + kFixedBytes;
-  static constexpr int kThreads = FMT == PMOE_BF16 ? 192 : 320;  // + 4 converter warps
-  static_assert(kStages >= 2 && kSmemBytes <= 227 * 1024, "shared memory");
+  static constexpr int kSmemBytes = kRingBytes + kFixedBytes;
+  // + 4 converter warps and a second producer warp (activation tiles)
+  static constexpr int kThreads = kQuant ? 352 : 192;
+  static_assert((kQuant ? (kAStages >= 2 && kQStages >= 4) : kStages >= 2) && kSmemBytes <= 227 * 1024,
+                "shared memory");
 };
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
@@ -190,17 +204,30 @@ __global__ void __launch_bounds__(TcCfg<FMT, NMAX>::kThreads, 1)
                       const int32_t* __restrict__ plan, int E, int wave, int sub, Workspace ws, int I, int H,
                       const uint8_t* __restrict__ arena, size_t stride, ExpertLayout lay, int32_t* __restrict__ err) {
   using C = TcCfg<FMT, NMAX>;
-  constexpr bool kQuant = FMT != PMOE_BF16;
+  constexpr bool kQuant = C::kQuant;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  float* staging = reinterpret_cast<float*>(smem + C::kStages * C::kStageBytes);
+  // bf16: smem = kStages x (A | B). Quantised: A ring, then B ring, then Q ring.
+  uint8_t* aring = smem;
+  uint8_t* bring = aring + C::kAStages * C::kABytes;
+  uint8_t* qring = bring + C::kBStages * C::kBBytes;
+  float* staging = reinterpret_cast<float*>(smem + C::kRingBytes);
   uint32_t* scale_cache = reinterpret_cast<uint32_t*>(staging + C::kStagingFloats);
-  uint64_t* full = reinterpret_cast<uint64_t*>(scale_cache + C::kScaleWords);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(scale_cache + C::kScaleWords);
+  // bf16 stages
+  uint64_t* full = bars;
   uint64_t* empty = full + C::kStages;
-  uint64_t* acc_full = empty + C::kStages;  // [2]
-  uint64_t* acc_empty = acc_full + 2;       // [2]
-  uint64_t* conv = acc_empty + 2;           // [kStages] quantised A converted (kQuant only)
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(conv + C::kStages);
+  // quantised rings: raw tile landed / read by the converters; B tile landed / used by
+  // the MMAs; converted A tile written / used by the MMAs
+  uint64_t* qfull = empty + C::kStages;
+  uint64_t* qempty = qfull + C::kQStages;
+  uint64_t* bfull = qempty + C::kQStages;
+  uint64_t* bempty = bfull + C::kBStages;
+  uint64_t* afull = bempty + C::kBStages;
+  uint64_t* aempty = afull + C::kAStages;
+  uint64_t* acc_full = aempty + C::kAStages;  // [2]
+  uint64_t* acc_empty = acc_full + 2;         // [2]
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acc_empty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -219,12 +246,22 @@ __global__ void __launch_bounds__(TcCfg<FMT, NMAX>::kThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
+    for (int s = 0; s < C::kQStages; ++s) {
+      mbar_init(&qfull[s], 1);
+      mbar_init(&qempty[s], 128);
+    }
+    for (int s = 0; s < C::kBStages; ++s) {
+      mbar_init(&bfull[s], 1);
+      mbar_init(&bempty[s], 1);
+    }
+    for (int s = 0; s < C::kAStages; ++s) {
+      mbar_init(&afull[s], 128);
+      mbar_init(&aempty[s], 1);
+    }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
       mbar_init(&acc_empty[b], 128);
     }
-    if (kQuant)
-      for (int s = 0; s < C::kStages; ++s) mbar_init(&conv[s], 128);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     prefetch_map(&map_w);
@@ -241,9 +278,9 @@ __global__ void __launch_bounds__(TcCfg<FMT, NMAX>::kThreads, 1)
   fence_after();
   const uint32_t tmem = *tmem_holder;
 
-  if (warp == 0) {
+  if (warp == 0 && !kQuant) {
     if (lane == 0) {
-      // ---------------- TMA producer
+      // ---------------- TMA producer (bf16): A and B tiles of one stage
       int s = 0;
       uint32_t ph = 0;
       bool ok = true;
@@ -251,26 +288,16 @@ __global__ void __launch_bounds__(TcCfg<FMT, NMAX>::kThreads, 1)
         const int tile = t0 + item / m_tiles, mt = item % m_tiles;
         const int slot = ws.tiles[3 * tile + 0], pstart = ws.tiles[3 * tile + 1], np = ws.tiles[3 * tile + 2];
         const int nb = (np + kTileRowsB - 1) / kTileRowsB;
-        const uint32_t bytes = (kQuant ? C::kQBytes : C::kABytes) + nb * kTileRowsB * kBK * 2;
+        const uint32_t bytes = C::kABytes + nb * kTileRowsB * kBK * 2;
         for (int kb = 0; kb < n_kb; ++kb) {
           if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, err)) {
             ok = false;
             break;
           }
-          uint8_t* st = smem + s * C::kStageBytes;
+          uint8_t* st = smem + s * (C::kABytes + C::kBBytes);
           mbar_arrive_expect_tx(&full[s], bytes);
-          if (kQuant) {
-            // quantised rows land in the stage's staging area (row-major, unswizzled)
-            uint8_t* q = st + C::kABytes + C::kBBytes;
-            const int kc = FMT == PMOE_FP8_BLOCK128 ? kb * kBK : kb * kBK / 2;  // bytes along K
-            if (GATEUP) {
-              tma_load_3d(q, &map_w, &full[s], kc, mt * 64, slot);
-              tma_load_3d(q + C::kQBytes / 2, &map_w, &full[s], kc, I + mt * 64, slot);
-            } else {
-              tma_load_3d(q, &map_w, &full[s], kc, mt * 128, slot);
-            }
-          } else if (GATEUP) {
-            tma_load_3d(st, &map_w, &full[s], kb * kBK, mt * 64, slot);                 // gate rows
+          if (GATEUP) {
+            tma_load_3d(st, &map_w, &full[s], kb * kBK, mt * 64, slot);                      // gate rows
             tma_load_3d(st + C::kABytes / 2, &map_w, &full[s], kb * kBK, I + mt * 64, slot);  // up rows
           } else {
             tma_load_3d(st, &map_w, &full[s], kb * kBK, mt * 128, slot);
@@ -293,11 +320,81 @@ __global__ void __launch_bounds__(TcCfg<FMT, NMAX>::kThreads, 1)
         }
       }
     }
+  } else if (warp == 0 && kQuant) {
+    if (lane == 0) {
+      // ---------------- TMA producer of the raw weight tiles (quantised formats)
+      int q = 0;
+      uint32_t qph = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+        const int tile = t0 + item / m_tiles, mt = item % m_tiles;
+        const int slot = ws.tiles[3 * tile + 0];
+        for (int kb = 0; kb < n_kb; ++kb) {
+          if (!mbar_wait(&qempty[q], qph ^ 1u, abort_flag, err)) {
+            ok = false;
+            break;
+          }
+          uint8_t* dst = qring + q * C::kQBytes;
+          mbar_arrive_expect_tx(&qfull[q], C::kQBytes);
+          const int kc = FMT == PMOE_FP8_BLOCK128 ? kb * kBK : kb * kBK / 2;  // bytes along K
+          if (GATEUP) {
+            tma_load_3d(dst, &map_w, &qfull[q], kc, mt * 64, slot);
+            tma_load_3d(dst + C::kQBytes / 2, &map_w, &qfull[q], kc, I + mt * 64, slot);
+          } else {
+            tma_load_3d(dst, &map_w, &qfull[q], kc, mt * 128, slot);
+          }
+          if (++q == C::kQStages) {
+            q = 0;
+            qph ^= 1u;
+          }
+        }
+      }
+      for (int i = 0; i < C::kQStages; ++i) {  // drain: every raw tile read by the converters
+        mbar_wait(&qempty[q], qph ^ 1u, abort_flag, err);
+        if (++q == C::kQStages) {
+          q = 0;
+          qph ^= 1u;
+        }
+      }
+    }
+  } else if (kQuant && warp == 10) {
+    if (lane == 0) {
+      // ---------------- TMA producer of the activation tiles (quantised formats)
+      int b = 0;
+      uint32_t bph = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+        const int tile = t0 + item / m_tiles;
+        const int pstart = ws.tiles[3 * tile + 1], np = ws.tiles[3 * tile + 2];
+        const int nb = (np + kTileRowsB - 1) / kTileRowsB;
+        for (int kb = 0; kb < n_kb; ++kb) {
+          if (!mbar_wait(&bempty[b], bph ^ 1u, abort_flag, err)) {
+            ok = false;
+            break;
+          }
+          uint8_t* bst = bring + b * C::kBBytes;
+          mbar_arrive_expect_tx(&bfull[b], (uint32_t)(nb * kTileRowsB * kBK * 2));
+          for (int t = 0; t < nb; ++t)
+            tma_load_2d(bst + t * kTileRowsB * kBK * 2, &map_b, &bfull[b], kb * kBK, pstart + t * kTileRowsB);
+          if (++b == C::kBStages) {
+            b = 0;
+            bph ^= 1u;
+          }
+        }
+      }
+      for (int i = 0; i < C::kBStages; ++i) {  // drain: every B tile used by its MMAs
+        mbar_wait(&bempty[b], bph ^ 1u, abort_flag, err);
+        if (++b == C::kBStages) {
+          b = 0;
+          bph ^= 1u;
+        }
+      }
+    }
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------- MMA issuer
-      int s = 0;
-      uint32_t ph = 0;
+      int s = 0, qb = 0;
+      uint32_t ph = 0, qbph = 0;
       bool ok = true;
       int it = 0;
       for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++it) {
@@ -312,21 +409,45 @@ __global__ void __launch_bounds__(TcCfg<FMT, NMAX>::kThreads, 1)
         }
         const uint32_t d = tmem + (uint32_t)(ab * C::kAccCols);
         for (int kb = 0; kb < n_kb; ++kb) {
-          if (!mbar_wait(kQuant ? &conv[s] : &full[s], ph, abort_flag, err)) {
-            ok = false;
-            break;
+          uint32_t a0, bb;
+          if constexpr (kQuant) {
+            // s / ph walk the A ring, qb / qbph the B ring
+            if (!mbar_wait(&afull[s], ph, abort_flag, err) || !mbar_wait(&bfull[qb], qbph, abort_flag, err)) {
+              ok = false;
+              break;
+            }
+            a0 = smem_u32(aring + s * C::kABytes);
+            bb = smem_u32(bring + qb * C::kBBytes);
+          } else {
+            if (!mbar_wait(&full[s], ph, abort_flag, err)) {
+              ok = false;
+              break;
+            }
+            const uint8_t* st = smem + s * (C::kABytes + C::kBBytes);
+            a0 = smem_u32(st);
+            bb = smem_u32(st + C::kABytes);
           }
           fence_after();
-          const uint8_t* st = smem + s * C::kStageBytes;
-          const uint32_t a0 = smem_u32(st);
-          const uint32_t bb = smem_u32(st + C::kABytes);
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk)
             mma_bf16(d, sw128_desc(a0 + kk * 32), sw128_desc(bb + kk * 32), idesc, (kb > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(&empty[s]);
-          if (++s == C::kStages) {
-            s = 0;
-            ph ^= 1u;
+          if constexpr (kQuant) {
+            mma_commit(&aempty[s]);
+            mma_commit(&bempty[qb]);
+            if (++qb == C::kBStages) {
+              qb = 0;
+              qbph ^= 1u;
+            }
+            if (++s == C::kAStages) {
+              s = 0;
+              ph ^= 1u;
+            }
+          } else {
+            mma_commit(&empty[s]);
+            if (++s == C::kStages) {
+              s = 0;
+              ph ^= 1u;
+            }
           }
         }
         if (ok) mma_commit(&acc_full[ab]);
@@ -339,8 +460,8 @@ __global__ void __launch_bounds__(TcCfg<FMT, NMAX>::kThreads, 1)
     // value times 2^(X - 127) of its block of 32, exact in bf16) to bf16 and written in
     // the 128-byte-swizzled K-major layout TMA would have produced.
     const int r = threadIdx.x - 192;
-    int s = 0;
-    uint32_t ph = 0;
+    int q = 0, s = 0;  // raw tile (Q ring) and converted tile (A ring) of the current step
+    uint32_t qph = 0, ph = 0;
     bool ok = true;
     for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
       const int tile = t0 + item / m_tiles, mt = item % m_tiles;
@@ -360,18 +481,18 @@ __global__ void __launch_bounds__(TcCfg<FMT, NMAX>::kThreads, 1)
       if (cached)
         for (int j = 0; j < nblk; ++j) my_sc[j] = __ldg(srow + j);
       for (int kb = 0; kb < n_kb; ++kb) {
-        if (!mbar_wait(&full[s], ph, abort_flag, err)) {
+        if (!mbar_wait(&qfull[q], qph, abort_flag, err) || !mbar_wait(&aempty[s], ph ^ 1u, abort_flag, err)) {
           ok = false;
           break;
         }
-        uint8_t* st = smem + s * C::kStageBytes;
-        uint4* arow = reinterpret_cast<uint4*>(st + r * 128);
+        const uint8_t* qt = qring + q * C::kQBytes;  // row r at qt + r * (kQBytes / 128)
+        uint4* arow = reinterpret_cast<uint4*>(aring + s * C::kABytes + r * 128);
         if (FMT == PMOE_FP8_BLOCK128) {
-          const uint8_t* q = st + C::kABytes + C::kBBytes + r * kBK;
+          const uint8_t* qr = qt + r * kBK;
           const float sv = __uint_as_float(cached ? my_sc[(kb * kBK) >> 7] : __ldg(srow + ((kb * kBK) >> 7)));
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
-            const uint2 v = *reinterpret_cast<const uint2*>(q + c * 8);
+            const uint2 v = *reinterpret_cast<const uint2*>(qr + c * 8);
             const uint32_t wv[2] = {v.x, v.y};
             uint32_t out[4];
 #pragma unroll
@@ -389,12 +510,12 @@ __global__ void __launch_bounds__(TcCfg<FMT, NMAX>::kThreads, 1)
           }
         } else if (FMT == PMOE_MXFP4) {
           // 64 codes = two blocks of 32, each with its own E8M0 byte
-          const uint8_t* q = st + C::kABytes + C::kBBytes + r * (kBK / 2);
+          const uint8_t* qr = qt + r * (kBK / 2);
           const uint32_t xw = cached ? my_sc[(kb * kBK) >> 7] : __ldg(srow + ((kb * kBK) >> 7));
           const int xb = ((kb * kBK) >> 5) & 3;  // first of the stage's two scale bytes in the word
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
-            const uint32_t word = *reinterpret_cast<const uint32_t*>(q + c * 4);  // 8 codes, low nibble first
+            const uint32_t word = *reinterpret_cast<const uint32_t*>(qr + c * 4);  // 8 codes, low nibble first
             const uint32_t xbyte = (xw >> (8 * (xb + (c >> 2)))) & 0xffu;
             const float sv = xbyte ? __uint_as_float(xbyte << 23) : __uint_as_float(0x00400000u);
             uint32_t out[4];
@@ -409,12 +530,12 @@ __global__ void __launch_bounds__(TcCfg<FMT, NMAX>::kThreads, 1)
             arow[c ^ (r & 7)] = make_uint4(out[0], out[1], out[2], out[3]);
           }
         } else {
-          const uint8_t* q = st + C::kABytes + C::kBBytes + r * (kBK / 2);
+          const uint8_t* qr = qt + r * (kBK / 2);
           const uint32_t szw = cached ? my_sc[(kb * kBK) >> 7] : __ldg(srow + ((kb * kBK) >> 7));
           const float2 sz = __half22float2(*reinterpret_cast<const __half2*>(&szw));
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
-            const uint32_t word = *reinterpret_cast<const uint32_t*>(q + c * 4);  // 8 nibbles, low first
+            const uint32_t word = *reinterpret_cast<const uint32_t*>(qr + c * 4);  // 8 nibbles, low first
             uint32_t out[4];
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
@@ -427,8 +548,13 @@ __global__ void __launch_bounds__(TcCfg<FMT, NMAX>::kThreads, 1)
           }
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        mbar_arrive(&conv[s]);
-        if (++s == C::kStages) {
+        mbar_arrive(&afull[s]);
+        mbar_arrive(&qempty[q]);
+        if (++q == C::kQStages) {
+          q = 0;
+          qph ^= 1u;
+        }
+        if (++s == C::kAStages) {
           s = 0;
           ph ^= 1u;
         }
