@@ -18,7 +18,11 @@
 // N = the tile's pair count rounded up to 16 (<= 256): the instruction descriptor is
 // built per tile, so no MMA work is spent on other experts' pairs beyond that.
 // Warp roles: warp 0 lane 0 issues TMA, warp 1 lane 0 issues tcgen05.mma (warp 1 owns
-// the TMEM allocation), warps 2-5 drain TMEM (32 lanes each) in the epilogue.
+// the TMEM allocation), warps 2-5 drain TMEM (32 lanes each) in the epilogue. Quantised
+// weights: warp 0 streams the raw weight tiles into a deep ring of their own, warp 14
+// the activation tiles, and converter warps 6-13 dequantise each raw tile into a shallow
+// ring of bf16 operand tiles (the raw bytes, not the operand tiles, are what must be in
+// flight from HBM).
 // Every mbarrier wait is bounded; on expiry the CTA records kErrTcTimeout, stops,
 // waits (bounded) for its copies in flight, frees its TMEM and returns.
 #include "tc_gemm.h"
@@ -154,8 +158,8 @@ struct TcCfg {
                                  : (FMT == PMOE_INT4_GPTQ_G128 || FMT == PMOE_MXFP4) ? 128 * kBK / 2
                                                                                      : 0;
   static constexpr int kStagingFloats = 128 * 17;
-  // quantised formats: each converter thread's row of scales (<= 16 words per row), padded
-  static constexpr int kScaleWords = kQuant ? 128 * 17 : 0;
+  // quantised formats: each converter thread's copy of its row's scales (<= 16 words), padded
+  static constexpr int kScaleWords = kQuant ? 256 * 17 : 0;
   static constexpr int kFixedBytes = kStagingFloats * 4 + kScaleWords * 4 + 1024 + 1024;
   static constexpr int kBudget = 220 * 1024 - kFixedBytes;
   // bf16: stages of (A + B) as deep as fit, at most 8
@@ -174,8 +178,8 @@ struct TcCfg {
   static constexpr int kAccCols = 256;   // one accumulator buffer (N <= 256 fp32 columns)
   static constexpr int kTmemCols = 512;  // two buffers: the epilogue of tile i overlaps the MMAs of tile i+1
   static constexpr int kSmemBytes = kRingBytes + kFixedBytes;
-  // + 4 converter warps and a second producer warp (activation tiles)
-  static constexpr int kThreads = kQuant ? 352 : 192;
+  // + 8 converter warps (two threads per A-tile row) and a second producer warp (activation tiles)
+  static constexpr int kThreads = kQuant ? 480 : 192;
   static_assert((kQuant ? (kAStages >= 2 && kQStages >= 4) : kStages >= 2) && kSmemBytes <= 227 * 1024,
                 "shared memory");
 };
@@ -248,14 +252,14 @@ __global__ void __launch_bounds__(TcCfg<FMT, NMAX>::kThreads, 1)
     }
     for (int s = 0; s < C::kQStages; ++s) {
       mbar_init(&qfull[s], 1);
-      mbar_init(&qempty[s], 128);
+      mbar_init(&qempty[s], 256);
     }
     for (int s = 0; s < C::kBStages; ++s) {
       mbar_init(&bfull[s], 1);
       mbar_init(&bempty[s], 1);
     }
     for (int s = 0; s < C::kAStages; ++s) {
-      mbar_init(&afull[s], 128);
+      mbar_init(&afull[s], 256);
       mbar_init(&aempty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -357,7 +361,7 @@ __global__ void __launch_bounds__(TcCfg<FMT, NMAX>::kThreads, 1)
         }
       }
     }
-  } else if (kQuant && warp == 10) {
+  } else if (kQuant && warp == 14) {
     if (lane == 0) {
       // ---------------- TMA producer of the activation tiles (quantised formats)
       int b = 0;
@@ -453,13 +457,14 @@ __global__ void __launch_bounds__(TcCfg<FMT, NMAX>::kThreads, 1)
         if (ok) mma_commit(&acc_full[ab]);
       }
     }
-  } else if (kQuant && warp >= 6) {
-    // ---------------- converters: warps 6..9, thread r owns row r of the A tile. Each
+  } else if (kQuant && warp >= 6 && warp <= 13) {
+    // ---------------- converters: warps 6..13, two threads per row of the A tile (thread
+    // ct owns row ct % 128, K half ct / 128 of each stage). Each
     // quantised row (64 K values) is dequantised with its scale (block-FP8: the fp32
     // scale of its 128x128 block; int4: (q - z) * s of its group of 128; MXFP4: the E2M1
     // value times 2^(X - 127) of its block of 32, exact in bf16) to bf16 and written in
     // the 128-byte-swizzled K-major layout TMA would have produced.
-    const int r = threadIdx.x - 192;
+    const int ct = threadIdx.x - 192, r = ct & 127, hf = ct >> 7;
     int q = 0, s = 0;  // raw tile (Q ring) and converted tile (A ring) of the current step
     uint32_t qph = 0, ph = 0;
     bool ok = true;
@@ -476,7 +481,7 @@ __global__ void __launch_bounds__(TcCfg<FMT, NMAX>::kThreads, 1)
       const int nblk = cols >> 7;
       const uint32_t* srow = reinterpret_cast<const uint32_t*>(sc) +
                              (FMT == PMOE_FP8_BLOCK128 ? (size_t)(grow >> 7) * nblk : (size_t)grow * nblk);
-      uint32_t* my_sc = scale_cache + r * 17;
+      uint32_t* my_sc = scale_cache + ct * 17;
       const bool cached = nblk <= 16;
       if (cached)
         for (int j = 0; j < nblk; ++j) my_sc[j] = __ldg(srow + j);
@@ -491,7 +496,7 @@ __global__ void __launch_bounds__(TcCfg<FMT, NMAX>::kThreads, 1)
           const uint8_t* qr = qt + r * kBK;
           const float sv = __uint_as_float(cached ? my_sc[(kb * kBK) >> 7] : __ldg(srow + ((kb * kBK) >> 7)));
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
+          for (int c = 4 * hf; c < 4 * hf + 4; ++c) {
             const uint2 v = *reinterpret_cast<const uint2*>(qr + c * 8);
             const uint32_t wv[2] = {v.x, v.y};
             uint32_t out[4];
@@ -514,7 +519,7 @@ __global__ void __launch_bounds__(TcCfg<FMT, NMAX>::kThreads, 1)
           const uint32_t xw = cached ? my_sc[(kb * kBK) >> 7] : __ldg(srow + ((kb * kBK) >> 7));
           const int xb = ((kb * kBK) >> 5) & 3;  // first of the stage's two scale bytes in the word
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
+          for (int c = 4 * hf; c < 4 * hf + 4; ++c) {
             const uint32_t word = *reinterpret_cast<const uint32_t*>(qr + c * 4);  // 8 codes, low nibble first
             const uint32_t xbyte = (xw >> (8 * (xb + (c >> 2)))) & 0xffu;
             const float sv = xbyte ? __uint_as_float(xbyte << 23) : __uint_as_float(0x00400000u);
@@ -534,7 +539,7 @@ __global__ void __launch_bounds__(TcCfg<FMT, NMAX>::kThreads, 1)
           const uint32_t szw = cached ? my_sc[(kb * kBK) >> 7] : __ldg(srow + ((kb * kBK) >> 7));
           const float2 sz = __half22float2(*reinterpret_cast<const __half2*>(&szw));
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
+          for (int c = 4 * hf; c < 4 * hf + 4; ++c) {
             const uint32_t word = *reinterpret_cast<const uint32_t*>(qr + c * 4);  // 8 nibbles, low first
             uint32_t out[4];
 #pragma unroll
