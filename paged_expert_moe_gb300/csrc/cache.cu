@@ -28,8 +28,6 @@
 #include <thread>
 #include <vector>
 
-#include <sys/mman.h>
-
 using namespace pmoe;
 
 namespace {
@@ -117,9 +115,6 @@ struct pmoe_cache {
   cudaStream_t copy_stream = nullptr;
   cudaStream_t plan_stream = nullptr;  // residency kernels + plan read-back (copy-engine mode)
   std::vector<uint8_t*> host_store, host_store_dev, arena;
-  // host_map[l]: the anonymous mapping the layer's store was registered from (base, bytes),
-  // or {nullptr, 0} when the store came from cudaHostAlloc
-  std::vector<std::pair<void*, size_t>> host_map;
   std::vector<LayerState> st;
   std::vector<int32_t*> plan_dev;
   int32_t* plan_host = nullptr;
@@ -213,15 +208,8 @@ void free_cache(pmoe_cache* c) {
   resolve_marks(c);
   for (cudaEvent_t e : c->pool)
     if (e) cudaEventDestroy(e);
-  for (size_t l = 0; l < c->host_store.size(); ++l) {
-    if (c->host_store[l] == nullptr) continue;
-    if (l < c->host_map.size() && c->host_map[l].first != nullptr) {
-      cudaHostUnregister(c->host_store[l]);
-      munmap(c->host_map[l].first, c->host_map[l].second);
-    } else {
-      cudaFreeHost(c->host_store[l]);
-    }
-  }
+  for (auto p : c->host_store)
+    if (p) cudaFreeHost(p);
   for (auto p : c->arena)
     if (p) cudaFree(p);
   if (c->plan_host) cudaFreeHost(c->plan_host);
@@ -367,7 +355,6 @@ int expert_cache_create(const pmoe_cache_desc* desc, pmoe_cache** out) {
   c->words = PlanLayout{d.num_experts}.words();
   const int E = d.num_experts, K = d.num_slots, Lr = d.num_layers;
   c->host_store.assign(Lr, nullptr);
-  c->host_map.assign(Lr, {nullptr, 0});
   c->host_store_dev.assign(Lr, nullptr);
   c->arena.assign(Lr, nullptr);
   c->st.resize(Lr);
@@ -407,37 +394,12 @@ int expert_cache_create(const pmoe_cache_desc* desc, pmoe_cache** out) {
       goto fail;
     }
     void* p = nullptr;
-    const size_t bytes = (size_t)E * c->stride;
-    // Preferred: an anonymous mapping with transparent huge pages requested, pinned and
-    // mapped for the device. The SM-pull page-in reads the store through the device's
-    // address translation; huge pages keep that translation to a few entries per layer,
-    // where a store pinned from small pages (what pinned allocations tend to get once a
-    // host's memory is fragmented) makes first reads of each page slow. The mapping is
-    // aligned to 512 MiB, the largest transparent huge page size (64 KiB base pages).
-    {
-      const size_t align = size_t(512) << 20;
-      void* raw = mmap(nullptr, bytes + align, PROT_READ | PROT_WRITE, MAP_PRIVATE | MAP_ANONYMOUS | MAP_NORESERVE,
-                       -1, 0);
-      if (raw != MAP_FAILED) {
-        uint8_t* al = (uint8_t*)(((uintptr_t)raw + align - 1) & ~(uintptr_t)(align - 1));
-        madvise(al, bytes, MADV_HUGEPAGE);
-        if (cudaHostRegister(al, bytes, cudaHostRegisterMapped | cudaHostRegisterPortable) == cudaSuccess) {
-          p = al;
-          c->host_map[l] = {raw, bytes + align};
-        } else {
-          cudaGetLastError();
-          munmap(raw, bytes + align);
-        }
-      }
-    }
-    if (p == nullptr) {
-      const cudaError_t e = cudaHostAlloc(&p, bytes, cudaHostAllocMapped | cudaHostAllocPortable);
-      if (e != cudaSuccess) {
-        set_cuda_error(e, "cudaHostAlloc (expert store)");
-        cudaGetLastError();
-        status = PMOE_EHOSTALLOC;
-        goto fail;
-      }
+    const cudaError_t e = cudaHostAlloc(&p, (size_t)E * c->stride, cudaHostAllocMapped | cudaHostAllocPortable);
+    if (e != cudaSuccess) {
+      set_cuda_error(e, "cudaHostAlloc (expert store)");
+      cudaGetLastError();
+      status = PMOE_EHOSTALLOC;
+      goto fail;
     }
     c->host_store[l] = (uint8_t*)p;
     void* pd = nullptr;
