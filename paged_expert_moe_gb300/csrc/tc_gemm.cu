@@ -169,7 +169,7 @@ struct TcCfg {
   // they get most of the memory (deep: many tiles in flight); the converted bf16 A tiles
   // only bridge the converters and the MMAs (shallow); the activation tiles (B) sit in
   // between.
-  static constexpr int kAStages = kQuant ? (NMAX > 64 ? 2 : 3) : 0;
+  static constexpr int kAStages = kQuant ? (NMAX > 64 ? 3 : 5) : 0;
   static constexpr int kBStages = kQuant ? (NMAX > 64 ? 3 : 6) : 0;
   static constexpr int kQFit = kQuant ? (kBudget - kAStages * kABytes - kBStages * kBBytes) / kQBytes : 0;
   static constexpr int kQStages = kQFit < 24 ? kQFit : 24;
