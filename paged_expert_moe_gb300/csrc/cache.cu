@@ -125,6 +125,8 @@ struct pmoe_cache {
   std::vector<cudaEvent_t> ev_plan, ev_layer_done, ev_ready;
   std::vector<int> staged, staged_waves, layer_used;
   std::vector<int> pull_deferred;  // the staged step's wave-0 page-in is left to the fused decode kernel
+  std::vector<int> plan_on_compute;  // the staged step was planned on the compute stream
+  bool pdl = false;  // cooperative launches with programmatic serialization are accepted
   cudaEvent_t ev_ids = nullptr, ev_wave_done = nullptr, ev_stack = nullptr;
   Workspace ws{};
   void* ws_buf = nullptr;
@@ -252,6 +254,9 @@ int issue_copies(pmoe_cache* c, int layer, int wave) {
 int flush_staged(pmoe_cache* c, int layer) {
   if (!c->staged[layer]) return PMOE_OK;
   c->staged[layer] = 0;
+  // (a step planned on a compute stream is always consumed by the forward that planned
+  // it, so it never reaches here)
+  c->plan_on_compute[layer] = 0;
   const int first = c->pull_deferred[layer] ? 0 : 1;
   c->pull_deferred[layer] = 0;
   for (int wv = first; wv < c->staged_waves[layer]; ++wv) {
@@ -349,6 +354,7 @@ int expert_cache_create(const pmoe_cache_desc* desc, pmoe_cache** out) {
   if (c == nullptr) return PMOE_ENOMEM;
   c->d = d;
   c->num_sms = prop.multiProcessorCount;
+  c->pdl = decode_pdl_supported(d.device);
   c->lay = expert_layout(d.format, d.hidden, d.intermediate);
   c->expert_bytes = c->lay.bytes;
   c->stride = round_up(c->expert_bytes, 4096);
@@ -365,6 +371,7 @@ int expert_cache_create(const pmoe_cache_desc* desc, pmoe_cache** out) {
   c->staged.assign(Lr, 0);
   c->staged_waves.assign(Lr, 0);
   c->pull_deferred.assign(Lr, 0);
+  c->plan_on_compute.assign(Lr, 0);
   c->layer_used.assign(Lr, 0);
   int status = PMOE_OK;
 #define PMOE_TRY(call)              \
@@ -555,9 +562,11 @@ namespace {
 // The residency step of `layer`, ordered after `ids_ready` (the ids' producer) and after
 // the layer's previous forward. defer_pull (SM-pull mode): leave the page-in of the
 // step's waves to the fused decode kernel, which copies each missing expert's bytes as
-// its chunks need them.
+// its chunks need them. compute (SM-pull with defer_pull only): plan on that stream,
+// directly ahead of the decode kernel, instead of on the copy stream.
 int ensure_resident_impl(pmoe_cache* c, int layer, const int32_t* ids, int n_ids, cudaEvent_t ids_ready,
-                         int* waves_out, bool defer_pull = false);
+                         int* waves_out, bool defer_pull = false, cudaStream_t compute = nullptr,
+                         bool on_compute = false);
 
 }  // namespace
 
@@ -594,7 +603,7 @@ int expert_cache_prefetch(pmoe_cache* c, int layer, const int32_t* ids, int n_id
 namespace {
 
 int ensure_resident_impl(pmoe_cache* c, int layer, const int32_t* ids, int n_ids, cudaEvent_t ids_ready,
-                         int* waves_out, bool defer_pull) {
+                         int* waves_out, bool defer_pull, cudaStream_t compute, bool on_compute) {
   if (c == nullptr || layer < 0 || layer >= c->d.num_layers || n_ids < 0 ||
       n_ids > c->d.max_tokens * c->d.top_k || (n_ids > 0 && ids == nullptr))
     return PMOE_EINVAL;
@@ -605,20 +614,28 @@ int ensure_resident_impl(pmoe_cache* c, int layer, const int32_t* ids, int n_ids
   }
   const bool ce = c->d.pagein_mode == PMOE_PAGEIN_COPY_ENGINE;
   // copy-engine mode plans on its own stream, so planning the next layer never queues
-  // behind this layer's copies; SM-pull plans and pulls in one stream order
-  cudaStream_t ps = ce ? c->plan_stream : c->copy_stream;
+  // behind this layer's copies; SM-pull plans and pulls in one stream order. A step
+  // whose page-in the decode kernel does itself plans on the compute stream, right
+  // before that kernel: router, residency and decode then follow one another in one
+  // stream, and each may launch while the one before it drains.
+  on_compute = on_compute && !ce && defer_pull && compute != nullptr;
+  cudaStream_t ps = ce ? c->plan_stream : on_compute ? compute : c->copy_stream;
   if (c->in_capture && ce) {
     snprintf(g_last_error, sizeof(g_last_error),
              "graph capture needs PMOE_PAGEIN_SM_PULL (copy-engine page-in reads the plan on the host)");
     return PMOE_EUNSUPPORTED;
   }
-  PMOE_CUDA(cudaStreamWaitEvent(ps, ids_ready, 0));
+  if (!on_compute) PMOE_CUDA(cudaStreamWaitEvent(ps, ids_ready, 0));
   // inside a captured graph the layer's previous forward precedes this step by graph order
   if (!c->in_capture) PMOE_CUDA(cudaStreamWaitEvent(ps, c->ev_layer_done[layer], 0));
+  c->plan_on_compute[layer] = on_compute ? 1 : 0;
   {
     KernelMark km(c, PMOE_K_RESIDENCY, ps);
+    // programmatic serialization only where nothing but the router precedes it in the
+    // stream (the timers put events between kernels outside graph capture)
+    const bool pdl = on_compute && c->pdl && !(c->timing && !c->in_capture);
     PMOE_CUDA(launch_residency(ids, n_ids, c->d.num_experts, c->d.num_slots, c->st[layer], c->plan_dev[layer],
-                               c->err_dev, c->ws.epoch, ps));
+                               c->err_dev, c->ws.epoch, ps, pdl));
   }
   c->layer_used[layer] = 1;
   int waves = -1;
@@ -649,7 +666,7 @@ int ensure_resident_impl(pmoe_cache* c, int layer, const int32_t* ids, int n_ids
   } else {
     // the plan is on the device now: compute on the resident experts may start while the
     // pull kernel brings the missing ones
-    PMOE_CUDA(cudaEventRecord(c->ev_plan[layer], c->copy_stream));
+    if (!on_compute) PMOE_CUDA(cudaEventRecord(c->ev_plan[layer], c->copy_stream));
     c->pull_deferred[layer] = defer_pull ? 1 : 0;
     if (!defer_pull) {
       KernelMark km(c, PMOE_K_PULL, c->copy_stream);
@@ -657,7 +674,7 @@ int ensure_resident_impl(pmoe_cache* c, int layer, const int32_t* ids, int n_ids
                                   c->expert_bytes, c->arena[layer], c->err_dev, c->copy_stream));
     }
   }
-  PMOE_CUDA(cudaEventRecord(c->ev_ready[layer], c->copy_stream));
+  if (!on_compute) PMOE_CUDA(cudaEventRecord(c->ev_ready[layer], c->copy_stream));
   c->staged[layer] = 1;
   c->staged_waves[layer] = waves >= 0 ? waves : max_waves(c, n_ids);
   if (waves_out) *waves_out = waves;
@@ -687,13 +704,16 @@ int moe_paged_forward(pmoe_cache* c, int layer, const void* x, int T, const int3
     // pages the missing experts in itself, overlapping the host link with the resident
     // experts' weight streaming
     PMOE_CUDA(cudaEventRecord(c->ev_ids, s));
-    const int r = ensure_resident_impl(c, layer, ids, P, c->ev_ids, nullptr, fused && !ce);
+    const int r = ensure_resident_impl(c, layer, ids, P, c->ev_ids, nullptr, fused && !ce, s, true);
     if (r == PMOE_EDEVICE) status = r;
     else if (r != PMOE_OK) return r;
   }
   c->staged[layer] = 0;
   const bool pull_in_kernel = c->pull_deferred[layer] != 0;
   c->pull_deferred[layer] = 0;
+  // the plan was made on this stream, right before the decode kernel
+  const bool planned_here = c->plan_on_compute[layer] != 0;
+  c->plan_on_compute[layer] = 0;
   const int nw = c->staged_waves[layer];
   // Copy-engine steps whose first wave has both resident and paged-in experts compute
   // the resident ones while the copies are still in flight (the plan lists them first).
@@ -723,10 +743,13 @@ int moe_paged_forward(pmoe_cache* c, int layer, const void* x, int T, const int3
                         c->arena[layer], c->stride, c->num_sms, c->err_dev, tc_tile_n(T, k, E), s));
     } else if (fused) {
       KernelMark km(c, PMOE_K_DECODE, s);
+      // launched behind the residency step it follows directly (wave 0 of a step planned
+      // on this stream), so that its CTAs start while the plan is being made
+      const int pdl = (planned_here && wv == 0 && sub == 0 && c->pdl && !(c->timing && !c->in_capture)) ? 1 : 0;
       PMOE_CUDA(launch_decode_fused(c->d.format, (const __nv_bfloat16*)x, ids, w, (const __nv_bfloat16*)residual,
                                     (__nv_bfloat16*)y, T, k, H, I, c->plan_dev[layer], E, wv, sub, fuse_combine,
                                     c->ws, c->arena[layer], c->host_store_dev[layer], pull_in_kernel ? 1 : 0,
-                                    c->stride, c->err_dev, c->num_sms, s));
+                                    c->stride, c->err_dev, c->num_sms, s, pdl));
     } else {
       {
         KernelMark km(c, PMOE_K_GATEUP, s);
@@ -742,7 +765,7 @@ int moe_paged_forward(pmoe_cache* c, int layer, const void* x, int T, const int3
 
   // grouping needs only the ids and the plan; in copy-engine mode the plan is ready
   // once the host has read it, before the copies land
-  PMOE_CUDA(cudaStreamWaitEvent(s, split0 ? c->ev_plan[layer] : c->ev_ready[layer], 0));
+  if (!planned_here) PMOE_CUDA(cudaStreamWaitEvent(s, split0 ? c->ev_plan[layer] : c->ev_ready[layer], 0));
   if (!fused) {  // the fused decode kernel groups the pairs itself
     KernelMark km(c, PMOE_K_GROUP, s);
     PMOE_CUDA(launch_group(ids, P, E, c->plan_dev[layer], c->ws, tc ? tc_tile_n(T, k, E) : 0, c->err_dev, s));

@@ -37,6 +37,7 @@
 #include "decode_common.cuh"
 
 #include <algorithm>
+#include <stdlib.h>
 
 namespace pmoe {
 namespace {
@@ -410,6 +411,7 @@ __global__ void __launch_bounds__(kDfThreads, 1) decode_fused_kernel(const DfArg
     s_abort = 0;
     s_pulled = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    pdl_wait();  // launched behind the residency step: its plan is complete from here on
     const int nw = a.plan[kPlanWaves], ws0 = a.plan[L.wave_start() + a.wave];
     const int ws1 = a.plan[L.wave_start() + a.wave + 1];
     static_assert(kDfLag == 3, "the entry-time slot reads below cover the first three experts");
@@ -462,6 +464,11 @@ __global__ void __launch_bounds__(kDfThreads, 1) decode_fused_kernel(const DfArg
     }
     s_placed = early_n;  // (published by the block barrier below)
   }
+  // Launched behind the residency step (programmatic serialization), the CTAs start
+  // while it runs; nothing that kernel or the ones before it write (plan, ids, weights,
+  // x, the slot arena) is read before this wait. The kernel never triggers its own
+  // dependents early: whatever follows it waits for its end.
+  pdl_wait();
   const int r_lo = (int)((long long)a.H * blockIdx.x / gridDim.x);
   const int r_hi = (int)((long long)a.H * (blockIdx.x + 1) / gridDim.x);
   // One round of independent loads: the plan words, the ids, the first wave's list (read
@@ -970,23 +977,31 @@ __global__ void __launch_bounds__(kDfThreads, 1) decode_fused_kernel(const DfArg
 }
 
 template <int FMT, int NCH1, int NCH2>
-cudaError_t launch_df(const DfArgs& a, int grid, size_t smem, cudaStream_t s) {
+cudaError_t launch_df(const DfArgs& a, int grid, size_t smem, cudaStream_t s, int pdl) {
   auto k = decode_fused_kernel<FMT, NCH1, NCH2>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   // cooperative (all CTAs co-resident: the down chunks wait for other CTAs' gate/up
-  // rows), launched through cudaLaunchKernelEx so that it can be recorded into a graph
+  // rows), launched through cudaLaunchKernelEx so that it can be recorded into a graph;
+  // optionally with programmatic serialization behind the residency step
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kDfThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = pdl ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, k, a);
+}
+
+__global__ void pdl_probe_kernel(int* out) {
+  pdl_wait();
+  if (threadIdx.x == 0) out[blockIdx.x] = 1;
 }
 
 size_t fmt_row_bytes(int fmt, int n) {
@@ -1047,6 +1062,45 @@ extern "C" __attribute__((visibility("default"))) int pmoe_debug_decode_chunks(u
 }
 #endif
 
+bool decode_pdl_supported(int device) {
+  // 0 = not probed yet, 1 = accepted, -1 = refused (per device; the first cache created
+  // on a device probes it, outside any stream capture)
+  static int state[64] = {};
+  if (device < 0 || device >= 64) return false;
+  if (state[device] != 0) return state[device] > 0;
+  const char* off = getenv("PMOE_NO_PDL");  // deployment switch: plain stream order
+  if (off != nullptr && off[0] == '1') {
+    state[device] = -1;
+    return false;
+  }
+  int ok = 0;
+  int* out = nullptr;
+  cudaStream_t st = nullptr;
+  if (cudaMalloc(&out, 2 * sizeof(int)) == cudaSuccess && cudaMemset(out, 0, 2 * sizeof(int)) == cudaSuccess &&
+      cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) == cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2);
+    cfg.blockDim = dim3(32);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    int host[2] = {0, 0};
+    if (cudaLaunchKernelEx(&cfg, pdl_probe_kernel, out) == cudaSuccess && cudaStreamSynchronize(st) == cudaSuccess &&
+        cudaMemcpy(host, out, sizeof(host), cudaMemcpyDeviceToHost) == cudaSuccess)
+      ok = host[0] == 1 && host[1] == 1;
+  }
+  (void)cudaGetLastError();  // a refused attribute combination is not a sticky error
+  if (st != nullptr) cudaStreamDestroy(st);
+  if (out != nullptr) cudaFree(out);
+  state[device] = ok ? 1 : -1;
+  return ok != 0;
+}
+
 bool decode_fused_supported(int fmt, int T, int top_k, int H, int I, int num_sms) {
   DfGeom g;
   return df_geometry(fmt, T, top_k, H, I, num_sms, &g);
@@ -1056,7 +1110,7 @@ cudaError_t launch_decode_fused(int fmt, const __nv_bfloat16* x, const int32_t* 
                                 const __nv_bfloat16* residual, __nv_bfloat16* y, int T, int top_k, int H, int I,
                                 const int32_t* plan, int E, int wave, int sub, int fuse_combine, const Workspace& ws,
                                 uint8_t* arena, const uint8_t* store, int pull, size_t stride, int32_t* err, int num_sms,
-                                cudaStream_t s) {
+                                cudaStream_t s, int pdl) {
   DfGeom g;
   if (!df_geometry(fmt, T, top_k, H, I, num_sms, &g)) return cudaErrorInvalidValue;
   DfArgs a;
@@ -1086,7 +1140,7 @@ cudaError_t launch_decode_fused(int fmt, const __nv_bfloat16* x, const int32_t* 
   a.err = err;
   const size_t smem = g.ring + g.fixed;
   const int nch1 = (int)(fmt_row_bytes(fmt, H) / 16), nch2 = (int)(fmt_row_bytes(fmt, I) / 16);
-#define PMOE_DF(F, A, B) return launch_df<F, A, B>(a, num_sms, smem, s)
+#define PMOE_DF(F, A, B) return launch_df<F, A, B>(a, num_sms, smem, s, pdl)
   if (fmt == PMOE_BF16) {
     if (nch1 <= 32 * 4 && nch2 <= 32 * 1) PMOE_DF(PMOE_BF16, 4, 1);
     if (nch1 <= 32 * 8 && nch2 <= 32 * 3) PMOE_DF(PMOE_BF16, 8, 3);

@@ -15,6 +15,15 @@ constexpr int kMaxTopK = 32;
 constexpr int kGemvMaxTokens = 8;  // decode (weight-streaming) path for T <= this
 constexpr int kDecodeMaxPairs = 64;  // T * top_k of the fused decode kernel
 
+// Programmatic dependent launch (sm_90 and later). A kernel launched with the
+// programmatic-serialization attribute may start while the kernel before it in the
+// stream is still running; pdl_wait() blocks until that kernel has completed and its
+// writes are visible, so a dependent kernel reads nothing its predecessor writes before
+// it. pdl_trigger() lets the dependent kernel launch before this one ends. Both are no-ops
+// for kernels launched without the attribute.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Device error word bits.
 enum : int32_t { kErrBadExpertId = 1, kErrPlanOverflow = 2, kErrBadSlot = 4, kErrPullTimeout = 8 };
 
@@ -81,7 +90,8 @@ size_t router_gemm_smem(int H, int E);
 cudaError_t launch_router_gemm_topk(const __nv_bfloat16* x, const __nv_bfloat16* wr, int T, int H, int E, int top_k,
                                     int renorm, float* logits_out, int32_t* ids, float* w, cudaStream_t s);
 cudaError_t launch_residency(const int32_t* ids, int n_ids, int E, int K, LayerState st,
-                             int32_t* plan, int32_t* err, unsigned long long* epoch, cudaStream_t s);
+                             int32_t* plan, int32_t* err, unsigned long long* epoch, cudaStream_t s,
+                             bool pdl = false);
 cudaError_t launch_group(const int32_t* ids, int P, int E, const int32_t* plan, Workspace ws,
                          int tile_n, int32_t* err, cudaStream_t s);
 cudaError_t launch_gather_rows(const __nv_bfloat16* x, const int32_t* perm, int P, int top_k, int H,
@@ -100,7 +110,10 @@ cudaError_t launch_decode_fused(int fmt, const __nv_bfloat16* x, const int32_t* 
                                 const __nv_bfloat16* residual, __nv_bfloat16* y, int T, int top_k, int H, int I,
                                 const int32_t* plan, int E, int wave, int sub, int fuse_combine, const Workspace& ws,
                                 uint8_t* arena, const uint8_t* store, int pull, size_t stride, int32_t* err,
-                                int num_sms, cudaStream_t s);
+                                int num_sms, cudaStream_t s, int pdl = 0);
+// Whether this device accepts a cooperative launch with programmatic serialization
+// (probed once per device with an empty kernel, outside any stream capture).
+bool decode_pdl_supported(int device);
 cudaError_t launch_pull_pages(const int32_t* plan, int E, int wave, const uint8_t* host_store_dev,
                               size_t stride, size_t expert_bytes, uint8_t* arena, int32_t* err,
                               cudaStream_t s);

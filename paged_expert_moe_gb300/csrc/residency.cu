@@ -65,17 +65,24 @@ __device__ __forceinline__ void residency_body(const int32_t* __restrict__ ids, 
 
   const PlanLayout L{E};
   const int tid = threadIdx.x;
+  // The kernel that consumes the plan may launch now and wait for this one to end. The
+  // table was last written by this layer's previous residency step, which ended before
+  // anything after it in the stream began; the ids and the plan (which the previous
+  // step's compute reads) are touched only after the wait for the kernel before this
+  // one (the router) to complete.
+  pdl_trigger();
   const int step = *st.step;
   if (tid < E) {
     s_pend[tid] = 0;
     s_slot_of[tid] = st.slot_of[tid];
-    plan[L.wave_of() + tid] = -1;
   }
   if (tid < K) {
     s_exp_in[tid] = st.expert_in[tid];
     s_last[tid] = st.last_use[tid];
   }
   if (tid == 0) s_bad = 0;
+  pdl_wait();
+  if (tid < E) plan[L.wave_of() + tid] = -1;
   __syncthreads();
   for (int p = tid; p < n_ids; p += kThreads) {
     const int e = ids[p];
@@ -202,15 +209,29 @@ __global__ void __launch_bounds__(kThreads) residency_layers_kernel(const int32_
 }  // namespace
 
 cudaError_t launch_residency(const int32_t* ids, int n_ids, int E, int K, LayerState st, int32_t* plan,
-                             int32_t* err, unsigned long long* epoch, cudaStream_t s) {
+                             int32_t* err, unsigned long long* epoch, cudaStream_t s, bool pdl) {
   static bool carveout_set = false;  // keep room for a decode CTA on the same SM
   if (!carveout_set) {
     cudaFuncSetAttribute(residency_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                          (int)cudaSharedmemCarveoutMaxShared);
     carveout_set = true;
   }
-  residency_kernel<<<1, kThreads, 0, s>>>(ids, n_ids, E, K, st, plan, err, epoch);
-  return cudaGetLastError();
+  if (!pdl) {
+    residency_kernel<<<1, kThreads, 0, s>>>(ids, n_ids, E, K, st, plan, err, epoch);
+    return cudaGetLastError();
+  }
+  // may start while the kernel before it (the router) drains; it waits for it before
+  // reading the ids
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, residency_kernel, ids, n_ids, E, K, st, plan, err, epoch);
 }
 
 cudaError_t launch_residency_layers(const int32_t* ids, int n_ids, int layers, int E, int K, LayerState st0,

@@ -85,6 +85,7 @@ template <int NPL>
 __global__ void __launch_bounds__(256) router_topk_kernel(const float* __restrict__ logits, int T, int E,
                                                           int top_k, int renorm, int32_t* __restrict__ ids,
                                                           float* __restrict__ w) {
+  pdl_trigger();  // the residency step may launch now; it waits for these ids itself
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= T) return;
   warp_topk<NPL>(logits + (size_t)t * E, E, top_k, renorm, ids + (size_t)t * top_k, w + (size_t)t * top_k);
