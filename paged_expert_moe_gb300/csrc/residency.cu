@@ -7,49 +7,16 @@
 // page-in). Post "Locality of reference helped ...", section "The fix": a hit moves
 // no bytes, a miss copies one expert and evicts the least recently used one.
 //
-// Rules (the readings where the pages are silent):
-//   * every expert used in a step gets last_use = the layer's step counter;
-//   * victims are unprotected slots (empty, or holding an expert not pending in this
-//     step) in ascending (last_use, slot) order; empty slots have last_use = -1;
-//   * a wave holds every pending resident expert plus the lowest-id non-resident
-//     pending experts that fit in the remaining K - |resident| slots;
-//   * the i-th miss (ascending expert id) takes the i-th victim.
-// One thread owns one expert id and one slot (E, K <= 1024 = blockDim.x).
-#include "pmoe_internal.h"
+// The planning itself is step::lru_plan_core (step_common.cuh, which states the rules
+// taken where the pages are silent); this kernel loads the layer's table, plans the step
+// and writes the table, the plan header and the counters back. One thread owns one
+// expert id and one slot (E, K <= 1024 = blockDim.x).
+#include "step_common.cuh"
 
 namespace pmoe {
 namespace {
 
 constexpr int kThreads = 1024;
-
-// Exclusive block-wide prefix sum of one int per thread; *total receives the sum.
-__device__ int block_exclusive_scan(int v, int* s_warp, int* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int x = v;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, x, off);
-    if (lane >= off) x += y;
-  }
-  if (lane == 31) s_warp[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    int w = s_warp[lane];
-    int wx = w;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, wx, off);
-      if (lane >= off) wx += y;
-    }
-    s_warp[lane] = wx - w;  // exclusive warp offsets
-    if (lane == 31) s_warp[32] = wx;
-  }
-  __syncthreads();
-  const int r = s_warp[warp] + x - v;
-  *total = s_warp[32];
-  __syncthreads();
-  return r;
-}
 
 __device__ __forceinline__ void residency_body(const int32_t* __restrict__ ids, int n_ids, int E, int K,
                                                LayerState st, int32_t* __restrict__ plan, int32_t* __restrict__ err,
@@ -63,7 +30,6 @@ __device__ __forceinline__ void residency_body(const int32_t* __restrict__ ids, 
   __shared__ int s_warp[33];
   __shared__ int s_bad;
 
-  const PlanLayout L{E};
   const int tid = threadIdx.x;
   // The kernel that consumes the plan may launch now and wait for this one to end. The
   // table was last written by this layer's previous residency step, which ended before
@@ -82,86 +48,12 @@ __device__ __forceinline__ void residency_body(const int32_t* __restrict__ ids, 
   }
   if (tid == 0) s_bad = 0;
   pdl_wait();
-  if (tid < E) plan[L.wave_of() + tid] = -1;
-  __syncthreads();
-  for (int p = tid; p < n_ids; p += kThreads) {
-    const int e = ids[p];
-    if (e < 0 || e >= E) s_bad = 1;
-    else s_pend[e] = 1;
-  }
-  __syncthreads();
-  const int n_unique = __syncthreads_count(tid < E && s_pend[tid]);
-
-  int wave = 0, n_miss = 0, n_wexp = 0;
-  while (true) {
-    const bool pend = tid < E && s_pend[tid] != 0;
-    if (__syncthreads_count(pend) == 0 || wave >= E) break;
-    const bool res = pend && s_slot_of[tid] >= 0;
-    const bool nonres = pend && !res;
-    const int n_res = __syncthreads_count(res);
-    const int cap = K - n_res;
-    int n_nonres;
-    const int rank = block_exclusive_scan(nonres ? 1 : 0, s_warp, &n_nonres);
-    const int n_load = n_nonres < cap ? n_nonres : cap;
-    if (nonres && rank < n_load) s_rank_exp[rank] = tid;
-    bool unprot = false;
-    if (tid < K) {
-      const int x = s_exp_in[tid];
-      unprot = (x < 0) || (s_pend[x] == 0);
-      s_unprot[tid] = unprot ? 1 : 0;
-    }
-    __syncthreads();
-    if (unprot) {
-      const int my_last = s_last[tid];
-      int vr = 0;
-      for (int v = 0; v < K; ++v)
-        vr += (s_unprot[v] && (s_last[v] < my_last || (s_last[v] == my_last && v < tid))) ? 1 : 0;
-      if (vr < n_load) {
-        const int e_new = s_rank_exp[vr];
-        const int old = s_exp_in[tid];
-        if (old >= 0) s_slot_of[old] = -1;
-        s_exp_in[tid] = e_new;
-        s_slot_of[e_new] = tid;
-        plan[L.miss_exp() + n_miss + vr] = e_new;
-        plan[L.miss_slot() + n_miss + vr] = tid;
-      }
-    }
-    __syncthreads();
-    // wave list: the experts that were resident (hits) first, then this wave's misses,
-    // each part in ascending id, so compute on the hits can start before the page-in
-    const bool inw = tid < E && s_pend[tid] != 0 && s_slot_of[tid] >= 0;
-    const bool inw_hit = inw && res;
-    int n_w, n_h;
-    const int hrank = block_exclusive_scan(inw_hit ? 1 : 0, s_warp, &n_h);
-    const int mrank = block_exclusive_scan((inw && !inw_hit) ? 1 : 0, s_warp, &n_w);
-    n_w += n_h;
-    if (inw) {
-      const int slot = s_slot_of[tid];
-      const int at = n_wexp + (inw_hit ? hrank : n_h + mrank);
-      plan[L.wave_exp() + at] = tid;
-      plan[L.wave_slot() + at] = slot;
-      plan[L.wave_of() + tid] = wave;
-      s_last[slot] = step;
-    }
-    if (tid == 0) {
-      plan[L.wave_start() + wave] = n_wexp;
-      plan[L.miss_start() + wave] = n_miss;
-      plan[L.wave_hits() + wave] = n_h;
-    }
-    __syncthreads();
-    if (inw) s_pend[tid] = 0;
-    n_wexp += n_w;
-    n_miss += n_load;
-    ++wave;
-    __syncthreads();
-  }
+  const step::LruSmem m{s_pend, s_slot_of, s_exp_in, s_last, s_unprot, s_rank_exp, s_warp, &s_bad};
+  const step::LruCounts n = step::lru_plan_core<kThreads>(ids, n_ids, E, K, step, m, plan);
   if (tid == 0) {
-    plan[L.wave_start() + wave] = n_wexp;
-    plan[L.miss_start() + wave] = n_miss;
-    plan[L.wave_hits() + wave] = 0;
-    plan[kPlanUnique] = n_unique;
-    plan[kPlanWaves] = wave;
-    plan[kPlanMisses] = n_miss;
+    plan[kPlanUnique] = n.unique;
+    plan[kPlanWaves] = n.waves;
+    plan[kPlanMisses] = n.misses;
     plan[kPlanError] = s_bad ? kErrBadExpertId : 0;
     plan[kPlanStep] = step;
     const unsigned long long ep = atomicAdd(epoch, 1ull) + 1ull;
@@ -169,9 +61,9 @@ __device__ __forceinline__ void residency_body(const int32_t* __restrict__ ids, 
     plan[kPlanEpochHi] = (int32_t)(uint32_t)(ep >> 32);
     if (s_bad) atomicOr(err, kErrBadExpertId);
     *st.step = step + 1;
-    st.counters[0] += (unsigned long long)(n_unique - n_miss);
-    st.counters[1] += (unsigned long long)n_miss;
-    st.counters[2] += (unsigned long long)wave;
+    st.counters[0] += (unsigned long long)(n.unique - n.misses);
+    st.counters[1] += (unsigned long long)n.misses;
+    st.counters[2] += (unsigned long long)n.waves;
     st.counters[3] += 1ull;
   }
   if (tid < E) st.slot_of[tid] = s_slot_of[tid];

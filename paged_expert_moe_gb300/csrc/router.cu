@@ -5,81 +5,14 @@
 // Experts actually do?": each token is routed to top_k of E experts. Selection
 // compares the fp32 logits themselves (descending, ties to the lower id), so the
 // chosen ids never depend on how exp is rounded.
-#include "pmoe_internal.h"
+#include "step_common.cuh"
 
 #include <math.h>
 
 namespace pmoe {
 namespace {
 
-// Top-k of one token's E logits by one warp; lane l holds logits e = l + 32 * i, i < NPL.
-// row may point to global or shared memory.
-template <int NPL>
-__device__ __forceinline__ void warp_topk(const float* row, int E, int top_k, int renorm, int32_t* ids_row,
-                                          float* w_row) {
-  const int lane = threadIdx.x & 31;
-  float v[NPL];
-#pragma unroll
-  for (int i = 0; i < NPL; ++i) {
-    const int e = lane + 32 * i;
-    v[i] = (e < E) ? row[e] : -INFINITY;
-  }
-  uint32_t taken = 0;
-#pragma unroll
-  for (int i = 0; i < NPL; ++i)
-    if (lane + 32 * i >= E) taken |= 1u << i;
-
-  float my_sel = -INFINITY;  // lane r keeps the r-th selected logit
-  int my_id = -1;
-  float vmax = 0.f;
-  for (int r = 0; r < top_k; ++r) {
-    float bv = -INFINITY;
-    int be = 0x7fffffff;
-#pragma unroll
-    for (int i = 0; i < NPL; ++i) {
-      const int e = lane + 32 * i;
-      if (!(taken >> i & 1u) && (v[i] > bv || be == 0x7fffffff)) {
-        bv = v[i];
-        be = e;
-      }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-      const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-      if (ov > bv || (ov == bv && oe < be) || (be == 0x7fffffff && oe != 0x7fffffff)) {
-        bv = ov;
-        be = oe;
-      }
-    }
-    if ((be & 31) == lane && be != 0x7fffffff) taken |= 1u << (be >> 5);
-    if (r == 0) vmax = bv;
-    if (lane == r) {
-      my_sel = bv;
-      my_id = be;
-    }
-  }
-  // softmax pieces: the full denominator (only needed without renormalisation)
-  float denom;
-  const float e_sel = (lane < top_k) ? expf(my_sel - vmax) : 0.f;
-  if (renorm) {
-    denom = e_sel;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) denom += __shfl_xor_sync(0xffffffffu, denom, off);
-  } else {
-    float sum = 0.f;
-#pragma unroll
-    for (int i = 0; i < NPL; ++i)
-      if (lane + 32 * i < E) sum += expf(v[i] - vmax);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-    denom = sum;
-  }
-  if (lane < top_k) {
-    ids_row[lane] = my_id;
-    w_row[lane] = e_sel / denom;
-  }
-}
+using step::warp_topk;
 
 template <int NPL>
 __global__ void __launch_bounds__(256) router_topk_kernel(const float* __restrict__ logits, int T, int E,
