@@ -130,6 +130,11 @@ struct pmoe_cache {
   cudaEvent_t ev_ids = nullptr, ev_wave_done = nullptr, ev_stack = nullptr;
   Workspace ws{};
   void* ws_buf = nullptr;
+  // persistent stack decode (SM-pull caches of several layers; inside ws_buf)
+  unsigned long long* stack_hq = nullptr;  // [2][16][I]
+  unsigned long long* stack_xq = nullptr;  // [2][2][H]
+  uint8_t** stack_arenas = nullptr;        // [L] device copy of arena
+  const uint8_t** stack_stores = nullptr;  // [L] device copy of host_store_dev
   std::vector<TcMaps> maps;  // per layer tensor maps (bf16 prefill path)
   TcMaps ws_maps{};
   // per-kernel timers
@@ -469,6 +474,12 @@ int expert_cache_create(const pmoe_cache_desc* desc, pmoe_cache** out) {
     const size_t o_ch = carve(4 * chunk_cap);
     const size_t o_ep = carve(8);
     const size_t o_hq = carve(8 * std::min(P, (size_t)kDecodeMaxPairs) * d.intermediate);
+    // the persistent stack decode: tagged exchange words (two layers' worth each) and the
+    // layers' arena and host-store pointers
+    const bool stack_bufs = Lr > 1 && d.pagein_mode == PMOE_PAGEIN_SM_PULL;
+    const size_t o_shq = stack_bufs ? carve(8 * 2 * 16 * (size_t)d.intermediate) : 0;
+    const size_t o_sxq = stack_bufs ? carve(8 * 2 * 2 * (size_t)d.hidden) : 0;
+    const size_t o_tab = stack_bufs ? carve(2 * 8 * (size_t)Lr) : 0;
     const cudaError_t e = cudaMalloc(&c->ws_buf, off);
     if (e != cudaSuccess) {
       set_cuda_error(e, "cudaMalloc (workspace)");
@@ -492,6 +503,16 @@ int expert_cache_create(const pmoe_cache_desc* desc, pmoe_cache** out) {
     c->ws.epoch = (unsigned long long*)(b + o_ep);
     PMOE_TRY(cudaMemset(c->ws.epoch, 0, 8));
     c->ws.hq = (unsigned long long*)(b + o_hq);
+    if (stack_bufs) {
+      c->stack_hq = (unsigned long long*)(b + o_shq);
+      c->stack_xq = (unsigned long long*)(b + o_sxq);
+      PMOE_TRY(cudaMemset(c->stack_hq, 0, 8 * 2 * 16 * (size_t)d.intermediate));
+      PMOE_TRY(cudaMemset(c->stack_xq, 0, 8 * 2 * 2 * (size_t)d.hidden));
+      c->stack_arenas = (uint8_t**)(b + o_tab);
+      c->stack_stores = (const uint8_t**)(b + o_tab + 8 * (size_t)Lr);
+      PMOE_TRY(cudaMemcpy(c->stack_arenas, c->arena.data(), 8 * (size_t)Lr, cudaMemcpyHostToDevice));
+      PMOE_TRY(cudaMemcpy((void*)c->stack_stores, c->host_store_dev.data(), 8 * (size_t)Lr, cudaMemcpyHostToDevice));
+    }
     PMOE_TRY(cudaMemset(c->ws.hq, 0, 8 * std::min(P, (size_t)kDecodeMaxPairs) * d.intermediate));
   }
   if (c->use_tc) {
@@ -849,6 +870,25 @@ int moe_paged_stack_forward(pmoe_cache* c, const void* x, int T, const int32_t* 
       KernelMark km(c, PMOE_K_RESIDENCY, ps);
       PMOE_CUDA(launch_residency_layers(ids, P, L, c->d.num_experts, c->d.num_slots, c->st[0], c->state_stride,
                                         c->plan_dev[0], c->words, c->err_dev, c->ws.epoch, ps));
+    }
+    // Every layer's step one wave (T * top_k <= K): all layers in one persistent launch,
+    // which pages each layer's misses in ahead of its compute and hands h_{l+1} from layer
+    // to layer on the device
+    if (c->stack_hq != nullptr && P <= c->d.num_slots &&
+        decode_stack_supported(c->d.format, T, c->d.top_k, c->d.hidden, c->d.intermediate, L, c->num_sms)) {
+      PMOE_CUDA(cudaEventRecord(c->ev_ready[0], ps));
+      PMOE_CUDA(cudaStreamWaitEvent(s, c->ev_ready[0], 0));
+      for (int l = 0; l < L; ++l) c->layer_used[l] = 1;
+      {
+        KernelMark km(c, PMOE_K_DECODE, s);
+        PMOE_CUDA(launch_decode_stack(c->d.format, (const __nv_bfloat16*)x, (__nv_bfloat16*)y, ids, w, T, c->d.top_k,
+                                      c->d.hidden, c->d.intermediate, c->d.num_experts, L, c->plan_dev[0], c->words,
+                                      c->stack_arenas, c->stack_stores, c->stack_hq, c->stack_xq, c->stride,
+                                      c->err_dev, c->num_sms, s));
+      }
+      if (!c->in_capture)
+        for (int l = 0; l < L; ++l) PMOE_CUDA(cudaEventRecord(c->ev_layer_done[l], s));
+      return status;
     }
     for (int l = 0; l < L; ++l) {
       PMOE_CUDA(cudaEventRecord(c->ev_ready[l], ps));

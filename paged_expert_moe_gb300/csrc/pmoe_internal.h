@@ -106,6 +106,19 @@ cudaError_t launch_combine(const Workspace& ws, const float* w, const __nv_bfloa
                            __nv_bfloat16* y, int T, int top_k, int H, cudaStream_t s,
                            const int32_t* skip_if_single_wave_plan = nullptr);
 bool decode_fused_supported(int fmt, int T, int top_k, int H, int I, int num_sms);
+// The fused decode kernels' chunking of one CTA's rows: chunks per gate/up part (cg) and
+// per down part (cd), and the ring bytes of the largest chunk.
+bool decode_chunking(int fmt, int T, int top_k, int H, int I, int num_sms, int* cg, int* cd, size_t* max_chunk);
+// Persistent decode of all L layers of a stack in one cooperative launch, every layer's
+// step planned beforehand and one wave each (T * top_k <= K). x: h_0 [T][H], y: h_L;
+// ids, w: [L][T][top_k]; plan0: layer l's plan at plan0 + l * plan_words; arenas,
+// stores: device arrays of the layers' slot arenas and mapped host stores; hq
+// [2][16][I] and xq [2][T][H]: tagged exchange words (zeroed once).
+bool decode_stack_supported(int fmt, int T, int top_k, int H, int I, int L, int num_sms);
+cudaError_t launch_decode_stack(int fmt, const __nv_bfloat16* x, __nv_bfloat16* y, const int32_t* ids, const float* w,
+                                int T, int top_k, int H, int I, int E, int L, const int32_t* plan0, int plan_words,
+                                uint8_t* const* arenas, const uint8_t* const* stores, unsigned long long* hq,
+                                unsigned long long* xq, size_t stride, int32_t* err, int num_sms, cudaStream_t s);
 cudaError_t launch_decode_fused(int fmt, const __nv_bfloat16* x, const int32_t* ids, const float* w,
                                 const __nv_bfloat16* residual, __nv_bfloat16* y, int T, int top_k, int H, int I,
                                 const int32_t* plan, int E, int wave, int sub, int fuse_combine, const Workspace& ws,

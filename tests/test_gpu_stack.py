@@ -38,8 +38,10 @@ def _stack_inputs(L, E, k, H, B, steps, seed):
     return traces, logits, xs
 
 
-@pytest.mark.parametrize("B,mode", [(4, 0), (1, 0), (4, 1)])
+@pytest.mark.parametrize("B,mode", [(4, 0), (1, 0), (4, 1), (1, 1), (2, 1)])
 def test_int4_stack_against_oracle_and_without_prefetch(pm, B, mode):
+    """SM-pull mode with B * top_k <= K (B = 1, 2 at K = 26) runs all layers in one
+    persistent launch; B = 4 there (several waves) and copy-engine mode run per layer."""
     L, E, k, H, I, K, steps = 4, 128, 8, 2048, 768, 26, 5
     layers = [hz.SyntheticLayer(2, E, H, I, seed=600, layer=l, fast_int4=True) for l in range(L)]
     traces, logits, xs = _stack_inputs(L, E, k, H, B, steps, seed=601 + B)
@@ -73,5 +75,33 @@ def test_int4_stack_against_oracle_and_without_prefetch(pm, B, mode):
         assert exp_in.tolist() == sims[l].expert_in and last.tolist() == sims[l].last_use
     if B == 4:
         assert sum(sims[l].waves for l in range(L)) > L * steps  # B=4 exceeds K // top_k = 3
+    stack.close()
+    plain.close()
+
+
+@pytest.mark.parametrize("fmt", [0, 1, 3])
+def test_one_launch_stack_equals_per_layer_calls(pm, fmt):
+    """bf16, block-FP8 and MXFP4 experts: the persistent stack launch (every layer one
+    wave: B * top_k = 8 <= K = 12) equals one forward call per layer with residual = input,
+    bit for bit, step after step, and the tables agree."""
+    L, E, k, H, I, K, B, steps = 3, 32, 4, 512, 256, 12, 2, 4
+    layers = [hz.SyntheticLayer(fmt, E, H, I, seed=620 + fmt, layer=l) for l in range(L)]
+    traces, logits, xs = _stack_inputs(L, E, k, H, B, steps, seed=630 + fmt)
+    mode = pm.PMOE_PAGEIN_SM_PULL
+    stack = hz.make_cache(layers, k, K, max_tokens=B, mode=mode)
+    plain = hz.make_cache(layers, k, K, max_tokens=B, mode=mode)
+    for s in range(steps):
+        lg = torch.from_numpy(logits[s].reshape(L * B, E)).cuda()
+        ids, w = pm.moe_router_topk(lg, k)
+        x = hz.to_device_bf16(xs[s])
+        y = stack.moe_paged_stack_forward(x, ids, w)
+        h = x
+        for l in range(L):
+            h = plain.moe_paged_forward(l, h, ids[l * B:(l + 1) * B], w[l * B:(l + 1) * B], residual=h)
+        torch.cuda.synchronize()
+        assert torch.equal(y.view(torch.int16), h.view(torch.int16)), f"step {s}"
+    for l in range(L):
+        assert stack.expert_cache_stats(l) == plain.expert_cache_stats(l)
+        assert stack.expert_cache_slot_table(l)[0].tolist() == plain.expert_cache_slot_table(l)[0].tolist()
     stack.close()
     plain.close()
