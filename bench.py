@@ -734,7 +734,8 @@ def run_stack_child(args, local):
     share a process with the other measurements); returns its stack_int4 record."""
     env = dict(os.environ, WORLD_SIZE="1", RANK="0", LOCAL_RANK=str(local))
     r = subprocess.run([sys.executable, os.path.abspath(__file__), "--section", "stack", "--stack-steps",
-                        str(args.stack_steps)], capture_output=True, text=True, env=env)
+                        str(args.stack_steps), "--stack-layers", str(args.stack_layers)], capture_output=True,
+                       text=True, env=env)
     lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
     if r.returncode != 0 or not lines:
         return {"error": f"stack section exited {r.returncode}: {r.stderr[-300:]}"}
@@ -747,8 +748,8 @@ def run_stack_section(pm, torch, args, local, h2d):
     stack = {}
     # the paged and the all-resident caches side by side, their runs interleaved, so that
     # both see the same host state (each 15 GB pinning slows later runs on a box)
-    pull = make_stack_cache(pm, torch, local, mode=1)
-    res = make_stack_cache(pm, torch, local, mode=1, K=E)
+    pull = make_stack_cache(pm, torch, local, mode=1, layers=args.stack_layers)
+    res = make_stack_cache(pm, torch, local, mode=1, layers=args.stack_layers, K=E)
     runs, res_runs = {}, {}
     for B in (1, 4):
         runs[B] = run_stack(pm, torch, B, args.stack_steps, 3, local, graph=True, h2d_gbs=h2d, cache=pull)
@@ -764,7 +765,7 @@ def run_stack_section(pm, torch, args, local, h2d):
                                            "min(...), t_link = paged bytes / pinned H2D GB/s, t_resident = the "
                                            "same steps with K = E (no misses)"})
         stack[f"B{B}_graph"] = g_run
-    ce = make_stack_cache(pm, torch, local, mode=0)
+    ce = make_stack_cache(pm, torch, local, mode=0, layers=args.stack_layers)
     for B in (1, 4):
         stack[f"B{B}"] = run_stack(pm, torch, B, args.stack_steps, 3, local, h2d_gbs=h2d, cache=ce)
     ce.close()
@@ -972,6 +973,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--prefill-steps", type=int, default=6)
     ap.add_argument("--stack-steps", type=int, default=60)
+    ap.add_argument("--stack-layers", type=int, default=STACK_L,
+                    help="layers of the stack section (48 for the measured workload; fewer for profiling)")
     ap.add_argument("--section", default="all",
                     choices=["all", "prefill", "prefill_sweep", "stack", "decode_staged", "fp8", "mxfp4"],
                     help="run only one part (profiling); the default runs everything")
