@@ -472,6 +472,11 @@ int expert_cache_create(const pmoe_cache_desc* desc, pmoe_cache** out) {
                  o_o = carve(4 * P * d.hidden), o_x = c->use_tc ? carve(2 * P * d.hidden) : 0;
     const size_t chunk_cap = ((P + 255) / 256) * (size_t)E;
     const size_t o_ch = carve(4 * chunk_cap);
+    // block-FP8 on the tensor path: the activation planes' scales (the planes themselves
+    // take the bytes of x_perm and h)
+    const bool f8_tc = c->use_tc && d.format == PMOE_FP8_BLOCK128;
+    const size_t o_sx = f8_tc ? carve(4 * P) : 0;
+    const size_t o_hsc = f8_tc ? carve(4 * P * (size_t)(d.intermediate / 64)) : 0;
     const size_t o_ep = carve(8);
     const size_t o_hq = carve(8 * std::min(P, (size_t)kDecodeMaxPairs) * d.intermediate);
     // the persistent stack decode: tagged exchange words (two layers' worth each) and the
@@ -498,6 +503,9 @@ int expert_cache_create(const pmoe_cache_desc* desc, pmoe_cache** out) {
     c->ws.h = (__nv_bfloat16*)(b + o_h);
     c->ws.o_part = (float*)(b + o_o);
     c->ws.x_perm = c->use_tc ? (__nv_bfloat16*)(b + o_x) : nullptr;
+    c->ws.sx = f8_tc ? (float*)(b + o_sx) : nullptr;
+    c->ws.hsc = f8_tc ? (float*)(b + o_hsc) : nullptr;
+    c->ws.p_cap = P;
     c->ws.chunk_cnt = (int32_t*)(b + o_ch);
     c->ws.chunk_cap = (int)chunk_cap;
     c->ws.epoch = (unsigned long long*)(b + o_ep);
@@ -524,7 +532,7 @@ int expert_cache_create(const pmoe_cache_desc* desc, pmoe_cache** out) {
         goto fail;
       }
     }
-    const int r = tc_make_act_maps(c->ws.x_perm, c->ws.h, (size_t)d.max_tokens * d.top_k, d.hidden, d.intermediate,
+    const int r = tc_make_act_maps(d.format, c->ws.x_perm, c->ws.h, (size_t)d.max_tokens * d.top_k, d.hidden, d.intermediate,
                                    &c->ws_maps);
     if (r != PMOE_OK) {
       status = r;
@@ -793,7 +801,11 @@ int moe_paged_forward(pmoe_cache* c, int layer, const void* x, int T, const int3
   }
   if (tc) {
     KernelMark km(c, PMOE_K_GATHER, s);
-    PMOE_CUDA(launch_gather_rows((const __nv_bfloat16*)x, c->ws.perm, P, k, H, c->ws.x_perm, s));
+    if (tc_fp8_planes(c->d.format, tc_tile_n(T, k, E)))
+      PMOE_CUDA(launch_gather_rows_fp8x2((const __nv_bfloat16*)x, c->ws.perm, P, k, H, c->ws.p_cap,
+                                         reinterpret_cast<uint8_t*>(c->ws.x_perm), c->ws.sx, s));
+    else
+      PMOE_CUDA(launch_gather_rows((const __nv_bfloat16*)x, c->ws.perm, P, k, H, c->ws.x_perm, s));
   }
   for (int wv = 0; wv < nw; ++wv) {
     if (wv > 0 && !pull_in_kernel) {

@@ -10,6 +10,9 @@
 // Large P: per-chunk histograms, a per-expert scan over chunks, then each pair's
 // stable position from its chunk's prefix and its rank among equal ids before it.
 // A pair whose id is outside [0, E) is left out (pos = -1) and flagged.
+// Block-FP8 layers on the tensor path gather x as two e4m3 planes on a per-row
+// power-of-two scale instead (fp8_planes.cuh).
+#include "fp8_planes.cuh"
 #include "pmoe_internal.h"
 
 namespace pmoe {
@@ -195,6 +198,51 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const __nv_bfloat16* _
   }
 }
 
+// Row j of x_perm as two e4m3 planes: hi at xq[j][.], lo at xq[p_cap + j][.], and the
+// row's scale sx[j] (x_perm row j ~= sx[j] * (hi + lo)). One warp per row: a pass for the
+// row's largest magnitude, then one that splits every value.
+__global__ void __launch_bounds__(256) gather_rows_fp8x2_kernel(const __nv_bfloat16* __restrict__ x,
+                                                                const int32_t* __restrict__ perm, int P, int top_k,
+                                                                int H, size_t p_cap, uint8_t* __restrict__ xq,
+                                                                float* __restrict__ sx) {
+  const int lane = threadIdx.x & 31;
+  const int nwarps = gridDim.x * (blockDim.x >> 5);
+  const int nvec = H / 8;
+  for (int j = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); j < P; j += nwarps) {
+    const int t = perm[j] / top_k;
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H);
+    float amax = 0.f;
+    for (int c = lane; c < nvec; c += 32) {
+      const uint4 v = __ldg(src + c);
+      const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(b[i]);
+        amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    float s, inv;
+    plane_scale(amax, &s, &inv);
+    uint2* hi_row = reinterpret_cast<uint2*>(xq + (size_t)j * H);
+    uint2* lo_row = reinterpret_cast<uint2*>(xq + (p_cap + (size_t)j) * H);
+    for (int c = lane; c < nvec; c += 32) {
+      const uint4 v = __ldg(src + c);
+      const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&v);
+      uint16_t hi[4], lo[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(b[i]);
+        split_e4m3x2(f.x * inv, f.y * inv, &hi[i], &lo[i]);
+      }
+      hi_row[c] = make_uint2(hi[0] | ((uint32_t)hi[1] << 16), hi[2] | ((uint32_t)hi[3] << 16));
+      lo_row[c] = make_uint2(lo[0] | ((uint32_t)lo[1] << 16), lo[2] | ((uint32_t)lo[3] << 16));
+    }
+    if (lane == 0) sx[j] = s;
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_group(const int32_t* ids, int P, int E, const int32_t* plan, Workspace ws, int tile_n,
@@ -218,6 +266,16 @@ cudaError_t launch_gather_rows(const __nv_bfloat16* x, const int32_t* perm, int 
   int blocks = (P + 7) / 8;
   if (blocks > 4096) blocks = 4096;
   gather_rows_kernel<<<blocks, 256, 0, s>>>(x, perm, P, top_k, H, x_perm);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_rows_fp8x2(const __nv_bfloat16* x, const int32_t* perm, int P, int top_k, int H,
+                                     size_t p_cap, uint8_t* xq, float* sx, cudaStream_t s) {
+  if (P == 0) return cudaSuccess;
+  if (H % 8 != 0 || (size_t)P > p_cap) return cudaErrorInvalidValue;
+  int blocks = (P + 7) / 8;
+  if (blocks > 4096) blocks = 4096;
+  gather_rows_fp8x2_kernel<<<blocks, 256, 0, s>>>(x, perm, P, top_k, H, p_cap, xq, sx);
   return cudaGetLastError();
 }
 

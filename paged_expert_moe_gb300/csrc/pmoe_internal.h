@@ -69,6 +69,12 @@ struct Workspace {
   __nv_bfloat16* h;     // [P][I] intermediate activations, grouped order
   float* o_part;        // [P][H] per-pair down-projection outputs, grouped order
   __nv_bfloat16* x_perm;  // [P][H] tokens gathered in grouped order (tensor-core path)
+  // Block-FP8 layers on the tensor path hold x_perm and h as two e4m3 planes each, in the
+  // same bytes: x planes [2][p_cap][H], h planes [2][p_cap][I] (fp8_planes.cuh), with
+  // power-of-two scales sx[p_cap] (one per row) and hsc[I/64][p_cap] (one per 64 columns).
+  float* sx;
+  float* hsc;
+  size_t p_cap;         // rows the tensor-core activation buffers hold (max_tokens * top_k)
   int32_t* chunk_cnt;   // [ceil(P/256)][E] per-chunk histograms / prefixes (large-P grouping)
   // [min(P, 64)][I] fused-decode intermediate rows, one 64-bit word per element: bf16 bits
   // in the low 16, the launch's 48-bit tag above (zeroed once; tag 0 is never issued)
@@ -96,6 +102,8 @@ cudaError_t launch_group(const int32_t* ids, int P, int E, const int32_t* plan, 
                          int tile_n, int32_t* err, cudaStream_t s);
 cudaError_t launch_gather_rows(const __nv_bfloat16* x, const int32_t* perm, int P, int top_k, int H,
                                __nv_bfloat16* x_perm, cudaStream_t s);
+cudaError_t launch_gather_rows_fp8x2(const __nv_bfloat16* x, const int32_t* perm, int P, int top_k, int H,
+                                     size_t p_cap, uint8_t* xq, float* sx, cudaStream_t s);
 cudaError_t launch_gemv_gateup(int fmt, const __nv_bfloat16* x, int T, int top_k, int H, int I,
                                const int32_t* plan, int E, int wave, const Workspace& ws,
                                const uint8_t* arena, size_t stride, int num_sms, cudaStream_t s);

@@ -27,6 +27,8 @@
 // waits (bounded) for its copies in flight, frees its TMEM and returns.
 #include "tc_gemm.h"
 
+#include "fp8_planes.cuh"
+
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_fp4.h>
@@ -121,6 +123,21 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n"
+      ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+// Instruction descriptor, kind::f8f6f4: e4m3 A and B (format code 0, K-major), fp32 accumulator.
+__device__ __forceinline__ uint32_t idesc_e4m3(int M, int N) {
+  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// One FP8 MMA, K = 32 (32 bytes of each K-major row).
+__device__ __forceinline__ void mma_e4m3(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}\n"
       ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(acc)
       : "memory");
 }
@@ -623,6 +640,384 @@ __global__ void __launch_bounds__(TcCfg<FMT, NMAX>::kThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------- block-FP8 on kind::f8f6f4
+//
+// The e4m3 weight tiles go from TMA straight to the tensor cores. The activations come as
+// two e4m3 planes on power-of-two scales (fp8_planes.cuh), so a K step is two FP8 MMAs
+// (hi, then lo) into one accumulator: the cost of one bf16 MMA. The weights' 128x128 block
+// scale changes every 128 K and the h scales every 64 K, so the MMAs accumulate one K unit
+// (gate/up: a 128-K stage; down: half a stage) per TMEM partial buffer, and promotion
+// warps fold each partial into fp32 registers:
+//   gate/up  acc += partial * s_w[row block][k block]; the epilogue multiplies by the row's
+//            x scale sx[pair], forms h = silu(gate) * up and writes h as two planes with
+//            one scale per (pair, 64 columns), hsc[m-tile][pair]
+//   down     acc += partial * s_w[row block][k block] * hsc[k unit][pair]; the epilogue
+//            writes the fp32 partial o_part[pair][n]
+// Tiles as in tc_grouped_kernel (swap-AB: 128 weight rows on M, the tile's pairs on N),
+// at most kTcSmallN = 64 pairs. Two promotion groups of four warps take the items in turn,
+// each with its own ring of partial buffers, so one group's epilogue overlaps the other's
+// MMAs. The weight tiles (the HBM stream) and the activation planes (re-read by every
+// m-tile, from L2) have rings and producers of their own, the weights' the deeper one.
+// Warps: 0 TMA weights, 1 MMA issuer (owns the TMEM), 2-5 and 6-9 promotion groups 0 and 1
+// (TMEM lanes 32*(warp%4)..), 10 TMA activation planes.
+struct F8Cfg {
+  static constexpr int kN = 64;                   // pairs per tile (MMA N at most)
+  static constexpr int kBK = 128;                 // K per stage (one byte each)
+  static constexpr int kWBytes = 128 * kBK;       // weight tile, 128 rows
+  static constexpr int kPlaneBytes = kN * kBK;    // one activation plane
+  static constexpr int kXBytes = 2 * kPlaneBytes;
+  static constexpr int kStagingFloats = 128 * 17;  // per group
+  static constexpr int kHscUnits = 16;            // down: h scales staged per window of 16 K units
+  static constexpr int kHscFloats = kHscUnits * kN;
+  static constexpr int kFixedBytes = 2 * (kStagingFloats + kHscFloats + kN) * 4 + 1024 + 1024;
+  static constexpr int kRingStages = (220 * 1024 - kFixedBytes) / kWBytes;  // 16 KB each
+  static constexpr int kXStages = 4;
+  static constexpr int kWStages = kRingStages - kXStages;
+  static constexpr int kParts = 4;                // partial buffers per group
+  static constexpr int kTmemCols = 2 * kParts * kN;
+  static constexpr int kSmemBytes = (kWStages + kXStages) * kWBytes + kFixedBytes;
+  static constexpr int kGroupThreads = 128;
+  static constexpr int kThreads = 352;
+  static_assert(kWBytes == kXBytes && kWStages >= 6 && kSmemBytes <= 227 * 1024 && kTmemCols <= 512, "fp8 tiles");
+};
+
+// Named barriers of the two promotion groups (ids 1 and 2, 128 threads each).
+__device__ __forceinline__ void grp_bar(int g) { asm volatile("bar.sync %0, 128;" ::"r"(1 + g) : "memory"); }
+
+__device__ __forceinline__ int grp_bar_or(int g, int pred) {
+  int r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.s32 p, %2, 0;\n\t"
+      "bar.red.or.pred q, %1, 128, p;\n\t"
+      "selp.s32 %0, 1, 0, q;\n\t}\n"
+      : "=r"(r)
+      : "r"(1 + g), "r"(pred)
+      : "memory");
+  return r;
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+
+template <bool GATEUP>
+__global__ void __launch_bounds__(F8Cfg::kThreads, 1)
+    tc_fp8_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_b,
+                  const int32_t* __restrict__ plan, int E, int wave, int sub, Workspace ws, int I, int H,
+                  const uint8_t* __restrict__ arena, size_t stride, ExpertLayout lay, int32_t* __restrict__ err) {
+  using C = F8Cfg;
+  constexpr int kN = C::kN;
+  constexpr int kUnits = GATEUP ? 1 : 2;  // partial buffers per stage
+  constexpr int kSteps = 4 / kUnits;      // K = 32 MMA steps per unit
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* wring = smem;
+  uint8_t* xring = wring + C::kWStages * C::kWBytes;
+  float* staging0 = reinterpret_cast<float*>(xring + C::kXStages * C::kXBytes);  // [2][128 * 17]
+  float* hsc0 = staging0 + 2 * C::kStagingFloats;                                // [2][kHscUnits * kN]
+  float* sx0 = hsc0 + 2 * C::kHscFloats;                                         // [2][kN]
+  uint64_t* wfull = reinterpret_cast<uint64_t*>(sx0 + 2 * kN);
+  uint64_t* wempty = wfull + C::kWStages;
+  uint64_t* xfull = wempty + C::kWStages;
+  uint64_t* xempty = xfull + C::kXStages;
+  uint64_t* pfull = xempty + C::kXStages;     // [2][kParts] partial buffer written by the MMAs
+  uint64_t* pempty = pfull + 2 * C::kParts;  // [2][kParts] partial buffer read by its group
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(pempty + 2 * C::kParts);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (wave >= plan[kPlanWaves]) return;
+  int t0 = ws.tile_wave[wave], t1 = ws.tile_wave[wave + 1];
+  if (sub == 1) t1 = ws.tile_split[wave];
+  else if (sub == 2) t0 = ws.tile_split[wave];
+  const int m_tiles = GATEUP ? (I / 64) : (H / 128);
+  const int n_items = (t1 - t0) * m_tiles;
+  if ((int)blockIdx.x >= n_items) return;
+  const int kdim = GATEUP ? H : I;
+  const int n_kb = kdim / C::kBK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kWStages; ++s) {
+      mbar_init(&wfull[s], 1);
+      mbar_init(&wempty[s], 1);
+    }
+    for (int s = 0; s < C::kXStages; ++s) {
+      mbar_init(&xfull[s], 1);
+      mbar_init(&xempty[s], 1);
+    }
+    for (int r = 0; r < 2 * C::kParts; ++r) {
+      mbar_init(&pfull[r], 1);
+      mbar_init(&pempty[r], C::kGroupThreads);
+    }
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    prefetch_map(&map_w);
+    prefetch_map(&map_b);
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_holder)),
+                 "r"(C::kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  if (warp == 0 || warp == 10) {
+    if (lane == 0) {
+      // ---------------- TMA producers: weight tiles (warp 0) and activation planes (warp 10)
+      const bool wts = warp == 0;
+      const int depth = wts ? C::kWStages : C::kXStages;
+      uint64_t* fullb = wts ? wfull : xfull;
+      uint64_t* emptyb = wts ? wempty : xempty;
+      uint8_t* ring = wts ? wring : xring;
+      int s = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+        const int tile = t0 + item / m_tiles, mt = item % m_tiles;
+        const int slot = ws.tiles[3 * tile + 0], pstart = ws.tiles[3 * tile + 1], np = ws.tiles[3 * tile + 2];
+        const int nb = (np + kTileRowsB - 1) / kTileRowsB;
+        for (int kb = 0; kb < n_kb; ++kb) {
+          if (!mbar_wait(&emptyb[s], ph ^ 1u, abort_flag, err)) {
+            ok = false;
+            break;
+          }
+          uint8_t* st = ring + s * C::kWBytes;
+          if (wts) {
+            mbar_arrive_expect_tx(&fullb[s], (uint32_t)C::kWBytes);
+            if (GATEUP) {
+              tma_load_3d(st, &map_w, &fullb[s], kb * C::kBK, mt * 64, slot);                      // gate rows
+              tma_load_3d(st + C::kWBytes / 2, &map_w, &fullb[s], kb * C::kBK, I + mt * 64, slot);  // up rows
+            } else {
+              tma_load_3d(st, &map_w, &fullb[s], kb * C::kBK, mt * 128, slot);
+            }
+          } else {
+            mbar_arrive_expect_tx(&fullb[s], (uint32_t)(2 * nb * kTileRowsB * C::kBK));
+            for (int pl = 0; pl < 2; ++pl)
+              for (int b = 0; b < nb; ++b)
+                tma_load_3d(st + pl * C::kPlaneBytes + b * kTileRowsB * C::kBK, &map_b, &fullb[s], kb * C::kBK,
+                            pstart + b * kTileRowsB, pl);
+          }
+          if (++s == depth) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      // drain: every stage's last load consumed and its MMAs committed (bounded)
+      for (int i = 0; i < depth; ++i) {
+        mbar_wait(&emptyb[s], ph ^ 1u, abort_flag, err);
+        if (++s == depth) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer: per unit, hi and lo planes into one partial buffer of
+      // the item's group
+      int sw = 0, sx = 0;
+      uint32_t wph = 0, xph = 0;
+      int r0 = 0, r1 = 0;  // next partial buffer of each group's ring, and its phase
+      uint32_t rph0 = 0u, rph1 = 0u;
+      bool ok = true;
+      int it = 0;
+      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++it) {
+        const int g = it & 1;
+        const int tile = t0 + item / m_tiles;
+        const int np = ws.tiles[3 * tile + 2];
+        const int n_mma = (np + 15) & ~15;
+        const uint32_t idesc = idesc_e4m3(128, n_mma < 16 ? 16 : n_mma);
+        for (int kb = 0; kb < n_kb; ++kb) {
+          if (!mbar_wait(&wfull[sw], wph, abort_flag, err) || !mbar_wait(&xfull[sx], xph, abort_flag, err)) {
+            ok = false;
+            break;
+          }
+          fence_after();
+          const uint32_t a0 = smem_u32(wring + sw * C::kWBytes);
+          const uint32_t bh = smem_u32(xring + sx * C::kXBytes), bl = bh + C::kPlaneBytes;
+          for (int u = 0; u < kUnits; ++u) {
+            int rr = g ? r1 : r0;
+            uint32_t rp = g ? rph1 : rph0;
+            const int pb = g * C::kParts + rr;
+            if (!mbar_wait(&pempty[pb], rp ^ 1u, abort_flag, err)) {
+              ok = false;
+              break;
+            }
+            fence_after();
+            const uint32_t d = tmem + (uint32_t)(pb * kN);
+#pragma unroll
+            for (int j = 0; j < kSteps; ++j) {
+              const uint32_t ko = (uint32_t)((u * kSteps + j) * 32);
+              mma_e4m3(d, sw128_desc(a0 + ko), sw128_desc(bh + ko), idesc, j > 0 ? 1u : 0u);
+              mma_e4m3(d, sw128_desc(a0 + ko), sw128_desc(bl + ko), idesc, 1u);
+            }
+            mma_commit(&pfull[pb]);
+            if (++rr == C::kParts) {
+              rr = 0;
+              rp ^= 1u;
+            }
+            if (g) {
+              r1 = rr;
+              rph1 = rp;
+            } else {
+              r0 = rr;
+              rph0 = rp;
+            }
+          }
+          if (!ok) break;
+          mma_commit(&wempty[sw]);
+          mma_commit(&xempty[sx]);
+          if (++sw == C::kWStages) {
+            sw = 0;
+            wph ^= 1u;
+          }
+          if (++sx == C::kXStages) {
+            sx = 0;
+            xph ^= 1u;
+          }
+        }
+      }
+    }
+  } else {
+    // ---------------- promotion and epilogue: group g = warps 2-5 (g = 0) or 6-9 (g = 1)
+    // takes the items it = g, g + 2, ... of this CTA
+    const int g = (warp - 2) >> 2, qtr = warp & 3;
+    const int row = qtr * 32 + lane;                  // TMEM lane = weight row of the tile
+    const int et = (warp - 2 - 4 * g) * 32 + lane;    // 0..127 within the group
+    float* staging = staging0 + g * C::kStagingFloats;
+    float* hsc_sm = hsc0 + g * C::kHscFloats;
+    float* sx_sm = sx0 + g * kN;
+    const uint32_t tlane = (uint32_t)(qtr * 32) << 16;
+    const int n_units = n_kb * kUnits;
+    int r = 0;
+    uint32_t rph = 0;
+    bool bad = false;
+    int it = 0;
+    for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++it) {
+      if ((it & 1) != g) continue;
+      const int tile = t0 + item / m_tiles, mt = item % m_tiles;
+      const int slot = ws.tiles[3 * tile + 0], pstart = ws.tiles[3 * tile + 1], np = ws.tiles[3 * tile + 2];
+      const int n_mma = (np + 15) & ~15;
+      if (GATEUP && et < kN) sx_sm[et] = et < np ? ws.sx[pstart + et] : 0.f;  // read after grp_bar_or below
+      // this row's 128x128 weight-block scales: gate rows (lanes 0-63) and up rows (64-127)
+      // of a gate/up tile lie in one block row each
+      const int rb = GATEUP ? ((row < 64 ? mt * 64 : I + mt * 64) >> 7) : mt;
+      const float* sw_row = reinterpret_cast<const float*>(arena + (size_t)slot * stride +
+                                                           (GATEUP ? lay.gu_s : lay.d_s)) +
+                            (size_t)rb * n_kb;
+      float acc[kN];
+#pragma unroll
+      for (int i = 0; i < kN; ++i) acc[i] = 0.f;
+      for (int kb = 0; kb < n_kb; ++kb) {
+        const float sw = __ldg(sw_row + kb);
+        for (int u = 0; u < kUnits; ++u) {
+          const int ku = kb * kUnits + u;
+          if (!GATEUP && ku % C::kHscUnits == 0) {
+            // stage the h scales of the next window of K units for this tile's pairs
+            const int w = n_units - ku < C::kHscUnits ? n_units - ku : C::kHscUnits;
+            grp_bar(g);
+            for (int i = et; i < w * kN; i += C::kGroupThreads) {
+              const int uu = i / kN, c = i % kN;
+              hsc_sm[i] = c < np ? ws.hsc[(size_t)(ku + uu) * ws.p_cap + pstart + c] : 0.f;
+            }
+            grp_bar(g);
+          }
+          const int pb = g * C::kParts + r;
+          // tcgen05.ld is warp-collective: the warp goes on only if all its lanes' waits did
+          const bool got = __all_sync(0xffffffffu, !bad && mbar_wait(&pfull[pb], rph, abort_flag, err));
+          if (!got) bad = true;
+          fence_after();
+          if (got) {
+            // two halves of 32 columns (the second only if the MMAs wrote it)
+            const float* hs = hsc_sm + (ku % C::kHscUnits) * kN;
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+              if (h2 == 0 || n_mma > 32) {
+                uint32_t v[32];
+                tmem_ld32(tmem + tlane + (uint32_t)(pb * kN + 32 * h2), v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                  acc[32 * h2 + i] =
+                      fmaf(__uint_as_float(v[i]), GATEUP ? sw : sw * hs[32 * h2 + i], acc[32 * h2 + i]);
+              }
+            }
+          }
+          fence_before();
+          mbar_arrive(&pempty[pb]);
+          if (++r == C::kParts) {
+            r = 0;
+            rph ^= 1u;
+          }
+        }
+      }
+      if (grp_bar_or(g, bad ? 1 : 0)) break;
+      if (GATEUP) {
+        // exchange 16 pairs at a time through shared memory (gate rows 0-63, up rows
+        // 64-127); 8 threads per pair then form 8 consecutive h values each, take the
+        // scale of the pair's 64 columns and write both planes
+        uint8_t* hq = reinterpret_cast<uint8_t*>(ws.h);
+        const int pl = et >> 3, js = (et & 7) * 8;
+#pragma unroll
+        for (int cc = 0; cc < kN; cc += 16) {
+          if (cc < n_mma) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) staging[row * 17 + i] = acc[cc + i] * sx_sm[cc + i];
+            grp_bar(g);
+            float hv[8], amax = 0.f;
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) {
+              const float gt = staging[(js + jj) * 17 + pl], up = staging[(64 + js + jj) * 17 + pl];
+              hv[jj] = gt / (1.f + expf(-gt)) * up;
+              amax = fmaxf(amax, fabsf(hv[jj]));
+            }
+#pragma unroll
+            for (int o = 4; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+            float sc, inv;
+            plane_scale(amax, &sc, &inv);
+            uint16_t hi[4], lo[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) split_e4m3x2(hv[2 * q] * inv, hv[2 * q + 1] * inv, &hi[q], &lo[q]);
+            if (cc + pl < np) {
+              const size_t prow = (size_t)pstart + cc + pl;
+              *reinterpret_cast<uint2*>(hq + prow * I + mt * 64 + js) =
+                  make_uint2(hi[0] | ((uint32_t)hi[1] << 16), hi[2] | ((uint32_t)hi[3] << 16));
+              *reinterpret_cast<uint2*>(hq + (ws.p_cap + prow) * I + mt * 64 + js) =
+                  make_uint2(lo[0] | ((uint32_t)lo[1] << 16), lo[2] | ((uint32_t)lo[3] << 16));
+              if ((et & 7) == 0) ws.hsc[(size_t)mt * ws.p_cap + prow] = sc;
+            }
+            grp_bar(g);
+          }
+        }
+      } else {
+        const int n = mt * 128 + row;
+#pragma unroll
+        for (int i = 0; i < kN; ++i)
+          if (i < np) ws.o_part[(size_t)(pstart + i) * H + n] = acc[i];
+      }
+    }
+  }
+  fence_before();
+  __syncthreads();
+  fence_after();
+  if (warp == 1) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::kTmemCols) : "memory");
+  }
+}
+
 // ---------------------------------------------------------------- host side
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -642,16 +1037,45 @@ EncodeTiledFn get_encode() {
   return fn;
 }
 
+// bf16 elements with the 128-byte swizzle (MMA operands), raw bytes unswizzled (the
+// converters' input), or bytes with the 128-byte swizzle (e4m3 MMA operands)
+enum MapKind { kMapBf16Sw128, kMapBytes, kMapBytesSw128 };
+
 int encode(CUtensorMap* m, void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides_bytes,
-           const cuuint32_t* box, bool bytes_unswizzled = false) {
+           const cuuint32_t* box, MapKind kind = kMapBf16Sw128) {
   EncodeTiledFn fn = get_encode();
   if (fn == nullptr) return PMOE_ECUDA;
   cuuint32_t estr[3] = {1, 1, 1};
-  const CUresult r = fn(m, bytes_unswizzled ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank,
-                        base, dims, strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        bytes_unswizzled ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+  const CUresult r = fn(m, kind == kMapBf16Sw128 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                        rank, base, dims, strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        kind == kMapBytes ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? PMOE_OK : PMOE_ECUDA;
+}
+
+template <bool GATEUP>
+cudaError_t launch_f8_n(const CUtensorMap& mw, const CUtensorMap& mb, const int32_t* plan, int E, int wave, int sub,
+                        const Workspace& ws, int I, int H, const uint8_t* arena, size_t stride, int num_sms,
+                        int32_t* err, cudaStream_t s) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    const cudaError_t e = cudaFuncSetAttribute(tc_fp8_kernel<GATEUP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               F8Cfg::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  tc_fp8_kernel<GATEUP><<<num_sms, F8Cfg::kThreads, F8Cfg::kSmemBytes, s>>>(
+      mw, mb, plan, E, wave, sub, ws, I, H, arena, stride, expert_layout(PMOE_FP8_BLOCK128, H, I), err);
+  return cudaGetLastError();
+}
+
+// block-FP8 with the small pair cap (tc_fp8_planes)
+template <bool GATEUP>
+cudaError_t launch_f8(const CUtensorMap& mw, const CUtensorMap& mb, const int32_t* plan, int E, int wave, int sub,
+                      const Workspace& ws, int I, int H, const uint8_t* arena, size_t stride, int num_sms,
+                      int32_t* err, int tile_n, cudaStream_t s) {
+  if (tile_n > F8Cfg::kN) return cudaErrorInvalidValue;
+  return launch_f8_n<GATEUP>(mw, mb, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, s);
 }
 
 template <bool GATEUP, int FMT, int NMAX>
@@ -703,6 +1127,19 @@ int tc_make_weight_maps(uint8_t* arena, size_t stride, int K, int H, int I, int 
     return encode(&out->d, arena + lay.d_w, 3, dims, strides, box) == PMOE_OK ? PMOE_OK : PMOE_ECUDA;
   }
   if (fmt != PMOE_FP8_BLOCK128 && fmt != PMOE_INT4_GPTQ_G128 && fmt != PMOE_MXFP4) return PMOE_EUNSUPPORTED;
+  if (fmt == PMOE_FP8_BLOCK128) {
+    // e4m3 rows as MMA operands: 128-byte boxes (128 K), 128-byte swizzle
+    {
+      const cuuint64_t dims[3] = {(cuuint64_t)H, (cuuint64_t)(2 * I), (cuuint64_t)K};
+      const cuuint64_t strides[2] = {(cuuint64_t)H, (cuuint64_t)stride};
+      const cuuint32_t box[3] = {128, 64, 1};
+      if (encode(&out->gu8, arena + lay.gu_w, 3, dims, strides, box, kMapBytesSw128) != PMOE_OK) return PMOE_ECUDA;
+    }
+    const cuuint64_t dims[3] = {(cuuint64_t)I, (cuuint64_t)H, (cuuint64_t)K};
+    const cuuint64_t strides[2] = {(cuuint64_t)I, (cuuint64_t)stride};
+    const cuuint32_t box[3] = {128, 128, 1};
+    if (encode(&out->d8, arena + lay.d_w, 3, dims, strides, box, kMapBytesSw128) != PMOE_OK) return PMOE_ECUDA;
+  }
   // quantised weights are loaded as bytes (one e4m3, or two int4 / E2M1 codes, per byte), unswizzled
   const cuuint64_t hb = fmt == PMOE_FP8_BLOCK128 ? (cuuint64_t)H : (cuuint64_t)H / 2;
   const cuuint64_t ib = fmt == PMOE_FP8_BLOCK128 ? (cuuint64_t)I : (cuuint64_t)I / 2;
@@ -711,15 +1148,28 @@ int tc_make_weight_maps(uint8_t* arena, size_t stride, int K, int H, int I, int 
     const cuuint64_t dims[3] = {hb, (cuuint64_t)(2 * I), (cuuint64_t)K};
     const cuuint64_t strides[2] = {hb, (cuuint64_t)stride};
     const cuuint32_t box[3] = {kbb, 64, 1};
-    if (encode(&out->gu, arena + lay.gu_w, 3, dims, strides, box, true) != PMOE_OK) return PMOE_ECUDA;
+    if (encode(&out->gu, arena + lay.gu_w, 3, dims, strides, box, kMapBytes) != PMOE_OK) return PMOE_ECUDA;
   }
   const cuuint64_t dims[3] = {ib, (cuuint64_t)H, (cuuint64_t)K};
   const cuuint64_t strides[2] = {ib, (cuuint64_t)stride};
   const cuuint32_t box[3] = {kbb, 128, 1};
-  return encode(&out->d, arena + lay.d_w, 3, dims, strides, box, true) == PMOE_OK ? PMOE_OK : PMOE_ECUDA;
+  return encode(&out->d, arena + lay.d_w, 3, dims, strides, box, kMapBytes) == PMOE_OK ? PMOE_OK : PMOE_ECUDA;
 }
 
-int tc_make_act_maps(__nv_bfloat16* x_perm, __nv_bfloat16* h, size_t P, int H, int I, TcMaps* out) {
+int tc_make_act_maps(int fmt, __nv_bfloat16* x_perm, __nv_bfloat16* h, size_t P, int H, int I, TcMaps* out) {
+  if (fmt == PMOE_FP8_BLOCK128) {
+    // the two e4m3 planes of x and of h, [2][P][cols] bytes in the bf16 buffers' place
+    {
+      const cuuint64_t dims[3] = {(cuuint64_t)H, (cuuint64_t)P, 2};
+      const cuuint64_t strides[2] = {(cuuint64_t)H, (cuuint64_t)H * P};
+      const cuuint32_t box[3] = {128, (cuuint32_t)kTileRowsB, 1};
+      if (encode(&out->x8, x_perm, 3, dims, strides, box, kMapBytesSw128) != PMOE_OK) return PMOE_ECUDA;
+    }
+    const cuuint64_t dims[3] = {(cuuint64_t)I, (cuuint64_t)P, 2};
+    const cuuint64_t strides[2] = {(cuuint64_t)I, (cuuint64_t)I * P};
+    const cuuint32_t box[3] = {128, (cuuint32_t)kTileRowsB, 1};
+    if (encode(&out->h8, h, 3, dims, strides, box, kMapBytesSw128) != PMOE_OK) return PMOE_ECUDA;
+  }
   {
     const cuuint64_t dims[2] = {(cuuint64_t)H, (cuuint64_t)P};
     const cuuint64_t strides[1] = {(cuuint64_t)H * 2};
@@ -738,6 +1188,8 @@ int tc_make_act_maps(__nv_bfloat16* x_perm, __nv_bfloat16* h, size_t P, int H, i
 cudaError_t tc_gateup(int fmt, const TcMaps& wm, const TcMaps& am, const int32_t* plan, int E, int wave, int sub,
                       const Workspace& ws, int I, int H, const uint8_t* arena, size_t stride, int num_sms,
                       int32_t* err, int tile_n, cudaStream_t s) {
+  if (tc_fp8_planes(fmt, tile_n))
+    return launch_f8<true>(wm.gu8, am.x8, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, tile_n, s);
   if (fmt == PMOE_FP8_BLOCK128)
     return launch_tc<true, PMOE_FP8_BLOCK128>(wm.gu, am.x, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, tile_n, s);
   if (fmt == PMOE_INT4_GPTQ_G128)
@@ -751,6 +1203,8 @@ cudaError_t tc_gateup(int fmt, const TcMaps& wm, const TcMaps& am, const int32_t
 cudaError_t tc_down(int fmt, const TcMaps& wm, const TcMaps& am, const int32_t* plan, int E, int wave, int sub,
                     const Workspace& ws, int I, int H, const uint8_t* arena, size_t stride, int num_sms, int32_t* err,
                     int tile_n, cudaStream_t s) {
+  if (tc_fp8_planes(fmt, tile_n))
+    return launch_f8<false>(wm.d8, am.h8, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, tile_n, s);
   if (fmt == PMOE_FP8_BLOCK128)
     return launch_tc<false, PMOE_FP8_BLOCK128>(wm.d, am.h, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, tile_n, s);
   if (fmt == PMOE_INT4_GPTQ_G128)

@@ -15,13 +15,17 @@ struct TcMaps {
   CUtensorMap d;   // down rows of every slot: dims {I (bytes if quantised), H, K}
   CUtensorMap x;   // gathered activations x_perm: dims {H, P} bf16
   CUtensorMap h;   // intermediate h: dims {I, P} bf16
+  // block-FP8 on the e4m3 MMAs: weight rows in 128-byte swizzled boxes, and the two
+  // e4m3 planes of x and h ({H or I, P, 2} bytes, in the bf16 buffers' place)
+  CUtensorMap gu8, d8, x8, h8;
 };
 
 bool tc_supported(int H, int I);
-// Weight tensor maps over one layer's slot arena: bf16 rows (128-byte swizzle) or, for
-// block-FP8 and GPTQ-int4, the raw quantised bytes (dequantised in shared memory).
+// Weight tensor maps over one layer's slot arena: bf16 rows (128-byte swizzle) or the raw
+// quantised bytes (dequantised in shared memory); block-FP8 also as 128-byte swizzled
+// e4m3 operand boxes.
 int tc_make_weight_maps(uint8_t* arena, size_t stride, int K, int H, int I, int fmt, TcMaps* out);
-int tc_make_act_maps(__nv_bfloat16* x_perm, __nv_bfloat16* h, size_t P, int H, int I, TcMaps* out);
+int tc_make_act_maps(int fmt, __nv_bfloat16* x_perm, __nv_bfloat16* h, size_t P, int H, int I, TcMaps* out);
 // sub: 0 = the whole wave, 1 = its experts that were resident before the step,
 // 2 = its experts paged in for this wave (tiles of the two parts are contiguous).
 cudaError_t tc_gateup(int fmt, const TcMaps& wm, const TcMaps& am, const int32_t* plan, int E, int wave, int sub,
@@ -36,5 +40,8 @@ cudaError_t tc_down(int fmt, const TcMaps& wm, const TcMaps& am, const int32_t* 
 inline int tc_tile_n(int T, int top_k, int E) {
   return (long long)T * top_k <= (long long)(kTcSmallN / 2) * E ? kTcSmallN : kTcMaxN;
 }
+// Block-FP8 forwards with small tiles run e4m3 MMAs on two-plane activations (x gathered
+// by launch_gather_rows_fp8x2); with large tiles the weights are dequantised to bf16.
+inline bool tc_fp8_planes(int fmt, int tile_n) { return fmt == PMOE_FP8_BLOCK128 && tile_n <= kTcSmallN; }
 
 }  // namespace pmoe

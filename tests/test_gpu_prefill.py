@@ -46,11 +46,13 @@ def _forward(cache, x_bits, logits, k):
 
 
 @pytest.mark.parametrize("T,skew,fmt", [(300, True, 0), (9, False, 0), (64, False, 0), (1000, False, 0),
-                                        (300, True, 1), (64, False, 1), (300, True, 2), (64, False, 2),
-                                        (300, True, 3), (64, False, 3)])
+                                        (300, True, 1), (64, False, 1), (128, True, 1), (1000, False, 1),
+                                        (300, True, 2), (64, False, 2), (300, True, 3), (64, False, 3)])
 def test_prefill_small_layer_parity_and_bitwise_k_invariance(pm, T, skew, fmt):
-    """bf16, block-FP8, GPTQ-int4 and MXFP4 prefill tiles (the quantised formats are
-    dequantised to bf16 in shared memory)."""
+    """bf16, block-FP8, GPTQ-int4 and MXFP4 prefill tiles. Block-FP8 with few pairs per
+    expert (T=64, and T=128 skewed, where hot experts take several 64-pair tiles) runs
+    e4m3 MMAs on two-plane activations; with more (T=300, 1000) its weights are
+    dequantised to bf16 in shared memory, like int4 and MXFP4."""
     E, k, H, I = 16, 4, 256, 384
     L = hz.SyntheticLayer(fmt, E, H, I, seed=200 + T)
     rng = np.random.default_rng(200 + T)
