@@ -458,7 +458,8 @@ def run_prefill_sweep(pm, torch, args, local, hbm_peak, tc_peak):
         runs = {f"T{T}_warm_all_resident": run_prefill(pm, torch, store, args.prefill_steps, 2, local, K=E, cold=False,
                                                        fmt=fmt, T=T, n_inputs=2) for T in sizes}
         out[name] = _prefill_summary(runs, hbm_peak, tc_peak, wbytes_per_elem=bpe)
-    out["fp8"]["note"] = "FP8 weights are dequantised to bf16 in shared memory for kind::f16 MMAs"
+    out["fp8"]["note"] = ("256-pair tiles: FP8 weights dequantised to bf16 in shared memory for kind::f16 MMAs "
+                          "(64-pair tiles run e4m3 kind::f8f6f4 MMAs on two-plane activations)")
     out["mxfp4"]["note"] = "MXFP4 weights (E2M1 x E8M0, exact in bf16) are dequantised in shared memory for kind::f16 MMAs"
     return out
 
@@ -690,7 +691,9 @@ def run_fp8(pm, torch, args, local, hbm_peak):
                           "decode_kernel_measured_in": "page-in staged ahead by the pull kernel"},
             "prefill_512_cold": dict(pre, FLOP_per_step=flop, weight_bytes_per_step=E * ebytes,
                                      hbm_bound_tflops=flop / (E * ebytes / (hbm_peak * 1e9)) / 1e12,
-                                     note="FP8 weights are dequantised to bf16 in shared memory for kind::f16 MMAs")}
+                                     hbm_bound_frac=pre["gemm_tflops"] / (flop / (E * ebytes / (hbm_peak * 1e9)) / 1e12),
+                                     note="64-pair tiles: e4m3 weights into tcgen05 kind::f8f6f4 MMAs, activations "
+                                          "as two e4m3 planes (hi + lo) on power-of-two scales")}
 
 
 def run_mxfp4(pm, torch, args, local, hbm_peak):
