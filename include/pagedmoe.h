@@ -190,6 +190,31 @@ PMOE_API int moe_router_gemm_topk(const void* x, const void* router_weight, int 
                                   int renormalize, float* logits_out, int32_t* ids_out, float* w_out, void* stream);
 
 /*
+ * moe_group_by_expert — the grouping in front of the fused MoE (section "What does
+ * Paged Experts actually do?": the routed (token, rank) pairs run expert by expert),
+ * run by the same kernels moe_paged_forward uses for it. Pair p of a flattened id
+ * array (p = t * top_k + r):
+ *   counts[e]  pairs with id e;   offs = exclusive scan of counts, offs[E] = valid pairs
+ *   perm[j]    the pair at grouped position j: ids ascending, and pairs ascending within
+ *              one id (a stable sort by id)
+ *   pos[p]     j with perm[j] == p; -1 for an id outside [0, E), which is left out of
+ *              the grouping and ORs 1 into *err_dev
+ *   ids        device, int32 [P]
+ *   counts     device, int32 [E];   offs  device, int32 [E + 1]
+ *   perm, pos  device, int32 [P]; perm entries from offs[E] on are left as they were
+ *   scratch    device, int32 [scratch_ints] per-chunk histograms, needed when
+ *              moe_group_scratch_ints(P, E) > 0 (P above 8192), else may be NULL
+ *   err_dev    device int32, or NULL
+ * P in 0..2^24 and E in 1..1024, and enough scratch, else PMOE_EINVAL. P = 0 writes
+ * zero counts and offs.
+ */
+PMOE_API int moe_group_by_expert(const int32_t* ids, int P, int E, int32_t* counts, int32_t* offs, int32_t* perm,
+                                 int32_t* pos, int32_t* scratch, size_t scratch_ints, int32_t* err_dev,
+                                 void* stream);
+/* The int32 scratch moe_group_by_expert needs for P pairs over E experts (0 if none). */
+PMOE_API size_t moe_group_scratch_ints(int P, int E);
+
+/*
  * expert_cache_create — build the paged-expert state for `num_layers` MoE layers:
  * a pinned host store of all E experts per layer, a device arena of K slots per
  * layer, a device LRU table per layer (all slots empty), a copy stream, events and

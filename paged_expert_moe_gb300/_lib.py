@@ -56,6 +56,8 @@ _SIGS = {
     "pmoe_expert_bytes": ([_I, _I, _I], ctypes.c_size_t),
     "moe_router_topk": ([_P, _I, _I, _I, _I, _P, _P, _P], _I),
     "moe_router_gemm_topk": ([_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P], _I),
+    "moe_group_by_expert": ([_P, _I, _I, _P, _P, _P, _P, _P, ctypes.c_size_t, _P, _P], _I),
+    "moe_group_scratch_ints": ([_I, _I], ctypes.c_size_t),
     "expert_cache_create": ([ctypes.POINTER(pmoe_cache_desc), ctypes.POINTER(_P)], _I),
     "expert_cache_destroy": ([_P], None),
     "expert_cache_host_store": ([_P, _I, ctypes.POINTER(_P), ctypes.POINTER(ctypes.c_size_t)], _I),
@@ -127,6 +129,26 @@ def moe_router_topk(logits, top_k, renormalize=True, ids_out=None, w_out=None, s
     _check(lib.moe_router_topk(_ptr(logits), T, E, top_k, 1 if renormalize else 0, _ptr(ids_out), _ptr(w_out),
                                _stream_handle(stream)), "moe_router_topk")
     return ids_out, w_out
+
+
+def moe_group_by_expert(ids, E, err_out=None, stream=None):
+    """ids: CUDA int32 (any shape, flattened to P pairs) -> (counts [E], offs [E + 1],
+    perm [P], pos [P]) int32; perm entries from offs[E] on (ids outside [0, E)) are
+    undefined. err_out (CUDA int32 [1]) gets 1 ORed in for such an id."""
+    import torch
+    lib = load()
+    assert ids.dtype == torch.int32 and ids.is_cuda and ids.is_contiguous()
+    P = ids.numel()
+    dev = ids.device
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    offs = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    perm = torch.empty(max(P, 1), dtype=torch.int32, device=dev)[:P]
+    pos = torch.empty(max(P, 1), dtype=torch.int32, device=dev)[:P]
+    n_scratch = int(lib.moe_group_scratch_ints(P, E))
+    scratch = torch.empty(n_scratch, dtype=torch.int32, device=dev) if n_scratch > 0 else None
+    _check(lib.moe_group_by_expert(_ptr(ids), P, E, _ptr(counts), _ptr(offs), _ptr(perm), _ptr(pos), _ptr(scratch),
+                                   n_scratch, _ptr(err_out), _stream_handle(stream)), "moe_group_by_expert")
+    return counts, offs, perm, pos
 
 
 def moe_router_gemm_topk(x, router_weight, top_k, renormalize=True, ids_out=None, w_out=None, logits_out=None,

@@ -319,6 +319,29 @@ int moe_router_topk(const float* logits, int T, int E, int top_k, int renormaliz
   return PMOE_OK;
 }
 
+int moe_group_by_expert(const int32_t* ids, int P, int E, int32_t* counts, int32_t* offs, int32_t* perm,
+                        int32_t* pos, int32_t* scratch, size_t scratch_ints, int32_t* err_dev, void* stream) {
+  if (P < 0 || P > (1 << 24) || E < 1 || E > kMaxExperts) return PMOE_EINVAL;
+  if (counts == nullptr || offs == nullptr || (P > 0 && (ids == nullptr || perm == nullptr || pos == nullptr)))
+    return PMOE_EINVAL;
+  if (P > kGroupOneCtaMaxPairs && (scratch == nullptr || scratch_ints < moe_group_scratch_ints(P, E)))
+    return PMOE_EINVAL;
+  Workspace ws{};
+  ws.counts = counts;
+  ws.offs = offs;
+  ws.perm = perm;
+  ws.pos = pos;
+  ws.chunk_cnt = scratch;
+  ws.chunk_cap = (int)std::min(scratch_ints, (size_t)INT32_MAX);
+  PMOE_CUDA(launch_group(ids, P, E, nullptr, ws, 0, err_dev, (cudaStream_t)stream));
+  return PMOE_OK;
+}
+
+size_t moe_group_scratch_ints(int P, int E) {
+  if (P <= kGroupOneCtaMaxPairs) return 0;
+  return (size_t)((P + 255) / 256) * (size_t)E;
+}
+
 int moe_router_gemm_topk(const void* x, const void* router_weight, int T, int H, int E, int top_k, int renormalize,
                          float* logits_out, int32_t* ids_out, float* w_out, void* stream) {
   if (T < 0 || E < 1 || E > kMaxExperts || top_k < 1 || top_k > E || top_k > kMaxTopK || H < 8 || H % 8 != 0)

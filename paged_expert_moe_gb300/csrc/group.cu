@@ -30,7 +30,7 @@ __global__ void __launch_bounds__(kChunk) group_chunk_hist(const int32_t* __rest
   if (p < P) {
     const int e = ids[p];
     if (e >= 0 && e < E) atomicAdd(&s_cnt[e], 1);
-    else atomicOr(err, kErrBadExpertId);
+    else if (err != nullptr) atomicOr(err, kErrBadExpertId);
   }
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) chunk_cnt[(size_t)blockIdx.x * E + e] = s_cnt[e];
@@ -72,9 +72,11 @@ __global__ void __launch_bounds__(kChunk) group_chunk_place(const int32_t* __res
   ws.pos[p] = j;
 }
 
-// Single CTA: offs = scan(counts); per-wave tiles of at most tile_n pairs.
-__global__ void __launch_bounds__(1024) group_scan_tiles(int E, const int32_t* __restrict__ plan, Workspace ws,
-                                                         int tile_n, int32_t* __restrict__ err) {
+// offs = scan(counts); per-wave tiles of at most tile_n pairs. One CTA of 1024 threads,
+// counts already in ws.counts (written by this CTA before a barrier, or by an earlier
+// launch).
+__device__ void offs_and_tiles(int E, const int32_t* __restrict__ plan, const Workspace& ws, int tile_n,
+                               int32_t* __restrict__ err) {
   __shared__ int s_v[kMaxExperts + 1];
   __shared__ int s_t[kMaxExperts + 1];
   const int tid = threadIdx.x;
@@ -141,6 +143,78 @@ __global__ void __launch_bounds__(1024) group_scan_tiles(int E, const int32_t* _
   }
 }
 
+__global__ void __launch_bounds__(1024) group_scan_tiles(int E, const int32_t* __restrict__ plan, Workspace ws,
+                                                         int tile_n, int32_t* __restrict__ err) {
+  offs_and_tiles(E, plan, ws, tile_n, err);
+}
+
+// Single CTA, the whole grouping in one launch: a stable counting sort. The ids, the
+// per-warp histograms and perm live in shared memory (4 P + 128 E + 4 P bytes). The
+// ranking within a batch costs ~140 cycles per warp, so four launches over many CTAs
+// beat it beyond kGroupOneCtaMaxPairs. Warp w
+// takes the pairs [w * per, (w + 1) * per) in batches of 32; lanes of a batch with the
+// same id are ranked by lane (match + popcount), so an expert's pairs keep ascending
+// order. s_hist[w][e] first counts warp w's pairs of e, then holds their next position
+// relative to offs[e]. err may be null (bad ids then only get pos = -1).
+__global__ void __launch_bounds__(1024) group_one_cta(const int32_t* __restrict__ ids, int P, int E,
+                                                      const int32_t* __restrict__ plan, Workspace ws, int tile_n,
+                                                      int32_t* __restrict__ err) {
+  extern __shared__ int s_dyn[];
+  int* s_hist = s_dyn;            // [32][E]
+  int* s_ids = s_hist + 32 * E;   // [P]
+  int* s_perm = s_ids + P;        // [P]
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  for (int i = tid; i < P; i += blockDim.x) s_ids[i] = ids[i];
+  for (int i = tid; i < 32 * E; i += blockDim.x) s_hist[i] = 0;
+  __syncthreads();
+  const int per = (P + 31) / 32;
+  const int p0 = warp * per, p1 = min(P, p0 + per);
+  int* h = s_hist + warp * E;
+  const unsigned below = (1u << lane) - 1u;
+  for (int b = p0; b < p1; b += 32) {
+    const int p = b + lane;
+    const int id = p < p1 ? s_ids[p] : -1;
+    const bool ok = p < p1 && id >= 0 && id < E;
+    if (p < p1 && !ok) {
+      ws.pos[p] = -1;
+      if (err != nullptr) atomicOr(err, kErrBadExpertId);
+    }
+    const unsigned peers = __match_any_sync(0xffffffffu, ok ? id : -1);
+    if (ok && (peers & below) == 0) h[id] += __popc(peers);
+    __syncwarp();
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += blockDim.x) {
+    int run = 0;
+    for (int w = 0; w < 32; ++w) {
+      const int v = s_hist[w * E + e];
+      s_hist[w * E + e] = run;
+      run += v;
+    }
+    ws.counts[e] = run;
+  }
+  __syncthreads();
+  offs_and_tiles(E, plan, ws, tile_n, err);
+  __syncthreads();
+  for (int b = p0; b < p1; b += 32) {
+    const int p = b + lane;
+    const int id = p < p1 ? s_ids[p] : -1;
+    const bool ok = p < p1 && id >= 0 && id < E;
+    const unsigned peers = __match_any_sync(0xffffffffu, ok ? id : -1);
+    if (ok) {
+      const int j = ws.offs[id] + h[id] + __popc(peers & below);
+      s_perm[j] = p;
+      ws.pos[p] = j;
+    }
+    __syncwarp();
+    if (ok && (peers & below) == 0) h[id] += __popc(peers);
+    __syncwarp();
+  }
+  __syncthreads();
+  const int n_valid = ws.offs[E];
+  for (int j = tid; j < n_valid; j += blockDim.x) ws.perm[j] = s_perm[j];
+}
+
 // Single CTA for small P: everything in one launch (decode). Thread e owns expert e.
 __global__ void __launch_bounds__(1024) group_small(const int32_t* __restrict__ ids, int P, int E,
                                                     const int32_t* __restrict__ plan, Workspace ws,
@@ -153,7 +227,7 @@ __global__ void __launch_bounds__(1024) group_small(const int32_t* __restrict__ 
     s_ids[p] = id;
     if (id < 0 || id >= E) {
       ws.pos[p] = -1;
-      atomicOr(err, kErrBadExpertId);
+      if (err != nullptr) atomicOr(err, kErrBadExpertId);
     }
   }
   __syncthreads();
@@ -245,12 +319,26 @@ __global__ void __launch_bounds__(256) gather_rows_fp8x2_kernel(const __nv_bfloa
 
 }  // namespace
 
+cudaError_t launch_group_one_cta(const int32_t* ids, int P, int E, const int32_t* plan, Workspace ws, int tile_n,
+                                 int32_t* err, cudaStream_t s) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    const cudaError_t e = cudaFuncSetAttribute(group_one_cta, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)(8 * (size_t)kGroupOneCtaMaxPairs + 128 * (size_t)kMaxExperts));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  group_one_cta<<<1, 1024, 8 * (size_t)P + 128 * (size_t)E, s>>>(ids, P, E, plan, ws, tile_n, err);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_group(const int32_t* ids, int P, int E, const int32_t* plan, Workspace ws, int tile_n,
                          int32_t* err, cudaStream_t s) {
   if (P <= 1024 && tile_n <= 0) {
     group_small<<<1, 1024, 0, s>>>(ids, P, E, plan, ws, err);
     return cudaGetLastError();
   }
+  if (P <= kGroupOneCtaMaxPairs) return launch_group_one_cta(ids, P, E, plan, ws, tile_n, err, s);
   const int n_chunks = (P + kChunk - 1) / kChunk;
   if ((size_t)n_chunks * E > (size_t)ws.chunk_cap) return cudaErrorInvalidValue;
   group_chunk_hist<<<n_chunks, kChunk, 0, s>>>(ids, P, E, ws.chunk_cnt, err);

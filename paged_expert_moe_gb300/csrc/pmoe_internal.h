@@ -100,6 +100,12 @@ cudaError_t launch_residency(const int32_t* ids, int n_ids, int E, int K, LayerS
                              bool pdl = false);
 cudaError_t launch_group(const int32_t* ids, int P, int E, const int32_t* plan, Workspace ws,
                          int tile_n, int32_t* err, cudaStream_t s);
+// The whole grouping in one CTA (ids, histograms and perm in shared memory), which
+// launch_group takes for 1024 < P <= kGroupOneCtaMaxPairs (and P <= 1024 with tiles);
+// beyond it, four launches over per-chunk histograms (ws.chunk_cnt).
+constexpr int kGroupOneCtaMaxPairs = 8192;
+cudaError_t launch_group_one_cta(const int32_t* ids, int P, int E, const int32_t* plan, Workspace ws, int tile_n,
+                                 int32_t* err, cudaStream_t s);
 cudaError_t launch_gather_rows(const __nv_bfloat16* x, const int32_t* perm, int P, int top_k, int H,
                                __nv_bfloat16* x_perm, cudaStream_t s);
 cudaError_t launch_gather_rows_fp8x2(const __nv_bfloat16* x, const int32_t* perm, int P, int top_k, int H,
