@@ -643,8 +643,10 @@ __global__ void __launch_bounds__(TcCfg<FMT, NMAX>::kThreads, 1)
 // ---------------------------------------------------------------- block-FP8 on kind::f8f6f4
 //
 // The e4m3 weight tiles go from TMA straight to the tensor cores. The activations come as
-// two e4m3 planes on power-of-two scales (fp8_planes.cuh), so a K step is two FP8 MMAs
-// (hi, then lo) into one accumulator: the cost of one bf16 MMA. The weights' 128x128 block
+// two e4m3 planes on power-of-two scales (fp8_planes.cuh), and a K step multiplies both:
+// gate/up stacks them as one operand of 2N rows (one MMA; the hi and lo columns of the
+// partial are added in the promotion), down issues two MMAs (hi, then lo) into one
+// partial. Either way it costs what one bf16 MMA costs. The weights' 128x128 block
 // scale changes every 128 K and the h scales every 64 K, so the MMAs accumulate one K unit
 // (gate/up: a 128-K stage; down: half a stage) per TMEM partial buffer, and promotion
 // warps fold each partial into fp32 registers:
@@ -661,6 +663,11 @@ __global__ void __launch_bounds__(TcCfg<FMT, NMAX>::kThreads, 1)
 // Warps: 0 TMA weights, 1 MMA issuer (owns the TMEM), 2-5 and 6-9 promotion groups 0 and 1
 // (TMEM lanes 32*(warp%4)..), 10 TMA activation planes.
 struct F8Cfg {
+  // TMEM partial buffers per group: gate/up stacks the hi and lo planes as one 2N-row
+  // operand (one MMA per K step, 2 x 128 columns); down keeps them apart (two MMAs per
+  // K step into 4 x 64 columns: it has two K units per stage)
+  template <bool GATEUP> static constexpr int kParts = GATEUP ? 2 : 4;
+  template <bool GATEUP> static constexpr int kPartCols = GATEUP ? 128 : 64;
   static constexpr int kN = 64;                   // pairs per tile (MMA N at most)
   static constexpr int kBK = 128;                 // K per stage (one byte each)
   static constexpr int kWBytes = 128 * kBK;       // weight tile, 128 rows
@@ -673,12 +680,11 @@ struct F8Cfg {
   static constexpr int kRingStages = (220 * 1024 - kFixedBytes) / kWBytes;  // 16 KB each
   static constexpr int kXStages = 4;
   static constexpr int kWStages = kRingStages - kXStages;
-  static constexpr int kParts = 4;                // partial buffers per group
-  static constexpr int kTmemCols = 2 * kParts * kN;
+  static constexpr int kTmemCols = 512;           // 2 groups x (4 x 64 or 2 x 128 columns)
   static constexpr int kSmemBytes = (kWStages + kXStages) * kWBytes + kFixedBytes;
   static constexpr int kGroupThreads = 128;
   static constexpr int kThreads = 352;
-  static_assert(kWBytes == kXBytes && kWStages >= 6 && kSmemBytes <= 227 * 1024 && kTmemCols <= 512, "fp8 tiles");
+  static_assert(kWBytes == kXBytes && kWStages >= 6 && kSmemBytes <= 227 * 1024, "fp8 tiles");
 };
 
 // Named barriers of the two promotion groups (ids 1 and 2, 128 threads each).
@@ -717,6 +723,7 @@ __global__ void __launch_bounds__(F8Cfg::kThreads, 1)
   constexpr int kN = C::kN;
   constexpr int kUnits = GATEUP ? 1 : 2;  // partial buffers per stage
   constexpr int kSteps = 4 / kUnits;      // K = 32 MMA steps per unit
+  constexpr int kParts = C::template kParts<GATEUP>, kPartCols = C::template kPartCols<GATEUP>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* wring = smem;
@@ -729,8 +736,8 @@ __global__ void __launch_bounds__(F8Cfg::kThreads, 1)
   uint64_t* xfull = wempty + C::kWStages;
   uint64_t* xempty = xfull + C::kXStages;
   uint64_t* pfull = xempty + C::kXStages;     // [2][kParts] partial buffer written by the MMAs
-  uint64_t* pempty = pfull + 2 * C::kParts;  // [2][kParts] partial buffer read by its group
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(pempty + 2 * C::kParts);
+  uint64_t* pempty = pfull + 2 * kParts;  // [2][kParts] partial buffer read by its group
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(pempty + 2 * kParts);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -753,7 +760,7 @@ __global__ void __launch_bounds__(F8Cfg::kThreads, 1)
       mbar_init(&xfull[s], 1);
       mbar_init(&xempty[s], 1);
     }
-    for (int r = 0; r < 2 * C::kParts; ++r) {
+    for (int r = 0; r < 2 * kParts; ++r) {
       mbar_init(&pfull[r], 1);
       mbar_init(&pempty[r], C::kGroupThreads);
     }
@@ -803,11 +810,21 @@ __global__ void __launch_bounds__(F8Cfg::kThreads, 1)
               tma_load_3d(st, &map_w, &fullb[s], kb * C::kBK, mt * 128, slot);
             }
           } else {
-            mbar_arrive_expect_tx(&fullb[s], (uint32_t)(2 * nb * kTileRowsB * C::kBK));
-            for (int pl = 0; pl < 2; ++pl)
-              for (int b = 0; b < nb; ++b)
-                tma_load_3d(st + pl * C::kPlaneBytes + b * kTileRowsB * C::kBK, &map_b, &fullb[s], kb * C::kBK,
-                            pstart + b * kTileRowsB, pl);
+            if (GATEUP) {
+              // hi rows 0..n16-1, then the lo rows: one B operand of 2 n16 rows (16-row boxes)
+              const int n16 = (np + 15) & ~15;
+              mbar_arrive_expect_tx(&fullb[s], (uint32_t)(2 * n16 * C::kBK));
+              for (int pl = 0; pl < 2; ++pl)
+                for (int b = 0; b < n16; b += 16)
+                  tma_load_3d(st + (pl * n16 + b) * C::kBK, &map_b, &fullb[s], kb * C::kBK, pstart + b, pl);
+            } else {
+              // the two planes kPlaneBytes apart (32-row boxes)
+              mbar_arrive_expect_tx(&fullb[s], (uint32_t)(2 * nb * kTileRowsB * C::kBK));
+              for (int pl = 0; pl < 2; ++pl)
+                for (int b = 0; b < nb; ++b)
+                  tma_load_3d(st + pl * C::kPlaneBytes + b * kTileRowsB * C::kBK, &map_b, &fullb[s], kb * C::kBK,
+                              pstart + b * kTileRowsB, pl);
+            }
           }
           if (++s == depth) {
             s = 0;
@@ -839,7 +856,7 @@ __global__ void __launch_bounds__(F8Cfg::kThreads, 1)
         const int tile = t0 + item / m_tiles;
         const int np = ws.tiles[3 * tile + 2];
         const int n_mma = (np + 15) & ~15;
-        const uint32_t idesc = idesc_e4m3(128, n_mma < 16 ? 16 : n_mma);
+        const uint32_t idesc = idesc_e4m3(128, (GATEUP ? 2 : 1) * (n_mma < 16 ? 16 : n_mma));
         for (int kb = 0; kb < n_kb; ++kb) {
           if (!mbar_wait(&wfull[sw], wph, abort_flag, err) || !mbar_wait(&xfull[sx], xph, abort_flag, err)) {
             ok = false;
@@ -851,21 +868,21 @@ __global__ void __launch_bounds__(F8Cfg::kThreads, 1)
           for (int u = 0; u < kUnits; ++u) {
             int rr = g ? r1 : r0;
             uint32_t rp = g ? rph1 : rph0;
-            const int pb = g * C::kParts + rr;
+            const int pb = g * kParts + rr;
             if (!mbar_wait(&pempty[pb], rp ^ 1u, abort_flag, err)) {
               ok = false;
               break;
             }
             fence_after();
-            const uint32_t d = tmem + (uint32_t)(pb * kN);
+            const uint32_t d = tmem + (uint32_t)(pb * kPartCols);
 #pragma unroll
             for (int j = 0; j < kSteps; ++j) {
               const uint32_t ko = (uint32_t)((u * kSteps + j) * 32);
               mma_e4m3(d, sw128_desc(a0 + ko), sw128_desc(bh + ko), idesc, j > 0 ? 1u : 0u);
-              mma_e4m3(d, sw128_desc(a0 + ko), sw128_desc(bl + ko), idesc, 1u);
+              if (!GATEUP) mma_e4m3(d, sw128_desc(a0 + ko), sw128_desc(bl + ko), idesc, 1u);
             }
             mma_commit(&pfull[pb]);
-            if (++rr == C::kParts) {
+            if (++rr == kParts) {
               rr = 0;
               rp ^= 1u;
             }
@@ -935,7 +952,7 @@ __global__ void __launch_bounds__(F8Cfg::kThreads, 1)
             }
             grp_bar(g);
           }
-          const int pb = g * C::kParts + r;
+          const int pb = g * kParts + r;
           // tcgen05.ld is warp-collective: the warp goes on only if all its lanes' waits did
           const bool got = __all_sync(0xffffffffu, !bad && mbar_wait(&pfull[pb], rph, abort_flag, err));
           if (!got) bad = true;
@@ -947,18 +964,26 @@ __global__ void __launch_bounds__(F8Cfg::kThreads, 1)
             for (int h2 = 0; h2 < 2; ++h2) {
               if (h2 == 0 || n_mma > 32) {
                 uint32_t v[32];
-                tmem_ld32(tmem + tlane + (uint32_t)(pb * kN + 32 * h2), v);
-                tmem_wait_ld();
+                tmem_ld32(tmem + tlane + (uint32_t)(pb * kPartCols + 32 * h2), v);
+                if (GATEUP) {
+                  uint32_t u[32];  // the lo plane's columns, n_mma after the hi plane's
+                  tmem_ld32(tmem + tlane + (uint32_t)(pb * kPartCols + n_mma + 32 * h2), u);
+                  tmem_wait_ld();
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                  acc[32 * h2 + i] =
-                      fmaf(__uint_as_float(v[i]), GATEUP ? sw : sw * hs[32 * h2 + i], acc[32 * h2 + i]);
+                  for (int i = 0; i < 32; ++i)
+                    acc[32 * h2 + i] = fmaf(__uint_as_float(v[i]) + __uint_as_float(u[i]), sw, acc[32 * h2 + i]);
+                } else {
+                  tmem_wait_ld();
+#pragma unroll
+                  for (int i = 0; i < 32; ++i)
+                    acc[32 * h2 + i] = fmaf(__uint_as_float(v[i]), sw * hs[32 * h2 + i], acc[32 * h2 + i]);
+                }
               }
             }
           }
           fence_before();
           mbar_arrive(&pempty[pb]);
-          if (++r == C::kParts) {
+          if (++r == kParts) {
             r = 0;
             rph ^= 1u;
           }
@@ -1162,7 +1187,7 @@ int tc_make_act_maps(int fmt, __nv_bfloat16* x_perm, __nv_bfloat16* h, size_t P,
     {
       const cuuint64_t dims[3] = {(cuuint64_t)H, (cuuint64_t)P, 2};
       const cuuint64_t strides[2] = {(cuuint64_t)H, (cuuint64_t)H * P};
-      const cuuint32_t box[3] = {128, (cuuint32_t)kTileRowsB, 1};
+      const cuuint32_t box[3] = {128, 16, 1};
       if (encode(&out->x8, x_perm, 3, dims, strides, box, kMapBytesSw128) != PMOE_OK) return PMOE_ECUDA;
     }
     const cuuint64_t dims[3] = {(cuuint64_t)I, (cuuint64_t)P, 2};
