@@ -30,14 +30,26 @@ layout contract, independently of the CUDA code:
       X_gu  u8 [2I][H/32]  E8M0 scale per output row and block of 32 inputs
       X_d   u8 [H][I/32]
       w[n, c] = e2m1(q[n, c]) * 2^(X[n, c//32] - 127)
+  NVFP4 (format 4), H and I multiples of 128; two-level scaling: 16 inputs share one
+  e4m3 block scale, and each matrix has one fp32 tensor scale (gate_proj and up_proj,
+  stored as one fused matrix, share theirs). The pages name NVFP4 among the formats of
+  section "What does Paged Experts actually do?" (PR #45787) without its layout; this
+  is the two-level encoding the name stands for.
+      Q_gu  u8 [2I][H/2]   FP4 E2M1 codes, element c of a row: byte c//2, low nibble if c even
+      Q_d   u8 [H][I/2]
+      T_gu  fp32, then 12 bytes of padding
+      B_gu  u8 [2I][H/16]  e4m3 block scale per output row and block of 16 inputs
+      T_d   fp32, then 12 bytes of padding
+      B_d   u8 [H][I/16]
+      w[n, c] = e2m1(q[n, c]) * e4m3(B[n, c//16]) * T
 
-All sections are packed back to back in the order listed, with no padding.
+All sections are packed back to back in the order listed, with no other padding.
 TEST INFRASTRUCTURE ONLY (see the package docstring).
 """
 
 import numpy as np
 
-BF16, FP8_BLOCK128, INT4_GPTQ_G128, MXFP4 = 0, 1, 2, 3
+BF16, FP8_BLOCK128, INT4_GPTQ_G128, MXFP4, NVFP4 = 0, 1, 2, 3, 4
 
 
 def expert_nbytes(fmt, H, I):
@@ -51,6 +63,8 @@ def expert_nbytes(fmt, H, I):
         return n_w // 2 + 4 * ((2 * I) * (H // 128) + H * (I // 128))
     if fmt == MXFP4:
         return n_w // 2 + (2 * I) * (H // 32) + H * (I // 32)
+    if fmt == NVFP4:
+        return n_w // 2 + 16 + (2 * I) * (H // 16) + 16 + H * (I // 16)
     raise ValueError("unknown format")
 
 
@@ -145,6 +159,15 @@ def decode_expert(buf, fmt, H, I):
         xd, off = _take(buf, off, H * (I // 32))
         Wgu = _mxfp4_rows(qgu, xgu, 2 * I, H)
         Wd = _mxfp4_rows(qd, xd, H, I)
+    elif fmt == NVFP4:
+        qgu, off = _take(buf, off, I * H)
+        qd, off = _take(buf, off, H * I // 2)
+        tgu, off = _take(buf, off, 16)
+        bgu, off = _take(buf, off, 2 * I * (H // 16))
+        td, off = _take(buf, off, 16)
+        bd, off = _take(buf, off, H * (I // 16))
+        Wgu = _nvfp4_rows(qgu, bgu, tgu, 2 * I, H)
+        Wd = _nvfp4_rows(qd, bd, td, H, I)
     else:
         raise ValueError("unknown format")
     if off != buf.size:
@@ -172,3 +195,15 @@ def _mxfp4_rows(qbytes, xbytes, n_rows, n_cols):
     codes[:, 1::2] = q >> 4
     x = E8M0_TABLE[xbytes.reshape(n_rows, n_cols // 32)]
     return E2M1_TABLE[codes] * np.repeat(x, 32, axis=1)
+
+
+def _nvfp4_rows(qbytes, bbytes, tbytes, n_rows, n_cols):
+    """NVFP4 rows: E2M1 nibbles (low first), one e4m3 scale per (row, block of 16), and
+    the matrix's fp32 tensor scale (the first 4 of its 16 bytes)."""
+    q = qbytes.reshape(n_rows, n_cols // 2)
+    codes = np.empty((n_rows, n_cols), dtype=np.uint8)
+    codes[:, 0::2] = q & 0x0F
+    codes[:, 1::2] = q >> 4
+    b = E4M3_TABLE[bbytes.reshape(n_rows, n_cols // 16)]
+    t = float(tbytes[:4].view(np.float32)[0])
+    return E2M1_TABLE[codes] * np.repeat(b, 16, axis=1) * t

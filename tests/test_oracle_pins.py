@@ -215,7 +215,10 @@ def test_expert_sizes_match_the_layout_closed_forms():
     assert formats.expert_nbytes(2, H, I) == 2_506_752  # packed nibbles + 36,864 x (fp16 s, fp16 z)
     # "FP8 is about 4.72 MB (3 x 2048 x 768 weights at one byte, scales ignored)"
     assert 3 * H * I == 4_718_592
-    for f in (0, 1, 2):
+    # NVFP4: packed codes, then per matrix 16 bytes (fp32 tensor scale + padding) and one
+    # e4m3 byte per row and 16 inputs
+    assert formats.expert_nbytes(4, H, I) == 2_359_296 + 16 + 196_608 + 16 + 98_304 == 2_654_240
+    for f in (0, 1, 2, 3, 4):
         assert formats.expert_nbytes(f, H, I) == gen.expert_nbytes(f, H, I)
 
 
@@ -372,6 +375,56 @@ def test_mxfp4_generator_error_bound():
     assert (got[sat] == np.sign(wgu[sat]) * 6 * X[sat]).all()
     half_step = np.where(a < 2 * X, 0.25 * X, np.where(a < 4 * X, 0.5 * X, X))
     assert (np.abs(got - wgu)[~sat] <= half_step[~sat] * 1.0001).all()
+
+
+def test_nvfp4_nibble_order_and_two_level_scales():
+    """Hand-built NVFP4 expert. Codes: 0x32 = codes 2 (low, 1.0) then 3 (high, 1.5); 0xF9 =
+    codes 9 (-0.5) then 15 (-6); 0x07 = code 7 (6) then 0; 0x70 = 0 then 6. Block scales
+    (e4m3): 0x38 = 1.0, 0x40 = 2.0, 0x3C = 1.5, 0x01 = 2^-9 (the smallest subnormal).
+    Tensor scales: 0.5 for gate/up, 2.0 for down. One block scale per row and 16 inputs."""
+    H, I = 128, 128
+    qgu = np.zeros((2 * I, H // 2), np.uint8)
+    qgu[0, 0] = 0x32
+    qgu[5, 8] = 0xF9          # row 5: element 16 = -0.5, element 17 = -6 (block 1)
+    qgu[I + 3, 0] = 0x07      # up row 3: element 0 = 6
+    qd = np.zeros((H, I // 2), np.uint8)
+    qd[4, 63] = 0x70          # row 4: element 126 = 0, element 127 = 6 (block 7)
+    bgu = np.full((2 * I, H // 16), 0x38, np.uint8)
+    bgu[5, 1] = 0x40
+    bgu[I + 3, 0] = 0x01
+    bd = np.full((H, I // 16), 0x38, np.uint8)
+    bd[4, 7] = 0x3C
+    t = lambda v: np.concatenate([np.array([v], np.float32).view(np.uint8), np.zeros(12, np.uint8)])
+    buf = np.concatenate([qgu.ravel(), qd.ravel(), t(0.5), bgu.ravel(), t(2.0), bd.ravel()])
+    Wg, Wu, Wd = formats.decode_expert(buf, 4, H, I)
+    assert Wg[0, 0] == 0.5 and Wg[0, 1] == 0.75 and Wg[0, 2] == 0.0
+    assert Wg[5, 16] == -0.5 and Wg[5, 17] == -6.0 and Wg[5, 15] == 0.0
+    assert Wu[3, 0] == 6.0 * 2.0 ** -10 and Wu[3, 1] == 0.0
+    assert Wd[4, 127] == 18.0 and Wd[4, 126] == 0.0
+    assert np.count_nonzero(Wg) == 4 and np.count_nonzero(Wu) == 1 and np.count_nonzero(Wd) == 1
+
+
+def test_nvfp4_generator_error_bound():
+    """T = amax / (6 * 448). Per block of 16 with s = e4m3(block scale) * T: an element below
+    6s is off by at most half a grid step (s/4 below 2s, s/2 below 4s, s below 6s) and one at
+    or above 6s becomes +-6s. No block scale exceeds 448."""
+    H, I = 256, 128
+    rng = np.random.default_rng([15, 0, 0, 4])
+    wgu = rng.standard_normal((2 * I, H), dtype=np.float32) * np.float32(0.02)
+    buf = gen.expert_bytes(4, H, I, 15)
+    Wg, Wu, _ = formats.decode_expert(buf, 4, H, I)
+    got = np.concatenate([Wg, Wu])
+    off = 3 * H * I // 2
+    T = float(buf[off:off + 4].view(np.float32)[0])
+    assert T == float(np.float32(np.abs(wgu).max() / (6.0 * 448.0)))
+    b = formats.E4M3_TABLE[buf[off + 16:off + 16 + 2 * I * H // 16]].reshape(2 * I, H // 16)
+    assert b.max() <= 448.0 and b.min() >= 0.0
+    s_eff = np.repeat(b * T, 16, axis=1)
+    a = np.abs(wgu)
+    sat = a >= 6 * s_eff
+    assert (got[sat] == np.sign(wgu[sat]) * 6 * s_eff[sat]).all()
+    half_step = np.where(a < 2 * s_eff, 0.25 * s_eff, np.where(a < 4 * s_eff, 0.5 * s_eff, s_eff))
+    assert (np.abs(got - wgu)[~sat] <= half_step[~sat] * 1.0001 + 1e-12).all()
 
 
 def test_bf16_decode_matches_torch_bfloat16():

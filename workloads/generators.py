@@ -98,6 +98,8 @@ def expert_nbytes(fmt, H, I):
         return n_w // 2 + 4 * ((2 * I) * (H // 128) + H * (I // 128))
     if fmt == 3:
         return n_w // 2 + (2 * I) * (H // 32) + H * (I // 32)
+    if fmt == 4:
+        return n_w // 2 + 16 + (2 * I) * (H // 16) + 16 + H * (I // 16)
     raise ValueError("unknown format")
 
 
@@ -168,6 +170,38 @@ def _mxfp4_block_quant(w):
     return packed, (e + 127).astype(np.uint8)
 
 
+def _nvfp4_quant(w):
+    """[R, C] float32 -> (packed E2M1 codes [R, C/2] uint8, e4m3 block scales [R, C/16]
+    uint8, fp32 tensor scale T).
+
+    Two-level recipe: T = amax(w) / (6 * 448), so that the largest block scale is
+    e4m3's largest value; per (row, block of 16 columns) the scale code is
+    e4m3(amax_block / 6 / T) (round to nearest even, saturating at 448); each element
+    divided by e4m3(code) * T and rounded to the nearest E2M1 value, ties to the even
+    mantissa, saturating at 6. A block whose scale rounds to zero gets zero codes.
+    """
+    R, C = w.shape
+    amax = float(np.abs(w).max())
+    T = np.float32(amax / (6.0 * 448.0)) if amax > 0 else np.float32(1.0)
+    g = w.reshape(R, C // 16, 16).astype(np.float32)
+    bamax = np.abs(g).max(axis=2)
+    s_codes = _e4m3_codes(np.minimum(bamax / np.float32(6.0) / T, np.float32(448.0)))
+    import torch
+    s_vals = torch.from_numpy(s_codes.copy()).view(torch.float8_e4m3fn).to(torch.float32).numpy()
+    eff = (s_vals * T).astype(np.float32)
+    a = np.where(eff[:, :, None] > 0, np.abs(g) / np.where(eff > 0, eff, 1.0)[:, :, None], 0.0)
+    lo = np.searchsorted(_E2M1_MIDS, a, side="left")
+    hi = np.searchsorted(_E2M1_MIDS, a, side="right")
+    idx = np.where(lo == hi, lo, np.where(lo % 2 == 0, lo, hi))  # on a midpoint: the even code
+    codes = (idx | np.where(g < 0, 8, 0)).astype(np.uint8).reshape(R, C)
+    packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+    return packed, s_codes.reshape(R, C // 16), T
+
+
+def _tensor_scale_bytes(T):
+    return np.concatenate([np.array([T], np.float32).view(np.uint8), np.zeros(12, np.uint8)])
+
+
 def expert_bytes(fmt, H, I, seed, layer=0, expert=0, std=0.02):
     """One expert in the byte layout of `fmt`, drawn from N(0, std) master weights.
 
@@ -191,6 +225,10 @@ def expert_bytes(fmt, H, I, seed, layer=0, expert=0, std=0.02):
         qgu, xgu = _mxfp4_block_quant(wgu)
         qd, xd = _mxfp4_block_quant(wd)
         parts = [qgu.ravel(), qd.ravel(), xgu.ravel(), xd.ravel()]
+    elif fmt == 4:
+        qgu, bgu, tgu = _nvfp4_quant(wgu)
+        qd, bd, td = _nvfp4_quant(wd)
+        parts = [qgu.ravel(), qd.ravel(), _tensor_scale_bytes(tgu), bgu.ravel(), _tensor_scale_bytes(td), bd.ravel()]
     else:
         raise ValueError("unknown format")
     out = np.concatenate(parts)
