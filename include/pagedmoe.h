@@ -52,7 +52,15 @@
  *                        does Paged Experts actually do?", PR #45787). E2M1 times an
  *                        E8M0 scale is exact in bf16 (scales 2^-126 .. 2^125), so the
  *                        prefill path dequantises these weights without rounding.
- * FP8, int4 and MXFP4 need H and I multiples of 128; bf16 needs multiples of 8 (and,
+ *   PMOE_NVFP4           Q_gu u8 [2I][H/2], Q_d u8 [H][I/2] (FP4 E2M1 codes, as MXFP4),
+ *                        then T_gu fp32 + 12 bytes of padding, B_gu e4m3 [2I][H/16],
+ *                        then T_d fp32 + 12 bytes of padding, B_d e4m3 [H][I/16]
+ *                        (one e4m3 scale per output row and block of 16 inputs; one
+ *                        fp32 tensor scale per matrix, gate and up sharing theirs);
+ *                        w = e2m1(q) * e4m3(B) * T (the two-level NVFP4 encoding; the
+ *                        formats of PR #45787). E2M1 times an e4m3 scale is exact in
+ *                        bf16; T is applied in fp32.
+ * FP8, int4, MXFP4 and NVFP4 need H and I multiples of 128; bf16 needs multiples of 8 (and,
  * for the tensor-core prefill path, H a multiple of 128 and I of 128).
  *
  * Activations x, residual and y are bf16 [T][H] row-major; router logits fp32
@@ -89,7 +97,8 @@ typedef enum {
   PMOE_BF16 = 0,
   PMOE_FP8_BLOCK128 = 1,
   PMOE_INT4_GPTQ_G128 = 2,
-  PMOE_MXFP4 = 3
+  PMOE_MXFP4 = 3,
+  PMOE_NVFP4 = 4
 } pmoe_format;
 
 typedef enum {

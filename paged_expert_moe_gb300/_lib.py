@@ -16,7 +16,7 @@ LIB_PATH = os.path.join(HERE, "libpagedmoe.so")
 
 PMOE_OK, PMOE_EINVAL, PMOE_ENOMEM, PMOE_EHOSTALLOC, PMOE_ECUDA, PMOE_EUNSUPPORTED, PMOE_ETIMEOUT, PMOE_EDEVICE = \
     0, -1, -2, -3, -4, -5, -6, -7
-PMOE_BF16, PMOE_FP8_BLOCK128, PMOE_INT4_GPTQ_G128, PMOE_MXFP4 = 0, 1, 2, 3
+PMOE_BF16, PMOE_FP8_BLOCK128, PMOE_INT4_GPTQ_G128, PMOE_MXFP4, PMOE_NVFP4 = 0, 1, 2, 3, 4
 PMOE_PAGEIN_COPY_ENGINE, PMOE_PAGEIN_SM_PULL = 0, 1
 
 

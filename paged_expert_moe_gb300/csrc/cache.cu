@@ -94,7 +94,8 @@ bool stream_capturing(cudaStream_t s) {
 
 int validate_shape(int fmt, int H, int I) {
   if (H <= 0 || I <= 0 || H % 8 != 0 || I % 8 != 0) return PMOE_EINVAL;
-  if (fmt != PMOE_BF16 && fmt != PMOE_FP8_BLOCK128 && fmt != PMOE_INT4_GPTQ_G128 && fmt != PMOE_MXFP4)
+  if (fmt != PMOE_BF16 && fmt != PMOE_FP8_BLOCK128 && fmt != PMOE_INT4_GPTQ_G128 && fmt != PMOE_MXFP4 &&
+      fmt != PMOE_NVFP4)
     return PMOE_EUNSUPPORTED;
   if (fmt != PMOE_BF16 && (H % 128 != 0 || I % 128 != 0)) return PMOE_EUNSUPPORTED;
   // decode kernels hold a row in registers: H <= 4096 (bf16) / 4096 (fp8, int4), I <= 1536

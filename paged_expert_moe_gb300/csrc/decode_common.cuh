@@ -43,16 +43,25 @@ template <> struct Fmt<PMOE_BF16> { static constexpr int EPC = 8; static constex
 template <> struct Fmt<PMOE_FP8_BLOCK128> { static constexpr int EPC = 16; static constexpr int BPE2 = 2; };
 template <> struct Fmt<PMOE_INT4_GPTQ_G128> { static constexpr int EPC = 32; static constexpr int BPE2 = 1; };
 template <> struct Fmt<PMOE_MXFP4> { static constexpr int EPC = 32; static constexpr int BPE2 = 1; };
+template <> struct Fmt<PMOE_NVFP4> { static constexpr int EPC = 32; static constexpr int BPE2 = 1; };
 
 // E8M0 scale byte -> 2^(b - 127) as fp32 (b = 0 is the subnormal 2^-127)
 __device__ __forceinline__ float e8m0_f32(uint32_t b) {
   return b ? __uint_as_float(b << 23) : __uint_as_float(0x00400000u);
 }
 
-// Per-chunk dequantisation parameters of row `row` (of a [rows][cols] matrix), chunk `c`.
+// Per-chunk dequantisation parameters of row `row` (of a [rows][cols] matrix), chunk `c`:
+// the scale s and the zero point z (int4), or, for NVFP4, the scales of the chunk's two
+// blocks of 16 (s, then z), each times the matrix's tensor scale.
 struct ChunkQ {
   float s, z;
 };
+
+// e4m3 code -> fp32 (exact)
+__device__ __forceinline__ float e4m3_f32(uint32_t b) {
+  const __half_raw h = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)b, __NV_E4M3);
+  return __half2float(*reinterpret_cast<const __half*>(&h));
+}
 
 // COHERENT: the scales may have been written earlier in the same launch (an expert the
 // launch pages in itself), so they are read through L2 rather than the read-only path.
@@ -76,6 +85,21 @@ __device__ __forceinline__ ChunkQ chunk_q(const uint8_t* scales, int row, int c,
       b = __ldg(X);
     }
     q.s = e8m0_f32(b);
+  } else if constexpr (FMT == PMOE_NVFP4) {
+    // the matrix's scale section: fp32 tensor scale, 12 bytes of padding, then one e4m3
+    // byte per row and block of 16 inputs (chunk c holds blocks 2c and 2c + 1)
+    const uint16_t* B = reinterpret_cast<const uint16_t*>(scales + 16 + (size_t)row * (cols >> 4)) + c;
+    uint32_t b;
+    float t;
+    if constexpr (COHERENT) {
+      asm volatile("ld.global.cg.u16 %0, [%1];" : "=r"(b) : "l"(B));
+      asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(t) : "l"(scales));
+    } else {
+      b = __ldg(B);
+      t = __ldg(reinterpret_cast<const float*>(scales));
+    }
+    q.s = e4m3_f32(b & 0xffu) * t;
+    q.z = e4m3_f32(b >> 8) * t;
   } else if constexpr (FMT == PMOE_INT4_GPTQ_G128) {
     const __half2* SZ = reinterpret_cast<const __half2*>(scales) + (size_t)row * (cols >> 7) + ((c * 32) >> 7);
     uint32_t raw;
@@ -151,6 +175,24 @@ __device__ __forceinline__ float chunk_dot(uint4 w, const uint4* av, ChunkQ q) {
       }
     }
     return acc * q.s;
+  } else if constexpr (FMT == PMOE_NVFP4) {
+    // E2M1 codes as MXFP4, two blocks of 16: words 0-1 (scale s) and 2-3 (scale z)
+    const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+    float acc[2] = {0.f, 0.f};
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      const uint4 a = load_act<FMT, SRC>(av + h);
+      const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
+      const uint32_t word = wv[h];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const __half2_raw pr = __nv_cvt_fp4x2_to_halfraw2((__nv_fp4x2_storage_t)((word >> (8 * k)) & 0xffu), __NV_E2M1);
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&pr));
+        acc[h >> 1] = fmaf(f.x, bf_lo(aw[k]), acc[h >> 1]);
+        acc[h >> 1] = fmaf(f.y, bf_hi(aw[k]), acc[h >> 1]);
+      }
+    }
+    return acc[0] * q.s + acc[1] * q.z;
   } else {
     const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
     float acc = 0.f;

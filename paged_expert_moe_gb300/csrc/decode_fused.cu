@@ -745,6 +745,8 @@ struct DfGeom {
 };
 
 bool df_geometry(int fmt, int T, int top_k, int H, int I, int G, DfGeom* g) {
+  // formats the fused kernel streams (NVFP4 decodes through the GEMV kernels)
+  if (fmt != PMOE_BF16 && fmt != PMOE_FP8_BLOCK128 && fmt != PMOE_INT4_GPTQ_G128 && fmt != PMOE_MXFP4) return false;
   if (T < 1 || T * top_k > kDfMaxPairs || G < 1 || G > 1024 || H % 8 != 0 || I % 8 != 0) return false;
   if (H >= (1 << 20) || I >= (1 << 20)) return false;  // the schedule's 32-bit products
   const size_t rbg = fmt_row_bytes(fmt, H), rbd = fmt_row_bytes(fmt, I);

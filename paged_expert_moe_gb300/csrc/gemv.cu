@@ -267,6 +267,14 @@ ExpertLayout expert_layout(int fmt, int H, int I) {
     l.gu_s = l.d_w + n_d / 2;
     l.d_s = l.gu_s + (size_t)(2 * I) * (H / 32);  // one E8M0 byte per row and 32 inputs
     l.bytes = l.d_s + (size_t)H * (I / 32);
+  } else if (fmt == PMOE_NVFP4) {
+    // each scale section: fp32 tensor scale, 12 bytes of padding, one e4m3 byte per row
+    // and block of 16 inputs
+    l.gu_w = 0;
+    l.d_w = n_gu / 2;
+    l.gu_s = l.d_w + n_d / 2;
+    l.d_s = l.gu_s + 16 + (size_t)(2 * I) * (H / 16);
+    l.bytes = l.d_s + 16 + (size_t)H * (I / 16);
   } else {
     l.gu_w = 0;
     l.d_w = n_gu / 2;
@@ -299,6 +307,10 @@ cudaError_t launch_gemv_gateup(int fmt, const __nv_bfloat16* x, int T, int top_k
     const int nch = H / 32;
     if (nch <= 32 * 2) return gateup_t<PMOE_MXFP4, 2, 4>(x, T, top_k, H, I, plan, E, wave, ws, arena, stride, lay, grid, s);
     if (nch <= 32 * 4) return gateup_t<PMOE_MXFP4, 4, 4>(x, T, top_k, H, I, plan, E, wave, ws, arena, stride, lay, grid, s);
+  } else if (fmt == PMOE_NVFP4) {
+    const int nch = H / 32;
+    if (nch <= 32 * 2) return gateup_t<PMOE_NVFP4, 2, 4>(x, T, top_k, H, I, plan, E, wave, ws, arena, stride, lay, grid, s);
+    if (nch <= 32 * 4) return gateup_t<PMOE_NVFP4, 4, 4>(x, T, top_k, H, I, plan, E, wave, ws, arena, stride, lay, grid, s);
   }
   return cudaErrorInvalidValue;
 }
@@ -324,6 +336,10 @@ cudaError_t launch_gemv_down(int fmt, int H, int I, const int32_t* plan, int E, 
     const int nch = I / 32;
     if (nch <= 32 * 1) return down_t<PMOE_MXFP4, 1, 8>(H, I, plan, E, wave, ws, arena, stride, lay, grid, s);
     if (nch <= 32 * 2) return down_t<PMOE_MXFP4, 2, 4>(H, I, plan, E, wave, ws, arena, stride, lay, grid, s);
+  } else if (fmt == PMOE_NVFP4) {
+    const int nch = I / 32;
+    if (nch <= 32 * 1) return down_t<PMOE_NVFP4, 1, 8>(H, I, plan, E, wave, ws, arena, stride, lay, grid, s);
+    if (nch <= 32 * 2) return down_t<PMOE_NVFP4, 2, 4>(H, I, plan, E, wave, ws, arena, stride, lay, grid, s);
   }
   return cudaErrorInvalidValue;
 }

@@ -172,7 +172,8 @@ extern "C" int moe_decode_forward_noalloc(const void* experts, size_t stride, in
   if (E < 1 || E > kMaxExperts || top_k < 1 || top_k > E || T < 0 || T > kGemvMaxTokens) return PMOE_EINVAL;
   if (n_slots < 1 || (slot_of == nullptr && n_slots < E)) return PMOE_EINVAL;
   if (H <= 0 || I <= 0 || H % 8 != 0 || I % 8 != 0 || H > 4096 || I > 1536) return PMOE_EINVAL;
-  if (format != PMOE_BF16 && format != PMOE_FP8_BLOCK128 && format != PMOE_INT4_GPTQ_G128 && format != PMOE_MXFP4)
+  if (format != PMOE_BF16 && format != PMOE_FP8_BLOCK128 && format != PMOE_INT4_GPTQ_G128 && format != PMOE_MXFP4 &&
+      format != PMOE_NVFP4)
     return PMOE_EUNSUPPORTED;
   if (format != PMOE_BF16 && (H % 128 != 0 || I % 128 != 0)) return PMOE_EUNSUPPORTED;
   const ExpertLayout lay = expert_layout(format, H, I);

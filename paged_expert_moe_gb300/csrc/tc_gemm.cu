@@ -172,7 +172,8 @@ struct TcCfg {
   static constexpr int kBBytes = NMAX * kBK * 2;           // bf16 B tile (up to NMAX pairs)
   // quantised A tile as loaded by TMA, before the converter warps dequantise it
   static constexpr int kQBytes = FMT == PMOE_FP8_BLOCK128                           ? 128 * kBK
-                                 : (FMT == PMOE_INT4_GPTQ_G128 || FMT == PMOE_MXFP4) ? 128 * kBK / 2
+                                 : (FMT == PMOE_INT4_GPTQ_G128 || FMT == PMOE_MXFP4 || FMT == PMOE_NVFP4)
+                                     ? 128 * kBK / 2
                                                                                      : 0;
   static constexpr int kStagingFloats = 128 * 17;
   // quantised formats: each converter thread's copy of its row's scales (<= 16 words), padded
@@ -495,9 +496,13 @@ __global__ void __launch_bounds__(TcCfg<FMT, NMAX>::kThreads, 1)
       // this row's scales (block-FP8: one fp32 per 128-column block of its block row;
       // int4: one (s, z) pair per group; MXFP4: one E8M0 byte per 32 columns, four to a
       // word), read once per item instead of once per stage
-      const int nblk = cols >> 7;
-      const uint32_t* srow = reinterpret_cast<const uint32_t*>(sc) +
-                             (FMT == PMOE_FP8_BLOCK128 ? (size_t)(grow >> 7) * nblk : (size_t)grow * nblk);
+      // (NVFP4: one word = the four e4m3 block scales of a 64-input stage, after the
+      // 16-byte tensor-scale header; the tensor scale itself is applied in the epilogue)
+      const int nblk = FMT == PMOE_NVFP4 ? (cols >> 6) : (cols >> 7);
+      const uint32_t* srow =
+          FMT == PMOE_NVFP4 ? reinterpret_cast<const uint32_t*>(sc + 16 + (size_t)grow * (cols >> 4))
+                            : reinterpret_cast<const uint32_t*>(sc) +
+                                  (FMT == PMOE_FP8_BLOCK128 ? (size_t)(grow >> 7) * nblk : (size_t)grow * nblk);
       uint32_t* my_sc = scale_cache + ct * 17;
       const bool cached = nblk <= 16;
       if (cached)
@@ -527,6 +532,27 @@ __global__ void __launch_bounds__(TcCfg<FMT, NMAX>::kThreads, 1)
               const __nv_bfloat162 b1 = __floats2bfloat162_rn(f1.x * sv, f1.y * sv);
               out[2 * h] = *reinterpret_cast<const uint32_t*>(&b0);
               out[2 * h + 1] = *reinterpret_cast<const uint32_t*>(&b1);
+            }
+            arow[c ^ (r & 7)] = make_uint4(out[0], out[1], out[2], out[3]);
+          }
+        } else if (FMT == PMOE_NVFP4) {
+          // 64 codes = four blocks of 16, each with its own e4m3 byte; E2M1 times e4m3
+          // is exact in bf16
+          const uint8_t* qr = qt + r * (kBK / 2);
+          const uint32_t bw = cached ? my_sc[kb] : __ldg(srow + kb);
+#pragma unroll
+          for (int c = 4 * hf; c < 4 * hf + 4; ++c) {
+            const uint32_t word = *reinterpret_cast<const uint32_t*>(qr + c * 4);  // 8 codes, low nibble first
+            const __half_raw sh = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)((bw >> (8 * (c >> 1))) & 0xffu), __NV_E4M3);
+            const float sv = __half2float(*reinterpret_cast<const __half*>(&sh));
+            uint32_t out[4];
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              const __half2_raw pr =
+                  __nv_cvt_fp4x2_to_halfraw2((__nv_fp4x2_storage_t)((word >> (8 * h)) & 0xffu), __NV_E2M1);
+              const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&pr));
+              const __nv_bfloat162 bv = __floats2bfloat162_rn(f.x * sv, f.y * sv);
+              out[h] = *reinterpret_cast<const uint32_t*>(&bv);
             }
             arow[c ^ (r & 7)] = make_uint4(out[0], out[1], out[2], out[3]);
           }
@@ -593,6 +619,11 @@ __global__ void __launch_bounds__(TcCfg<FMT, NMAX>::kThreads, 1)
       const int pstart = ws.tiles[3 * tile + 1], np = ws.tiles[3 * tile + 2];
       const int n_mma = (np + 15) & ~15;
       const int ab = it & 1, use = it >> 1;
+      // NVFP4: the matrix's fp32 tensor scale, applied to the fp32 accumulators
+      const float tsc = FMT == PMOE_NVFP4 ? __ldg(reinterpret_cast<const float*>(
+                                                arena + (size_t)ws.tiles[3 * tile + 0] * stride +
+                                                (GATEUP ? lay.gu_s : lay.d_s)))
+                                          : 1.f;
       const bool got = mbar_wait(&acc_full[ab], (uint32_t)(use & 1), abort_flag, err);
       if (epi_bar_or(got ? 0 : 1)) break;
       fence_after();
@@ -605,7 +636,7 @@ __global__ void __launch_bounds__(TcCfg<FMT, NMAX>::kThreads, 1)
           // stage gate (rows 0-63) and up (rows 64-127) values, then each thread forms
           // 8 consecutive h values of one pair: one 16-byte store, 128 B per pair row
 #pragma unroll
-          for (int i = 0; i < 16; ++i) staging[row * 17 + i] = __uint_as_float(v[i]);
+          for (int i = 0; i < 16; ++i) staging[row * 17 + i] = __uint_as_float(v[i]) * tsc;
           epi_bar();
           const int pl = et >> 3, js = (et & 7) * 8;
           if (c + pl < np) {
@@ -625,7 +656,7 @@ __global__ void __launch_bounds__(TcCfg<FMT, NMAX>::kThreads, 1)
           const int n = mt * 128 + row;
 #pragma unroll
           for (int i = 0; i < 16; ++i)
-            if (c + i < np) ws.o_part[(size_t)(pstart + c + i) * H + n] = __uint_as_float(v[i]);
+            if (c + i < np) ws.o_part[(size_t)(pstart + c + i) * H + n] = __uint_as_float(v[i]) * tsc;
         }
       }
       fence_before();
@@ -1151,7 +1182,8 @@ int tc_make_weight_maps(uint8_t* arena, size_t stride, int K, int H, int I, int 
     const cuuint32_t box[3] = {(cuuint32_t)kBK, 128, 1};
     return encode(&out->d, arena + lay.d_w, 3, dims, strides, box) == PMOE_OK ? PMOE_OK : PMOE_ECUDA;
   }
-  if (fmt != PMOE_FP8_BLOCK128 && fmt != PMOE_INT4_GPTQ_G128 && fmt != PMOE_MXFP4) return PMOE_EUNSUPPORTED;
+  if (fmt != PMOE_FP8_BLOCK128 && fmt != PMOE_INT4_GPTQ_G128 && fmt != PMOE_MXFP4 && fmt != PMOE_NVFP4)
+    return PMOE_EUNSUPPORTED;
   if (fmt == PMOE_FP8_BLOCK128) {
     // e4m3 rows as MMA operands: 128-byte boxes (128 K), 128-byte swizzle
     {
@@ -1166,6 +1198,7 @@ int tc_make_weight_maps(uint8_t* arena, size_t stride, int K, int H, int I, int 
     if (encode(&out->d8, arena + lay.d_w, 3, dims, strides, box, kMapBytesSw128) != PMOE_OK) return PMOE_ECUDA;
   }
   // quantised weights are loaded as bytes (one e4m3, or two int4 / E2M1 codes, per byte), unswizzled
+  // (NVFP4's codes are laid out as MXFP4's)
   const cuuint64_t hb = fmt == PMOE_FP8_BLOCK128 ? (cuuint64_t)H : (cuuint64_t)H / 2;
   const cuuint64_t ib = fmt == PMOE_FP8_BLOCK128 ? (cuuint64_t)I : (cuuint64_t)I / 2;
   const cuuint32_t kbb = fmt == PMOE_FP8_BLOCK128 ? (cuuint32_t)kBK : (cuuint32_t)kBK / 2;
@@ -1220,6 +1253,8 @@ cudaError_t tc_gateup(int fmt, const TcMaps& wm, const TcMaps& am, const int32_t
   if (fmt == PMOE_INT4_GPTQ_G128)
     return launch_tc<true, PMOE_INT4_GPTQ_G128>(wm.gu, am.x, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, tile_n,
                                                 s);
+  if (fmt == PMOE_NVFP4)
+    return launch_tc<true, PMOE_NVFP4>(wm.gu, am.x, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, tile_n, s);
   if (fmt == PMOE_MXFP4)
     return launch_tc<true, PMOE_MXFP4>(wm.gu, am.x, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, tile_n, s);
   return launch_tc<true, PMOE_BF16>(wm.gu, am.x, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, tile_n, s);
@@ -1235,6 +1270,8 @@ cudaError_t tc_down(int fmt, const TcMaps& wm, const TcMaps& am, const int32_t* 
   if (fmt == PMOE_INT4_GPTQ_G128)
     return launch_tc<false, PMOE_INT4_GPTQ_G128>(wm.d, am.h, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, tile_n,
                                                  s);
+  if (fmt == PMOE_NVFP4)
+    return launch_tc<false, PMOE_NVFP4>(wm.d, am.h, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, tile_n, s);
   if (fmt == PMOE_MXFP4)
     return launch_tc<false, PMOE_MXFP4>(wm.d, am.h, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, tile_n, s);
   return launch_tc<false, PMOE_BF16>(wm.d, am.h, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, tile_n, s);

@@ -30,7 +30,7 @@ the sizing of one configuration:
 import argparse
 from dataclasses import dataclass, asdict
 
-FORMATS = {"bf16": 0, "fp8": 1, "int4": 2, "mxfp4": 3}
+FORMATS = {"bf16": 0, "fp8": 1, "int4": 2, "mxfp4": 3, "nvfp4": 4}
 
 
 def qwen3_kv_bytes_per_token(layers=48, kv_heads=4, head_dim=128, elem_bytes=2):

@@ -35,6 +35,8 @@ def test_expert_sizes_from_the_library():
     assert pm.pmoe_expert_bytes(pm.PMOE_FP8_BLOCK128, 2048, 768) == 4_719_744
     assert pm.pmoe_expert_bytes(pm.PMOE_INT4_GPTQ_G128, 2048, 768) == 2_506_752
     assert pm.pmoe_expert_bytes(pm.PMOE_MXFP4, 2048, 768) == 2_506_752
+    assert pm.pmoe_expert_bytes(pm.PMOE_NVFP4, 2048, 768) == 2_654_240
+    assert pm.pmoe_expert_bytes(pm.PMOE_NVFP4, 2048, 200) == 0
     assert pm.pmoe_expert_bytes(pm.PMOE_FP8_BLOCK128, 200, 768) == 0
     assert pm.pmoe_expert_bytes(pm.PMOE_MXFP4, 200, 768) == 0
     assert pm.pmoe_expert_bytes(7, 2048, 768) == 0
@@ -44,7 +46,7 @@ def test_expert_sizes_from_the_library():
 def test_library_expert_sizes_equal_the_oracle_layout(H, I):
     import paged_expert_moe_gb300 as pm
     from oracle import formats
-    for fmt in (pm.PMOE_BF16, pm.PMOE_FP8_BLOCK128, pm.PMOE_INT4_GPTQ_G128, pm.PMOE_MXFP4):
+    for fmt in (pm.PMOE_BF16, pm.PMOE_FP8_BLOCK128, pm.PMOE_INT4_GPTQ_G128, pm.PMOE_MXFP4, pm.PMOE_NVFP4):
         assert pm.pmoe_expert_bytes(fmt, H, I) == formats.expert_nbytes(fmt, H, I), (fmt, H, I)
 
 

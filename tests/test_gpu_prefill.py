@@ -47,12 +47,14 @@ def _forward(cache, x_bits, logits, k):
 
 @pytest.mark.parametrize("T,skew,fmt", [(300, True, 0), (9, False, 0), (64, False, 0), (1000, False, 0),
                                         (300, True, 1), (64, False, 1), (128, True, 1), (1000, False, 1),
-                                        (300, True, 2), (64, False, 2), (300, True, 3), (64, False, 3)])
+                                        (300, True, 2), (64, False, 2), (300, True, 3), (64, False, 3),
+                                        (300, True, 4), (64, False, 4)])
 def test_prefill_small_layer_parity_and_bitwise_k_invariance(pm, T, skew, fmt):
     """bf16, block-FP8, GPTQ-int4 and MXFP4 prefill tiles. Block-FP8 with few pairs per
     expert (T=64, and T=128 skewed, where hot experts take several 64-pair tiles) runs
     e4m3 MMAs on two-plane activations; with more (T=300, 1000) its weights are
-    dequantised to bf16 in shared memory, like int4 and MXFP4."""
+    dequantised to bf16 in shared memory, like int4, MXFP4 and NVFP4 (whose fp32 tensor
+    scale multiplies the accumulators)."""
     E, k, H, I = 16, 4, 256, 384
     L = hz.SyntheticLayer(fmt, E, H, I, seed=200 + T)
     rng = np.random.default_rng(200 + T)
@@ -113,7 +115,7 @@ def test_gemv_and_tensor_core_paths_agree_at_the_boundary(pm):
         hz.assert_layer_close(hz.bf16_to_f64(y), L.oracle_y(x_bits, ids, w), 0)
 
 
-@pytest.mark.parametrize("fmt", [1, 3])
+@pytest.mark.parametrize("fmt", [1, 3, 4])
 def test_prefill_quantised_512_tokens_k40(pm, fmt):
     """Block-FP8 (rel-Frobenius 3e-2) and MXFP4 (the bf16 tolerances: E2M1 times an E8M0
     scale is exact in bf16) Qwen3-30B-A3B layers, 512-token prefill, K=40 (several waves):

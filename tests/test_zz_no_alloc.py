@@ -38,7 +38,7 @@ def _experts_on_device(store, stride, order=None):
     return torch.from_numpy(buf).cuda()
 
 
-@pytest.mark.parametrize("fmt", [0, 1, 2, 3])
+@pytest.mark.parametrize("fmt", [0, 1, 2, 3, 4])
 def test_noalloc_matches_oracle_and_paged_forward_on_two_calls(pm, fmt):
     """Qwen3 shape (H=2048, I=768), 32 experts, 4 tokens, every format: each of two calls
     in a row is within the layer tolerance of the oracle and of moe_paged_forward, and
