@@ -500,6 +500,9 @@ def _summary(out):
     sm["mxfp4_decode_B1_tok_s"] = r3(g(out, "mxfp4", "decode_B1", "tokens_per_s"))
     sm["mxfp4_decode_kernel_hbm_frac"] = r3(g(out, "mxfp4", "decode_B1", "decode_kernel_hbm_frac"))
     sm["mxfp4_prefill512_gemm_tflops"] = r3(g(out, "mxfp4", "prefill_512_cold", "gemm_tflops"))
+    sm["nvfp4_decode_B1_tok_s"] = r3(g(out, "nvfp4", "decode_B1", "tokens_per_s"))
+    sm["nvfp4_decode_kernel_hbm_frac"] = r3(g(out, "nvfp4", "decode_B1", "decode_kernel_hbm_frac"))
+    sm["nvfp4_prefill512_gemm_tflops"] = r3(g(out, "nvfp4", "prefill_512_cold", "gemm_tflops"))
     for k_ in ("B1", "B1_graph", "B4", "B4_graph"):
         sm[f"stack_int4_{k_}_tok_s"] = r3(g(out, "stack_int4", k_, "tokens_per_s"))
         ov = g(out, "stack_int4", k_, "overlap")
@@ -526,6 +529,11 @@ def run_ours(args):
             print(json.dumps({"metric": METRIC, "impl": "ours", "section": "mxfp4",
                               "mxfp4": run_mxfp4(pm, torch, args, local, hbm_peak)}))
         return
+    if args.section == "nvfp4":
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "impl": "ours", "section": "nvfp4",
+                              "nvfp4": run_nvfp4(pm, torch, args, local, hbm_peak)}))
+        return
     if args.section in ("prefill", "stack", "decode_staged", "prefill_sweep"):
         # one part of the bench alone (for profiling); one JSON line with that part
         out = {"metric": METRIC, "impl": "ours", "section": args.section}
@@ -541,7 +549,7 @@ def run_ours(args):
         else:
             # the decode kernel alone on resident weights (page-in staged ahead): the launches
             # the roofline is measured on
-            fmt = {"bf16": 0, "fp8": 1, "int4": 2, "mxfp4": 3}[args.format]
+            fmt = {"bf16": 0, "fp8": 1, "int4": 2, "mxfp4": 3, "nvfp4": 4}[args.format]
             st = store if fmt == 0 else make_store(fmt=fmt)
             r = run_decode(pm, torch, st, args.batch, args.steps, args.warmup, local, e2e=False, mode=1, stage=True,
                            fmt=fmt)
@@ -570,6 +578,7 @@ def run_ours(args):
     stack = {}
     fp8 = None
     mxfp4 = None
+    nvfp4 = None
     sweep = None
     h2d = measure_h2d(torch, torch.device("cuda", local))
     # the other sections (batches, prefill, formats, the stack) run in single-GPU runs
@@ -593,6 +602,7 @@ def run_ours(args):
         sweep = run_prefill_sweep(pm, torch, args, local, hbm_peak, tc_peak)
         fp8 = run_fp8(pm, torch, args, local, hbm_peak)
         mxfp4 = run_mxfp4(pm, torch, args, local, hbm_peak)
+        nvfp4 = run_nvfp4(pm, torch, args, local, hbm_peak)
     job_ms = reduce_max(head["total_ms"], ws, torch.device("cuda", local))
     value = ws * 1 * args.steps / (job_ms / 1e3)
     if rank != 0:
@@ -655,6 +665,7 @@ def run_ours(args):
         "prefill_sweep": sweep,
         "fp8": fp8,
         "mxfp4": mxfp4,
+        "nvfp4": nvfp4,
         "stack_int4": ({"workload": "48-layer Qwen3-30B-A3B-shaped MoE stack (attention omitted), GPTQ-int4 g128 "
                                     "experts, K=26 slots/layer, p=0.8 reuse routing per layer, residual stream",
                         "hbm_roofline_tokens_per_s_B1": hbm_peak * 1e9 / (STACK_L * TOPK * 2_506_752),
@@ -718,6 +729,36 @@ def run_mxfp4(pm, torch, args, local, hbm_peak):
                                      hbm_bound_tflops=flop / (E * ebytes / (hbm_peak * 1e9)) / 1e12,
                                      note="E2M1 x E8M0 weights are dequantised (exactly) to bf16 in shared memory "
                                           "for kind::f16 MMAs")}
+
+
+def run_nvfp4(pm, torch, args, local, hbm_peak):
+    """NVFP4 experts (E2M1 codes, an e4m3 scale per 16 inputs, an fp32 tensor scale per
+    matrix): the same layer, K=40, decode B=1 over the p=0.8 reuse trace (the GEMV decode
+    kernels), plus a cold 512-token prefill."""
+    store = make_store(fmt=4)
+    ebytes = pm.pmoe_expert_bytes(4, H, I)
+    head = run_decode(pm, torch, store, 1, args.steps, args.warmup, local, e2e=False, mode=1, graph=True, fmt=4)
+    staged = run_decode(pm, torch, store, 1, args.steps, args.warmup, local, e2e=False, mode=1, stage=True, fmt=4)
+    kt = staged["kernel_times"]
+    dec_ms = kt["gateup"]["ms"] + kt["down"]["ms"]  # the GEMV gate/up and down kernels
+    dec_gbs = staged["expert_weight_bytes"] / (dec_ms / 1e3) / 1e9
+    pre = run_prefill(pm, torch, store, args.prefill_steps, 2, local, K=40, cold=True, fmt=4, T=512)
+    flop = 2.0 * 512 * TOPK * 3 * H * I
+    return {"workload": "Qwen3-30B-A3B-shaped MoE layer, NVFP4 experts (E2M1, e4m3 scale per 16 inputs, fp32 "
+                        "tensor scale per matrix), K=40",
+            "expert_bytes": ebytes,
+            "decode_B1": {"tokens_per_s": head["tokens_per_s"], "ms_per_step": head["ms_per_step"],
+                          "misses_per_step": head["misses_per_step"],
+                          "mode": "SM-pull page-in by the pull kernel, GEMV decode kernels, whole step replayed "
+                                  "as one CUDA graph",
+                          "decode_kernel_gbs": dec_gbs, "decode_kernel_hbm_frac": dec_gbs / hbm_peak,
+                          "decode_kernel_us": dec_ms / args.steps * 1e3,
+                          "decode_kernels": "GEMV gate/up + down (the fused decode kernel declines NVFP4)",
+                          "decode_kernel_measured_in": "page-in staged ahead by the pull kernel"},
+            "prefill_512_cold": dict(pre, FLOP_per_step=flop, weight_bytes_per_step=E * ebytes,
+                                     hbm_bound_tflops=flop / (E * ebytes / (hbm_peak * 1e9)) / 1e12,
+                                     note="E2M1 x e4m3 weights are dequantised (exactly) to bf16 in shared memory "
+                                          "for kind::f16 MMAs; the fp32 tensor scale multiplies the accumulators")}
 
 
 STACK_L, STACK_K = 48, 26
@@ -979,12 +1020,12 @@ def main():
     ap.add_argument("--stack-layers", type=int, default=STACK_L,
                     help="layers of the stack section (48 for the measured workload; fewer for profiling)")
     ap.add_argument("--section", default="all",
-                    choices=["all", "prefill", "prefill_sweep", "stack", "decode_staged", "fp8", "mxfp4"],
+                    choices=["all", "prefill", "prefill_sweep", "stack", "decode_staged", "fp8", "mxfp4", "nvfp4"],
                     help="run only one part (profiling); the default runs everything")
     ap.add_argument("--prefill-tokens", default="8192,16384",
                     help="token counts of the tensor-bound prefill sweep (comma-separated)")
     ap.add_argument("--batch", type=int, default=1, help="decode batch of --section decode_staged")
-    ap.add_argument("--format", default="bf16", choices=["bf16", "fp8", "int4", "mxfp4"],
+    ap.add_argument("--format", default="bf16", choices=["bf16", "fp8", "int4", "mxfp4", "nvfp4"],
                     help="expert format of --section decode_staged")
     args = ap.parse_args()
     if args.warmup < 3:
