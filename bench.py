@@ -733,14 +733,14 @@ def run_mxfp4(pm, torch, args, local, hbm_peak):
 
 def run_nvfp4(pm, torch, args, local, hbm_peak):
     """NVFP4 experts (E2M1 codes, an e4m3 scale per 16 inputs, an fp32 tensor scale per
-    matrix): the same layer, K=40, decode B=1 over the p=0.8 reuse trace (the GEMV decode
-    kernels), plus a cold 512-token prefill."""
+    matrix): the same layer, K=40, decode B=1 over the p=0.8 reuse trace, plus a cold
+    512-token prefill."""
     store = make_store(fmt=4)
     ebytes = pm.pmoe_expert_bytes(4, H, I)
     head = run_decode(pm, torch, store, 1, args.steps, args.warmup, local, e2e=False, mode=1, graph=True, fmt=4)
     staged = run_decode(pm, torch, store, 1, args.steps, args.warmup, local, e2e=False, mode=1, stage=True, fmt=4)
     kt = staged["kernel_times"]
-    dec_ms = kt["gateup"]["ms"] + kt["down"]["ms"]  # the GEMV gate/up and down kernels
+    dec_ms = kt["decode"]["ms"]
     dec_gbs = staged["expert_weight_bytes"] / (dec_ms / 1e3) / 1e9
     pre = run_prefill(pm, torch, store, args.prefill_steps, 2, local, K=40, cold=True, fmt=4, T=512)
     flop = 2.0 * 512 * TOPK * 3 * H * I
@@ -748,12 +748,9 @@ def run_nvfp4(pm, torch, args, local, hbm_peak):
                         "tensor scale per matrix), K=40",
             "expert_bytes": ebytes,
             "decode_B1": {"tokens_per_s": head["tokens_per_s"], "ms_per_step": head["ms_per_step"],
-                          "misses_per_step": head["misses_per_step"],
-                          "mode": "SM-pull page-in by the pull kernel, GEMV decode kernels, whole step replayed "
-                                  "as one CUDA graph",
+                          "misses_per_step": head["misses_per_step"], "mode": head["mode"],
                           "decode_kernel_gbs": dec_gbs, "decode_kernel_hbm_frac": dec_gbs / hbm_peak,
                           "decode_kernel_us": dec_ms / args.steps * 1e3,
-                          "decode_kernels": "GEMV gate/up + down (the fused decode kernel declines NVFP4)",
                           "decode_kernel_measured_in": "page-in staged ahead by the pull kernel"},
             "prefill_512_cold": dict(pre, FLOP_per_step=flop, weight_bytes_per_step=E * ebytes,
                                      hbm_bound_tflops=flop / (E * ebytes / (hbm_peak * 1e9)) / 1e12,

@@ -154,7 +154,7 @@ __global__ void __launch_bounds__(kDfThreads, 1) decode_fused_kernel(const DfArg
       const int nh = D0;  // (no page-in: every wave expert is resident)
       const DfSched sc0{D0, (int)gridDim.x, (int)blockIdx.x, a.I, a.H, a.cg, a.cd};
       const size_t rbg0 = (size_t)a.H * Fmt<FMT>::BPE2 / 2;
-      const int rsg0 = (a.H / 128) * 4;
+      const int rsg0 = row_scale_bytes(FMT, a.H);
       const unsigned R0 = (unsigned)a.ring_bytes;
       for (int q = 0; q < min(kDfLag, D0) * a.cg && q < kDfSlots; ++q) {
         const int4 cq = sched_entry(q, sc0);  // a gate/up chunk of wave expert q / cg
@@ -323,7 +323,7 @@ __global__ void __launch_bounds__(kDfThreads, 1) decode_fused_kernel(const DfArg
   if (tid == 0) DF_TRACE(1);
   const size_t rbg = (size_t)a.H * Fmt<FMT>::BPE2 / 2;  // one gate (or up) row
   const size_t rbd = (size_t)a.I * Fmt<FMT>::BPE2 / 2;  // one down row
-  const int rsg = (a.H / 128) * 4, rsd = (a.I / 128) * 4;  // one scale row of gate/up, of down
+  const int rsg = row_scale_bytes(FMT, a.H), rsd = row_scale_bytes(FMT, a.I);  // one scale row of gate/up, of down
 
   if (warp == kDfConsumerWarps) {
     // ---------------- producer: lane 0 places every chunk in the byte ring as soon as
@@ -524,31 +524,39 @@ __global__ void __launch_bounds__(kDfThreads, 1) decode_fused_kernel(const DfArg
         const uint8_t* src = a.store + (size_t)we.x * a.stride;
         uint8_t* dst = a.arena + (size_t)we.y * a.stride;
         const int z = cd.z, n = cd.w;
+        // NVFP4: the matrix's 16-byte tensor-scale header (just before its block scales),
+        // loaded first so that its host-link round trip overlaps the rows' and stored last
+        uint32_t hdr = 0;
+        const size_t hdr_off = ((cd.x & 3) == 1 ? a.lay.gu_s : a.lay.d_s) - 16;
+        if constexpr (FMT == PMOE_NVFP4)
+          if (vl < 4) hdr = *reinterpret_cast<const uint32_t*>(src + hdr_off + 4 * vl);
         if ((cd.x & 3) == 1) {
           lanes_copy16x2(src, dst, a.lay.gu_w + (size_t)z * rbg, (size_t)n * rbg, a.lay.gu_w + (size_t)(a.I + z) * rbg,
                          (size_t)n * rbg, vl, nl);
           if constexpr (FMT == PMOE_FP8_BLOCK128) {
             const size_t row = 4 * (size_t)hb;  // one block row of scales
-            lanes_copy4(src, dst, a.lay.gu_s + (size_t)(z >> 7) * row,
-                        (size_t)(((z + n - 1) >> 7) - (z >> 7) + 1) * row, vl, nl);
-            lanes_copy4(src, dst, a.lay.gu_s + (size_t)((a.I + z) >> 7) * row,
-                        (size_t)(((a.I + z + n - 1) >> 7) - ((a.I + z) >> 7) + 1) * row, vl, nl);
-          } else if constexpr (FMT == PMOE_INT4_GPTQ_G128 || FMT == PMOE_MXFP4) {
-            const size_t row = 4 * (size_t)hb;  // one row's scale bytes: (s, z) pairs, or E8M0 per 32 inputs
-            lanes_copy4(src, dst, a.lay.gu_s + (size_t)z * row, (size_t)n * row, vl, nl);
-            lanes_copy4(src, dst, a.lay.gu_s + (size_t)(a.I + z) * row, (size_t)n * row, vl, nl);
+            lanes_copy4x2(src, dst, a.lay.gu_s + (size_t)(z >> 7) * row,
+                          (size_t)(((z + n - 1) >> 7) - (z >> 7) + 1) * row, a.lay.gu_s + (size_t)((a.I + z) >> 7) * row,
+                          (size_t)(((a.I + z + n - 1) >> 7) - ((a.I + z) >> 7) + 1) * row, vl, nl);
+          } else if constexpr (FMT == PMOE_INT4_GPTQ_G128 || FMT == PMOE_MXFP4 || FMT == PMOE_NVFP4) {
+            // one row's scale bytes: (s, z) pairs, E8M0 per 32 inputs, or e4m3 per 16
+            const size_t row = (size_t)row_scale_bytes(FMT, a.H);
+            lanes_copy4x2(src, dst, a.lay.gu_s + (size_t)z * row, (size_t)n * row, a.lay.gu_s + (size_t)(a.I + z) * row,
+                          (size_t)n * row, vl, nl);
           }
         } else {
           lanes_copy16x2(src, dst, a.lay.d_w + (size_t)z * rbd, (size_t)n * rbd, 0, 0, vl, nl);
           if constexpr (FMT == PMOE_FP8_BLOCK128) {
             const size_t row = 4 * (size_t)ib;
-            lanes_copy4(src, dst, a.lay.d_s + (size_t)(z >> 7) * row,
-                        (size_t)(((z + n - 1) >> 7) - (z >> 7) + 1) * row, vl, nl);
-          } else if constexpr (FMT == PMOE_INT4_GPTQ_G128 || FMT == PMOE_MXFP4) {
-            const size_t row = 4 * (size_t)ib;
-            lanes_copy4(src, dst, a.lay.d_s + (size_t)z * row, (size_t)n * row, vl, nl);
+            lanes_copy4x2(src, dst, a.lay.d_s + (size_t)(z >> 7) * row,
+                          (size_t)(((z + n - 1) >> 7) - (z >> 7) + 1) * row, 0, 0, vl, nl);
+          } else if constexpr (FMT == PMOE_INT4_GPTQ_G128 || FMT == PMOE_MXFP4 || FMT == PMOE_NVFP4) {
+            const size_t row = (size_t)row_scale_bytes(FMT, a.I);
+            lanes_copy4x2(src, dst, a.lay.d_s + (size_t)z * row, (size_t)n * row, 0, 0, vl, nl);
           }
         }
+        if constexpr (FMT == PMOE_NVFP4)
+          if (vl < 4) *reinterpret_cast<uint32_t*>(dst + hdr_off + 4 * vl) = hdr;
         // the stores (generic proxy) are read next by bulk copies (async proxy)
         asm volatile("fence.proxy.async.global;" ::: "memory");
         pagers_sync();
@@ -581,6 +589,16 @@ __global__ void __launch_bounds__(kDfThreads, 1) decode_fused_kernel(const DfArg
       const int4 we = s_we[cd.y];
       const uint8_t* st = ring + s_off[s];
       bool ok = true;
+      // NVFP4: the chunk's matrix's tensor scale, in the 16-byte header before its block
+      // scales in the slot (an expert this launch pages in: written by this CTA's pagers
+      // before the chunk's progress, which the producer acquired before its copies)
+      float tsc = 1.f;
+      if constexpr (FMT == PMOE_NVFP4) {
+        if (cd.w > 0) {
+          const uint8_t* hdr = a.arena + (size_t)we.y * a.stride + (kind == 1 ? a.lay.gu_s : a.lay.d_s) - 16;
+          asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(tsc) : "l"(hdr));
+        }
+      }
       if (kind == 1) {
         if (warp == 0 && lane == 0) DF_TRACE(6);  // (the last write is the last gate/up chunk)
         for (int rp = first; rp < cd.w; rp += kDfConsumerWarps) {
@@ -621,8 +639,8 @@ __global__ void __launch_bounds__(kDfThreads, 1) decode_fused_kernel(const DfArg
               for (int c = 0; c < NCH1; ++c) {
                 const int idx = lane + 32 * c;
                 if (idx < nch1) {
-                  const ChunkQ qg = chunk_q_ring<FMT>(sgr, idx);
-                  const ChunkQ qu = chunk_q_ring<FMT>(sur, idx);
+                  const ChunkQ qg = chunk_q_ring<FMT>(sgr, idx, tsc);
+                  const ChunkQ qu = chunk_q_ring<FMT>(sur, idx, tsc);
                   g += chunk_dot<FMT, kSrcShared>(gw[c], xr + idx * (EPC / 8), qg);
                   u += chunk_dot<FMT, kSrcShared>(uw[c], xr + idx * (EPC / 8), qu);
                 }
@@ -658,7 +676,7 @@ __global__ void __launch_bounds__(kDfThreads, 1) decode_fused_kernel(const DfArg
             for (int c = 0; c < NCH2; ++c) {
               const int idx = lane + 32 * c;
               if (idx < nch2) {
-                const ChunkQ q = chunk_q_ring<FMT>(sdr, idx);
+                const ChunkQ q = chunk_q_ring<FMT>(sdr, idx, tsc);
                 if (pi < a.T) {
                   acc += chunk_dot<FMT, kSrcShared>(lds128(row + idx), hsv + (size_t)pi * (a.I / 8) + idx * (EPC / 8), q);
                 } else {
@@ -746,7 +764,9 @@ struct DfGeom {
 
 bool df_geometry(int fmt, int T, int top_k, int H, int I, int G, DfGeom* g) {
   // formats the fused kernel streams (NVFP4 decodes through the GEMV kernels)
-  if (fmt != PMOE_BF16 && fmt != PMOE_FP8_BLOCK128 && fmt != PMOE_INT4_GPTQ_G128 && fmt != PMOE_MXFP4) return false;
+  if (fmt != PMOE_BF16 && fmt != PMOE_FP8_BLOCK128 && fmt != PMOE_INT4_GPTQ_G128 && fmt != PMOE_MXFP4 &&
+      fmt != PMOE_NVFP4)
+    return false;
   if (T < 1 || T * top_k > kDfMaxPairs || G < 1 || G > 1024 || H % 8 != 0 || I % 8 != 0) return false;
   if (H >= (1 << 20) || I >= (1 << 20)) return false;  // the schedule's 32-bit products
   const size_t rbg = fmt_row_bytes(fmt, H), rbd = fmt_row_bytes(fmt, I);
@@ -770,7 +790,7 @@ bool df_geometry(int fmt, int T, int top_k, int H, int I, int G, DfGeom* g) {
     if (H % 128 != 0 || I % 128 != 0) return false;
     const ExpertLayout lay = expert_layout(fmt, H, I);
     if (lay.gu_s % 16 != 0 || lay.d_s % 16 != 0 || lay.bytes % 16 != 0) return false;
-    const size_t rsg = (size_t)(H / 128) * 4, rsd = (size_t)(I / 128) * 4;
+    const size_t rsg = (size_t)row_scale_bytes(fmt, H), rsd = (size_t)row_scale_bytes(fmt, I);
     scale_max = 2 * ((size_t)(rj + 1) * rsg + 32) + (size_t)(kDfMaxRows + 1) * rsd + 32;
   }
   // a down chunk also holds the h rows of up to T pairs
@@ -878,6 +898,10 @@ cudaError_t launch_decode_fused(int fmt, const __nv_bfloat16* x, const int32_t* 
   a.pull = (pull != 0 && store != nullptr) ? 1 : 0;
   a.stride = stride;
   a.lay = expert_layout(fmt, H, I);
+  if (fmt == PMOE_NVFP4) {  // the kernel's scale regions start after the 16-byte tensor-scale headers
+    a.lay.gu_s += 16;
+    a.lay.d_s += 16;
+  }
   a.err = err;
   const size_t smem = g.ring + g.fixed;
   const int nch1 = (int)(fmt_row_bytes(fmt, H) / 16), nch2 = (int)(fmt_row_bytes(fmt, I) / 16);
@@ -895,6 +919,9 @@ cudaError_t launch_decode_fused(int fmt, const __nv_bfloat16* x, const int32_t* 
   } else if (fmt == PMOE_MXFP4) {
     if (nch1 <= 32 * 2 && nch2 <= 32 * 1) PMOE_DF(PMOE_MXFP4, 2, 1);
     if (nch1 <= 32 * 4 && nch2 <= 32 * 2) PMOE_DF(PMOE_MXFP4, 4, 2);
+  } else if (fmt == PMOE_NVFP4) {
+    if (nch1 <= 32 * 2 && nch2 <= 32 * 1) PMOE_DF(PMOE_NVFP4, 2, 1);
+    if (nch1 <= 32 * 4 && nch2 <= 32 * 2) PMOE_DF(PMOE_NVFP4, 4, 2);
   }
 #undef PMOE_DF
   return cudaErrorInvalidValue;

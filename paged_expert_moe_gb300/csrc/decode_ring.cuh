@@ -131,7 +131,30 @@ __device__ __forceinline__ void lanes_copy16x2(const uint8_t* src, uint8_t* dst,
     }
   }
 }
-// The same for a small range whose size and offset are multiples of 4 (scale rows).
+// The same for small ranges whose sizes and offsets are multiples of 4 (scale rows): 8
+// loads in flight per lane (over the host link a load costs a round trip; one at a time,
+// a few hundred bytes of scale rows took several round trips per chunk).
+// (not inlined: its registers would otherwise count against the whole decode kernel)
+__device__ __noinline__ void lanes_copy4x2(const uint8_t* src, uint8_t* dst, size_t off1, size_t bytes1,
+                                           size_t off2, size_t bytes2, int vl, int nl) {
+  constexpr int U = 8;
+  const size_t n1 = bytes1 / 4, n = n1 + bytes2 / 4;
+  for (size_t base = (size_t)vl; base < n; base += (size_t)nl * U) {
+    uint32_t v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const size_t i = base + (size_t)u * nl;
+      if (i < n) v[u] = *reinterpret_cast<const uint32_t*>(src + (i < n1 ? off1 + i * 4 : off2 + (i - n1) * 4));
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const size_t i = base + (size_t)u * nl;
+      if (i < n) *reinterpret_cast<uint32_t*>(dst + (i < n1 ? off1 + i * 4 : off2 + (i - n1) * 4)) = v[u];
+    }
+  }
+}
+// One load in flight per lane (inlined; the persistent stack kernel keeps this form for
+// the formats whose scale rows are short).
 __device__ __forceinline__ void lanes_copy4(const uint8_t* src, uint8_t* dst, size_t off, size_t bytes, int vl,
                                             int nl) {
   for (size_t i = (size_t)vl * 4; i < bytes; i += (size_t)nl * 4)
@@ -260,6 +283,12 @@ __device__ __forceinline__ int ring_place(unsigned head, unsigned lo, bool empty
 struct ScaleSpan {
   uint32_t src, bytes, first;  // src: byte offset in the expert
 };
+// Bytes of one scale row of a matrix with n inputs per row: an fp32 per 128x128 block
+// (FP8, per block row), an (s, z) fp16 pair per 128 (int4), an E8M0 byte per 32 (MXFP4),
+// an e4m3 byte per 16 (NVFP4).
+__host__ __device__ __forceinline__ int row_scale_bytes(int fmt, int n) {
+  return fmt == PMOE_NVFP4 ? n / 16 : (n / 128) * 4;
+}
 template <int FMT>
 __device__ __forceinline__ int scale_row(int r) {
   return FMT == PMOE_FP8_BLOCK128 ? (r >> 7) : r;
@@ -271,10 +300,15 @@ __device__ __forceinline__ ScaleSpan scale_span(size_t region, int RS, int r0, i
   const uint32_t a0 = b0 & ~15u, a1 = (b1 + 15u) & ~15u;
   return ScaleSpan{a0, a1 - a0, b0 - a0};
 }
+// t: NVFP4's tensor scale of the row's matrix (unused by the other formats)
 template <int FMT>
-__device__ __forceinline__ ChunkQ chunk_q_ring(const uint8_t* row_scales, int c) {
+__device__ __forceinline__ ChunkQ chunk_q_ring(const uint8_t* row_scales, int c, float t = 1.f) {
   ChunkQ q{1.f, 0.f};
-  if constexpr (FMT == PMOE_FP8_BLOCK128) {
+  if constexpr (FMT == PMOE_NVFP4) {
+    const uint32_t b = reinterpret_cast<const uint16_t*>(row_scales)[c];  // blocks 2c and 2c + 1
+    q.s = e4m3_f32(b & 0xffu) * t;
+    q.z = e4m3_f32(b >> 8) * t;
+  } else if constexpr (FMT == PMOE_FP8_BLOCK128) {
     q.s = reinterpret_cast<const float*>(row_scales)[(c * 16) >> 7];
   } else if constexpr (FMT == PMOE_MXFP4) {
     q.s = e8m0_f32(row_scales[c]);  // one byte per block of 32 inputs: chunk c is block c

@@ -286,7 +286,7 @@ __global__ void __launch_bounds__(kDfThreads, 1) decode_stack_kernel(const StArg
   const int r_hi = (int)((long long)a.H * (blockIdx.x + 1) / G);
   const size_t rbg = (size_t)a.H * Fmt<FMT>::BPE2 / 2;  // one gate (or up) row
   const size_t rbd = (size_t)a.I * Fmt<FMT>::BPE2 / 2;  // one down row
-  const int rsg = (a.H / 128) * 4, rsd = (a.I / 128) * 4;  // one scale row of gate/up, of down
+  const int rsg = row_scale_bytes(FMT, a.H), rsd = row_scale_bytes(FMT, a.I);  // one scale row of gate/up, of down
   // tags: layer l's h words carry its plan epoch (wave 0, part 0, as in the single-layer
   // kernel); the words of h_l carry the same epoch with part 3, which no h word uses
   auto layer_epoch = [&](int l) {
@@ -478,6 +478,12 @@ __global__ void __launch_bounds__(kDfThreads, 1) decode_stack_kernel(const StArg
         const uint8_t* src = store + (size_t)we.x * a.stride;
         uint8_t* dst = arena + (size_t)we.y * a.stride;
         const int z = cd.z, n = cd.w;
+        // NVFP4: the matrix's 16-byte tensor-scale header (just before its block scales),
+        // loaded first so that its host-link round trip overlaps the rows' and stored last
+        uint32_t hdr = 0;
+        const size_t hdr_off = ((cd.x & 3) == 1 ? a.lay.gu_s : a.lay.d_s) - 16;
+        if constexpr (FMT == PMOE_NVFP4)
+          if (vl < 4) hdr = *reinterpret_cast<const uint32_t*>(src + hdr_off + 4 * vl);
         if ((cd.x & 3) == 1) {
           lanes_copy16x2(src, dst, a.lay.gu_w + (size_t)z * rbg, (size_t)n * rbg, a.lay.gu_w + (size_t)(a.I + z) * rbg,
                          (size_t)n * rbg, vl, nl);
@@ -491,6 +497,11 @@ __global__ void __launch_bounds__(kDfThreads, 1) decode_stack_kernel(const StArg
             const size_t row = 4 * (size_t)hb;  // one row's scale bytes
             lanes_copy4(src, dst, a.lay.gu_s + (size_t)z * row, (size_t)n * row, vl, nl);
             lanes_copy4(src, dst, a.lay.gu_s + (size_t)(a.I + z) * row, (size_t)n * row, vl, nl);
+          } else if constexpr (FMT == PMOE_NVFP4) {
+            // twice those rows' bytes (an e4m3 scale per 16 inputs): 8 loads in flight per lane
+            const size_t row = (size_t)row_scale_bytes(FMT, a.H);
+            lanes_copy4x2(src, dst, a.lay.gu_s + (size_t)z * row, (size_t)n * row, a.lay.gu_s + (size_t)(a.I + z) * row,
+                          (size_t)n * row, vl, nl);
           }
         } else {
           lanes_copy16x2(src, dst, a.lay.d_w + (size_t)z * rbd, (size_t)n * rbd, 0, 0, vl, nl);
@@ -501,8 +512,13 @@ __global__ void __launch_bounds__(kDfThreads, 1) decode_stack_kernel(const StArg
           } else if constexpr (FMT == PMOE_INT4_GPTQ_G128 || FMT == PMOE_MXFP4) {
             const size_t row = 4 * (size_t)ib;
             lanes_copy4(src, dst, a.lay.d_s + (size_t)z * row, (size_t)n * row, vl, nl);
+          } else if constexpr (FMT == PMOE_NVFP4) {
+            const size_t row = (size_t)row_scale_bytes(FMT, a.I);
+            lanes_copy4x2(src, dst, a.lay.d_s + (size_t)z * row, (size_t)n * row, 0, 0, vl, nl);
           }
         }
+        if constexpr (FMT == PMOE_NVFP4)
+          if (vl < 4) *reinterpret_cast<uint32_t*>(dst + hdr_off + 4 * vl) = hdr;
         // the stores (generic proxy) are read next by bulk copies (async proxy)
         asm volatile("fence.proxy.async.global;" ::: "memory");
         pagers_sync();
@@ -550,6 +566,17 @@ __global__ void __launch_bounds__(kDfThreads, 1) decode_stack_kernel(const StArg
         if (tid == 0) ST_CHUNK(kk, 1);
         const int4 we = we_l[cd.y];
         const uint8_t* st = ring + s_off[s];
+        // NVFP4: the chunk's matrix's tensor scale, in the 16-byte header before its block
+        // scales in the slot (an expert this launch pages in: written by this CTA's pagers
+        // before the chunk's progress, which the producer acquired before its copies)
+        float tsc = 1.f;
+        if constexpr (FMT == PMOE_NVFP4) {
+          if (cd.w > 0) {
+            const uint8_t* arena_l = *reinterpret_cast<uint8_t* const*>(m + 4);
+            const uint8_t* hdr = arena_l + (size_t)we.y * a.stride + (kind == 1 ? a.lay.gu_s : a.lay.d_s) - 16;
+            asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(tsc) : "l"(hdr));
+          }
+        }
         if (kind == 1) {
           for (int rp = first; rp < cd.w; rp += kDfConsumerWarps) {
             const uint4* grow = reinterpret_cast<const uint4*>(st + (size_t)rp * rbg);
@@ -589,8 +616,8 @@ __global__ void __launch_bounds__(kDfThreads, 1) decode_stack_kernel(const StArg
                 for (int c = 0; c < NCH1; ++c) {
                   const int idx = lane + 32 * c;
                   if (idx < nch1) {
-                    const ChunkQ qg = chunk_q_ring<FMT>(sgr, idx);
-                    const ChunkQ qu = chunk_q_ring<FMT>(sur, idx);
+                    const ChunkQ qg = chunk_q_ring<FMT>(sgr, idx, tsc);
+                    const ChunkQ qu = chunk_q_ring<FMT>(sur, idx, tsc);
                     g += chunk_dot<FMT, kSrcShared>(gw[c], xr + idx * (EPC / 8), qg);
                     u += chunk_dot<FMT, kSrcShared>(uw[c], xr + idx * (EPC / 8), qu);
                   }
@@ -624,7 +651,7 @@ __global__ void __launch_bounds__(kDfThreads, 1) decode_stack_kernel(const StArg
               for (int c = 0; c < NCH2; ++c) {
                 const int idx = lane + 32 * c;
                 if (idx < nch2) {
-                  const ChunkQ qd = chunk_q_ring<FMT>(sdr, idx);
+                  const ChunkQ qd = chunk_q_ring<FMT>(sdr, idx, tsc);
                   if (pi < a.T) {
                     acc += chunk_dot<FMT, kSrcShared>(lds128(row + idx), hsv + (size_t)pi * (a.I / 8) + idx * (EPC / 8),
                                                       qd);
@@ -767,6 +794,10 @@ cudaError_t launch_decode_stack(int fmt, const __nv_bfloat16* x, __nv_bfloat16* 
   a.cd = g.cd;
   a.stride = stride;
   a.lay = expert_layout(fmt, H, I);
+  if (fmt == PMOE_NVFP4) {  // the kernel's scale regions start after the 16-byte tensor-scale headers
+    a.lay.gu_s += 16;
+    a.lay.d_s += 16;
+  }
   a.err = err;
   const size_t smem = g.ring + g.fixed;
   const int nch1 = (int)(st_row_bytes(fmt, H) / 16), nch2 = (int)(st_row_bytes(fmt, I) / 16);
@@ -784,6 +815,9 @@ cudaError_t launch_decode_stack(int fmt, const __nv_bfloat16* x, __nv_bfloat16* 
   } else if (fmt == PMOE_MXFP4) {
     if (nch1 <= 32 * 2 && nch2 <= 32 * 1) PMOE_ST(PMOE_MXFP4, 2, 1);
     if (nch1 <= 32 * 4 && nch2 <= 32 * 2) PMOE_ST(PMOE_MXFP4, 4, 2);
+  } else if (fmt == PMOE_NVFP4) {
+    if (nch1 <= 32 * 2 && nch2 <= 32 * 1) PMOE_ST(PMOE_NVFP4, 2, 1);
+    if (nch1 <= 32 * 4 && nch2 <= 32 * 2) PMOE_ST(PMOE_NVFP4, 4, 2);
   }
 #undef PMOE_ST
   return cudaErrorInvalidValue;

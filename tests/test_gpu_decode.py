@@ -226,9 +226,10 @@ def test_decode_mxfp4_layer(pm, B, mode):
 @pytest.mark.parametrize("B,mode", [(1, 0), (2, 1), (4, 1)])
 def test_decode_nvfp4_layer(pm, B, mode):
     """NVFP4 experts (E2M1 codes, e4m3 scale per 16 inputs, fp32 tensor scale per matrix),
-    Qwen3 shape with 64 experts, through the GEMV decode kernels; SM-pull mode pages the
-    experts in with the pull kernel. B=4 at K=24 runs several waves in some steps. Bit for
-    bit equal to K=64 (everything resident)."""
+    Qwen3 shape with 64 experts; SM-pull mode pages the experts in inside the fused
+    decode kernel (block scales with the rows, the tensor-scale headers with them). B=4 at
+    K=24 runs several waves in some steps. Bit for bit equal to K=64 (everything
+    resident)."""
     L, steps, ys = _decode_case(pm, 4, 64, 24, B, 8, seed=51 + B, mode=mode)
     _assert_bitwise_equal_to_all_resident(L, steps, ys, B, mode=mode)
 

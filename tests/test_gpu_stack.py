@@ -81,10 +81,9 @@ def test_int4_stack_against_oracle_and_without_prefetch(pm, B, mode):
 
 @pytest.mark.parametrize("fmt", [0, 1, 3, 4])
 def test_one_launch_stack_equals_per_layer_calls(pm, fmt):
-    """bf16, block-FP8 and MXFP4 experts: the persistent stack launch (every layer one
-    wave: B * top_k = 8 <= K = 12) equals one forward call per layer with residual = input,
-    bit for bit, step after step, and the tables agree. NVFP4 layers, which decode through
-    the GEMV kernels, take the stack call's per-layer path: the same equality."""
+    """bf16, block-FP8, MXFP4 and NVFP4 experts: the persistent stack launch (every layer
+    one wave: B * top_k = 8 <= K = 12) equals one forward call per layer with residual =
+    input, bit for bit, step after step, and the tables agree."""
     L, E, k, H, I, K, B, steps = 3, 32, 4, 512, 256, 12, 2, 4
     layers = [hz.SyntheticLayer(fmt, E, H, I, seed=620 + fmt, layer=l) for l in range(L)]
     traces, logits, xs = _stack_inputs(L, E, k, H, B, steps, seed=630 + fmt)
