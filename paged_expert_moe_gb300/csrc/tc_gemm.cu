@@ -40,6 +40,7 @@ namespace {
 
 constexpr int kBK = 64;             // K elements per stage (128 bytes of bf16 = one swizzle row)
 constexpr int kTileRowsB = 32;      // rows per TMA box of the pair operand
+constexpr int kBigRowsB = 128;      // rows per box of a tile's whole 128-pair chunks (tiles of >= 128 pairs)
 constexpr long long kWaitLimit = 4000000000LL;  // clock64 cycles (~2 s) before a wait gives up
 constexpr int32_t kErrTcTimeout = 16;
 
@@ -223,6 +224,7 @@ __device__ __forceinline__ int epi_bar_or(int pred) {
 template <bool GATEUP, int FMT, int NMAX>
 __global__ void __launch_bounds__(TcCfg<FMT, NMAX>::kThreads, 1)
     tc_grouped_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_b,
+                      const __grid_constant__ CUtensorMap map_bb,
                       const int32_t* __restrict__ plan, int E, int wave, int sub, Workspace ws, int I, int H,
                       const uint8_t* __restrict__ arena, size_t stride, ExpertLayout lay, int32_t* __restrict__ err) {
   using C = TcCfg<FMT, NMAX>;
@@ -288,6 +290,7 @@ __global__ void __launch_bounds__(TcCfg<FMT, NMAX>::kThreads, 1)
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     prefetch_map(&map_w);
     prefetch_map(&map_b);
+    prefetch_map(&map_bb);
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_holder)),
@@ -299,6 +302,14 @@ __global__ void __launch_bounds__(TcCfg<FMT, NMAX>::kThreads, 1)
   __syncthreads();
   fence_after();
   const uint32_t tmem = *tmem_holder;
+  // a tile's pair rows (bf16 operand tiles): more than 64 of them in 128-row boxes, the
+  // last box reading past the tile (rows no MMA column uses; at most NMAX rows in all),
+  // fewer in 32-row boxes
+  auto b_boxes = [&](int np, int* nbig, int* nsmall) {
+    const bool big = NMAX >= kBigRowsB && np > 64;
+    *nbig = big ? (np + kBigRowsB - 1) / kBigRowsB : 0;
+    *nsmall = big ? 0 : (np + kTileRowsB - 1) / kTileRowsB;
+  };
 
   if (warp == 0 && !kQuant) {
     if (lane == 0) {
@@ -309,8 +320,10 @@ __global__ void __launch_bounds__(TcCfg<FMT, NMAX>::kThreads, 1)
       for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
         const int tile = t0 + item / m_tiles, mt = item % m_tiles;
         const int slot = ws.tiles[3 * tile + 0], pstart = ws.tiles[3 * tile + 1], np = ws.tiles[3 * tile + 2];
-        const int nb = (np + kTileRowsB - 1) / kTileRowsB;
-        const uint32_t bytes = C::kABytes + nb * kTileRowsB * kBK * 2;
+        int nbig, nsmall;
+        b_boxes(np, &nbig, &nsmall);
+        const int r0 = nbig * kBigRowsB;
+        const uint32_t bytes = C::kABytes + (r0 + nsmall * kTileRowsB) * kBK * 2;
         for (int kb = 0; kb < n_kb; ++kb) {
           if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, err)) {
             ok = false;
@@ -325,8 +338,10 @@ __global__ void __launch_bounds__(TcCfg<FMT, NMAX>::kThreads, 1)
             tma_load_3d(st, &map_w, &full[s], kb * kBK, mt * 128, slot);
           }
           uint8_t* bst = st + C::kABytes;
-          for (int b = 0; b < nb; ++b)
-            tma_load_2d(bst + b * kTileRowsB * kBK * 2, &map_b, &full[s], kb * kBK, pstart + b * kTileRowsB);
+          for (int b = 0; b < nbig; ++b)
+            tma_load_2d(bst + b * kBigRowsB * kBK * 2, &map_bb, &full[s], kb * kBK, pstart + b * kBigRowsB);
+          for (int b = 0; b < nsmall; ++b)
+            tma_load_2d(bst + (r0 + b * kTileRowsB) * kBK * 2, &map_b, &full[s], kb * kBK, pstart + r0 + b * kTileRowsB);
           if (++s == C::kStages) {
             s = 0;
             ph ^= 1u;
@@ -388,6 +403,7 @@ __global__ void __launch_bounds__(TcCfg<FMT, NMAX>::kThreads, 1)
       for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
         const int tile = t0 + item / m_tiles;
         const int pstart = ws.tiles[3 * tile + 1], np = ws.tiles[3 * tile + 2];
+        // 32-row boxes here (128-row ones measured 2-3% slower with the converter stage)
         const int nb = (np + kTileRowsB - 1) / kTileRowsB;
         for (int kb = 0; kb < n_kb; ++kb) {
           if (!mbar_wait(&bempty[b], bph ^ 1u, abort_flag, err)) {
@@ -1135,7 +1151,8 @@ cudaError_t launch_f8(const CUtensorMap& mw, const CUtensorMap& mb, const int32_
 }
 
 template <bool GATEUP, int FMT, int NMAX>
-cudaError_t launch_tc_n(const CUtensorMap& mw, const CUtensorMap& mb, const int32_t* plan, int E, int wave, int sub,
+cudaError_t launch_tc_n(const CUtensorMap& mw, const CUtensorMap& mb, const CUtensorMap& mbb, const int32_t* plan, int E,
+                        int wave, int sub,
                         const Workspace& ws, int I, int H, const uint8_t* arena, size_t stride, int num_sms,
                         int32_t* err, cudaStream_t s) {
   using C = TcCfg<FMT, NMAX>;
@@ -1147,18 +1164,20 @@ cudaError_t launch_tc_n(const CUtensorMap& mw, const CUtensorMap& mb, const int3
     attr_set = true;
   }
   tc_grouped_kernel<GATEUP, FMT, NMAX><<<num_sms, C::kThreads, C::kSmemBytes, s>>>(
-      mw, mb, plan, E, wave, sub, ws, I, H, arena, stride, expert_layout(FMT, H, I), err);
+      mw, mb, mbb, plan, E, wave, sub, ws, I, H, arena, stride, expert_layout(FMT, H, I), err);
   return cudaGetLastError();
 }
 
 // tile_n: the pair cap the grouping used for this forward's tiles (kTcSmallN or kTcMaxN)
 template <bool GATEUP, int FMT>
-cudaError_t launch_tc(const CUtensorMap& mw, const CUtensorMap& mb, const int32_t* plan, int E, int wave, int sub,
+cudaError_t launch_tc(const CUtensorMap& mw, const CUtensorMap& mb, const CUtensorMap& mbb, const int32_t* plan, int E,
+                      int wave, int sub,
                       const Workspace& ws, int I, int H, const uint8_t* arena, size_t stride, int num_sms,
                       int32_t* err, int tile_n, cudaStream_t s) {
   if (tile_n <= kTcSmallN)
-    return launch_tc_n<GATEUP, FMT, kTcSmallN>(mw, mb, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, s);
-  return launch_tc_n<GATEUP, FMT, kTcMaxN>(mw, mb, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, s);
+    return launch_tc_n<GATEUP, FMT, kTcSmallN>(mw, mb, mbb, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err,
+                                               s);
+  return launch_tc_n<GATEUP, FMT, kTcMaxN>(mw, mb, mbb, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, s);
 }
 
 }  // namespace
@@ -1240,6 +1259,18 @@ int tc_make_act_maps(int fmt, __nv_bfloat16* x_perm, __nv_bfloat16* h, size_t P,
     const cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)kTileRowsB};
     if (encode(&out->h, h, 2, dims, strides, box) != PMOE_OK) return PMOE_ECUDA;
   }
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)H, (cuuint64_t)P};
+    const cuuint64_t strides[1] = {(cuuint64_t)H * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)kBigRowsB};
+    if (encode(&out->xb, x_perm, 2, dims, strides, box) != PMOE_OK) return PMOE_ECUDA;
+  }
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)I, (cuuint64_t)P};
+    const cuuint64_t strides[1] = {(cuuint64_t)I * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)kBigRowsB};
+    if (encode(&out->hb, h, 2, dims, strides, box) != PMOE_OK) return PMOE_ECUDA;
+  }
   return PMOE_OK;
 }
 
@@ -1249,15 +1280,15 @@ cudaError_t tc_gateup(int fmt, const TcMaps& wm, const TcMaps& am, const int32_t
   if (tc_fp8_planes(fmt, tile_n))
     return launch_f8<true>(wm.gu8, am.x8, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, tile_n, s);
   if (fmt == PMOE_FP8_BLOCK128)
-    return launch_tc<true, PMOE_FP8_BLOCK128>(wm.gu, am.x, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, tile_n, s);
+    return launch_tc<true, PMOE_FP8_BLOCK128>(wm.gu, am.x, am.xb, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, tile_n, s);
   if (fmt == PMOE_INT4_GPTQ_G128)
-    return launch_tc<true, PMOE_INT4_GPTQ_G128>(wm.gu, am.x, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, tile_n,
+    return launch_tc<true, PMOE_INT4_GPTQ_G128>(wm.gu, am.x, am.xb, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, tile_n,
                                                 s);
   if (fmt == PMOE_NVFP4)
-    return launch_tc<true, PMOE_NVFP4>(wm.gu, am.x, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, tile_n, s);
+    return launch_tc<true, PMOE_NVFP4>(wm.gu, am.x, am.xb, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, tile_n, s);
   if (fmt == PMOE_MXFP4)
-    return launch_tc<true, PMOE_MXFP4>(wm.gu, am.x, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, tile_n, s);
-  return launch_tc<true, PMOE_BF16>(wm.gu, am.x, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, tile_n, s);
+    return launch_tc<true, PMOE_MXFP4>(wm.gu, am.x, am.xb, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, tile_n, s);
+  return launch_tc<true, PMOE_BF16>(wm.gu, am.x, am.xb, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, tile_n, s);
 }
 
 cudaError_t tc_down(int fmt, const TcMaps& wm, const TcMaps& am, const int32_t* plan, int E, int wave, int sub,
@@ -1266,15 +1297,15 @@ cudaError_t tc_down(int fmt, const TcMaps& wm, const TcMaps& am, const int32_t* 
   if (tc_fp8_planes(fmt, tile_n))
     return launch_f8<false>(wm.d8, am.h8, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, tile_n, s);
   if (fmt == PMOE_FP8_BLOCK128)
-    return launch_tc<false, PMOE_FP8_BLOCK128>(wm.d, am.h, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, tile_n, s);
+    return launch_tc<false, PMOE_FP8_BLOCK128>(wm.d, am.h, am.hb, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, tile_n, s);
   if (fmt == PMOE_INT4_GPTQ_G128)
-    return launch_tc<false, PMOE_INT4_GPTQ_G128>(wm.d, am.h, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, tile_n,
+    return launch_tc<false, PMOE_INT4_GPTQ_G128>(wm.d, am.h, am.hb, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, tile_n,
                                                  s);
   if (fmt == PMOE_NVFP4)
-    return launch_tc<false, PMOE_NVFP4>(wm.d, am.h, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, tile_n, s);
+    return launch_tc<false, PMOE_NVFP4>(wm.d, am.h, am.hb, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, tile_n, s);
   if (fmt == PMOE_MXFP4)
-    return launch_tc<false, PMOE_MXFP4>(wm.d, am.h, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, tile_n, s);
-  return launch_tc<false, PMOE_BF16>(wm.d, am.h, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, tile_n, s);
+    return launch_tc<false, PMOE_MXFP4>(wm.d, am.h, am.hb, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, tile_n, s);
+  return launch_tc<false, PMOE_BF16>(wm.d, am.h, am.hb, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, tile_n, s);
 }
 
 }  // namespace pmoe

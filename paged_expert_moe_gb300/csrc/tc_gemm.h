@@ -13,8 +13,11 @@ constexpr int kTcSmallN = 64;  // the cap for forwards with few tokens per exper
 struct TcMaps {
   CUtensorMap gu;  // gate/up rows of every slot: dims {H (bytes if quantised), 2I, K}
   CUtensorMap d;   // down rows of every slot: dims {I (bytes if quantised), H, K}
-  CUtensorMap x;   // gathered activations x_perm: dims {H, P} bf16
-  CUtensorMap h;   // intermediate h: dims {I, P} bf16
+  CUtensorMap x;   // gathered activations x_perm: dims {H, P} bf16, 32-row boxes
+  CUtensorMap h;   // intermediate h: dims {I, P} bf16, 32-row boxes
+  // the same with 128-row boxes, for a tile's whole 128-pair chunks: each TMA instruction
+  // costs time of its own, so fewer and larger boxes stream a stage faster
+  CUtensorMap xb, hb;
   // block-FP8 on the e4m3 MMAs: weight rows in 128-byte swizzled boxes, and the two
   // e4m3 planes of x and h ({H or I, P, 2} bytes, in the bf16 buffers' place)
   CUtensorMap gu8, d8, x8, h8;
