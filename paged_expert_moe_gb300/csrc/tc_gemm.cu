@@ -97,6 +97,14 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1, int c2,
+                                            int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];"
+      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
+      : "memory");
+}
+
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
@@ -332,8 +340,7 @@ __global__ void __launch_bounds__(TcCfg<FMT, NMAX>::kThreads, 1)
           uint8_t* st = smem + s * (C::kABytes + C::kBBytes);
           mbar_arrive_expect_tx(&full[s], bytes);
           if (GATEUP) {
-            tma_load_3d(st, &map_w, &full[s], kb * kBK, mt * 64, slot);                      // gate rows
-            tma_load_3d(st + C::kABytes / 2, &map_w, &full[s], kb * kBK, I + mt * 64, slot);  // up rows
+            tma_load_4d(st, &map_w, &full[s], kb * kBK, mt * 64, 0, slot);  // 64 gate rows, then the 64 up rows
           } else {
             tma_load_3d(st, &map_w, &full[s], kb * kBK, mt * 128, slot);
           }
@@ -1117,7 +1124,7 @@ int encode(CUtensorMap* m, void* base, int rank, const cuuint64_t* dims, const c
            const cuuint32_t* box, MapKind kind = kMapBf16Sw128) {
   EncodeTiledFn fn = get_encode();
   if (fn == nullptr) return PMOE_ECUDA;
-  cuuint32_t estr[3] = {1, 1, 1};
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};  // element strides, one per dimension (rank <= 5)
   const CUresult r = fn(m, kind == kMapBf16Sw128 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8,
                         rank, base, dims, strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         kind == kMapBytes ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
@@ -1195,6 +1202,12 @@ int tc_make_weight_maps(uint8_t* arena, size_t stride, int K, int H, int I, int 
       const cuuint64_t strides[2] = {(cuuint64_t)H * 2, (cuuint64_t)stride};
       const cuuint32_t box[3] = {(cuuint32_t)kBK, 64, 1};  // 64 gate or 64 up rows
       if (encode(&out->gu, arena, 3, dims, strides, box) != PMOE_OK) return PMOE_ECUDA;
+    }
+    {
+      const cuuint64_t dims[4] = {(cuuint64_t)H, (cuuint64_t)I, 2, (cuuint64_t)K};
+      const cuuint64_t strides[3] = {(cuuint64_t)H * 2, (cuuint64_t)I * H * 2, (cuuint64_t)stride};
+      const cuuint32_t box[4] = {(cuuint32_t)kBK, 64, 2, 1};  // 64 gate rows and the matching 64 up rows
+      if (encode(&out->gu4, arena, 4, dims, strides, box) != PMOE_OK) return PMOE_ECUDA;
     }
     const cuuint64_t dims[3] = {(cuuint64_t)I, (cuuint64_t)H, (cuuint64_t)K};
     const cuuint64_t strides[2] = {(cuuint64_t)I * 2, (cuuint64_t)stride};
@@ -1288,7 +1301,7 @@ cudaError_t tc_gateup(int fmt, const TcMaps& wm, const TcMaps& am, const int32_t
     return launch_tc<true, PMOE_NVFP4>(wm.gu, am.x, am.xb, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, tile_n, s);
   if (fmt == PMOE_MXFP4)
     return launch_tc<true, PMOE_MXFP4>(wm.gu, am.x, am.xb, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, tile_n, s);
-  return launch_tc<true, PMOE_BF16>(wm.gu, am.x, am.xb, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, tile_n, s);
+  return launch_tc<true, PMOE_BF16>(wm.gu4, am.x, am.xb, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, tile_n, s);
 }
 
 cudaError_t tc_down(int fmt, const TcMaps& wm, const TcMaps& am, const int32_t* plan, int E, int wave, int sub,

@@ -21,6 +21,9 @@ struct TcMaps {
   // block-FP8 on the e4m3 MMAs: weight rows in 128-byte swizzled boxes, and the two
   // e4m3 planes of x and h ({H or I, P, 2} bytes, in the bf16 buffers' place)
   CUtensorMap gu8, d8, x8, h8;
+  // bf16 gate/up rows as {H, I, 2 (gate, up), K}: one box holds a tile's 64 gate rows and
+  // the matching 64 up rows
+  CUtensorMap gu4;
 };
 
 bool tc_supported(int H, int I);
