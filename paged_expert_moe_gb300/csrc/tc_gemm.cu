@@ -771,6 +771,7 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
 template <bool GATEUP>
 __global__ void __launch_bounds__(F8Cfg::kThreads, 1)
     tc_fp8_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_b,
+                  const __grid_constant__ CUtensorMap map_bb,
                   const int32_t* __restrict__ plan, int E, int wave, int sub, Workspace ws, int I, int H,
                   const uint8_t* __restrict__ arena, size_t stride, ExpertLayout lay, int32_t* __restrict__ err) {
   using C = F8Cfg;
@@ -822,6 +823,7 @@ __global__ void __launch_bounds__(F8Cfg::kThreads, 1)
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     prefetch_map(&map_w);
     prefetch_map(&map_b);
+    prefetch_map(&map_bb);
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_holder)),
@@ -833,6 +835,8 @@ __global__ void __launch_bounds__(F8Cfg::kThreads, 1)
   __syncthreads();
   fence_after();
   const uint32_t tmem = *tmem_holder;
+  // rows of each activation plane a tile's stage holds: 32 or 64 (one box of both planes)
+  auto plane_rows = [](int np) { return np <= 32 ? 32 : 64; };
 
   if (warp == 0 || warp == 10) {
     if (lane == 0) {
@@ -848,7 +852,7 @@ __global__ void __launch_bounds__(F8Cfg::kThreads, 1)
       for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
         const int tile = t0 + item / m_tiles, mt = item % m_tiles;
         const int slot = ws.tiles[3 * tile + 0], pstart = ws.tiles[3 * tile + 1], np = ws.tiles[3 * tile + 2];
-        const int nb = (np + kTileRowsB - 1) / kTileRowsB;
+        const int nst = plane_rows(np);
         for (int kb = 0; kb < n_kb; ++kb) {
           if (!mbar_wait(&emptyb[s], ph ^ 1u, abort_flag, err)) {
             ok = false;
@@ -857,28 +861,15 @@ __global__ void __launch_bounds__(F8Cfg::kThreads, 1)
           uint8_t* st = ring + s * C::kWBytes;
           if (wts) {
             mbar_arrive_expect_tx(&fullb[s], (uint32_t)C::kWBytes);
-            if (GATEUP) {
-              tma_load_3d(st, &map_w, &fullb[s], kb * C::kBK, mt * 64, slot);                      // gate rows
-              tma_load_3d(st + C::kWBytes / 2, &map_w, &fullb[s], kb * C::kBK, I + mt * 64, slot);  // up rows
-            } else {
+            if (GATEUP)
+              tma_load_4d(st, &map_w, &fullb[s], kb * C::kBK, mt * 64, 0, slot);  // 64 gate rows, then the 64 up rows
+            else
               tma_load_3d(st, &map_w, &fullb[s], kb * C::kBK, mt * 128, slot);
-            }
           } else {
-            if (GATEUP) {
-              // hi rows 0..n16-1, then the lo rows: one B operand of 2 n16 rows (16-row boxes)
-              const int n16 = (np + 15) & ~15;
-              mbar_arrive_expect_tx(&fullb[s], (uint32_t)(2 * n16 * C::kBK));
-              for (int pl = 0; pl < 2; ++pl)
-                for (int b = 0; b < n16; b += 16)
-                  tma_load_3d(st + (pl * n16 + b) * C::kBK, &map_b, &fullb[s], kb * C::kBK, pstart + b, pl);
-            } else {
-              // the two planes kPlaneBytes apart (32-row boxes)
-              mbar_arrive_expect_tx(&fullb[s], (uint32_t)(2 * nb * kTileRowsB * C::kBK));
-              for (int pl = 0; pl < 2; ++pl)
-                for (int b = 0; b < nb; ++b)
-                  tma_load_3d(st + pl * C::kPlaneBytes + b * kTileRowsB * C::kBK, &map_b, &fullb[s], kb * C::kBK,
-                              pstart + b * kTileRowsB, pl);
-            }
+            // one box: nst hi rows, then nst lo rows (rows past the tile feed MMA columns no
+            // one reads)
+            mbar_arrive_expect_tx(&fullb[s], (uint32_t)(2 * nst * C::kBK));
+            tma_load_3d(st, nst == 32 ? &map_b : &map_bb, &fullb[s], kb * C::kBK, pstart, 0);
           }
           if (++s == depth) {
             s = 0;
@@ -910,7 +901,8 @@ __global__ void __launch_bounds__(F8Cfg::kThreads, 1)
         const int tile = t0 + item / m_tiles;
         const int np = ws.tiles[3 * tile + 2];
         const int n_mma = (np + 15) & ~15;
-        const uint32_t idesc = idesc_e4m3(128, (GATEUP ? 2 : 1) * (n_mma < 16 ? 16 : n_mma));
+        const int nst = plane_rows(np);
+        const uint32_t idesc = idesc_e4m3(128, GATEUP ? 2 * nst : (n_mma < 16 ? 16 : n_mma));
         for (int kb = 0; kb < n_kb; ++kb) {
           if (!mbar_wait(&wfull[sw], wph, abort_flag, err) || !mbar_wait(&xfull[sx], xph, abort_flag, err)) {
             ok = false;
@@ -918,7 +910,7 @@ __global__ void __launch_bounds__(F8Cfg::kThreads, 1)
           }
           fence_after();
           const uint32_t a0 = smem_u32(wring + sw * C::kWBytes);
-          const uint32_t bh = smem_u32(xring + sx * C::kXBytes), bl = bh + C::kPlaneBytes;
+          const uint32_t bh = smem_u32(xring + sx * C::kXBytes), bl = bh + (uint32_t)(nst * C::kBK);
           for (int u = 0; u < kUnits; ++u) {
             int rr = g ? r1 : r0;
             uint32_t rp = g ? rph1 : rph0;
@@ -1020,8 +1012,8 @@ __global__ void __launch_bounds__(F8Cfg::kThreads, 1)
                 uint32_t v[32];
                 tmem_ld32(tmem + tlane + (uint32_t)(pb * kPartCols + 32 * h2), v);
                 if (GATEUP) {
-                  uint32_t u[32];  // the lo plane's columns, n_mma after the hi plane's
-                  tmem_ld32(tmem + tlane + (uint32_t)(pb * kPartCols + n_mma + 32 * h2), u);
+                  uint32_t u[32];  // the lo plane's columns, plane_rows(np) after the hi plane's
+                  tmem_ld32(tmem + tlane + (uint32_t)(pb * kPartCols + plane_rows(np) + 32 * h2), u);
                   tmem_wait_ld();
 #pragma unroll
                   for (int i = 0; i < 32; ++i)
@@ -1133,7 +1125,8 @@ int encode(CUtensorMap* m, void* base, int rank, const cuuint64_t* dims, const c
 }
 
 template <bool GATEUP>
-cudaError_t launch_f8_n(const CUtensorMap& mw, const CUtensorMap& mb, const int32_t* plan, int E, int wave, int sub,
+cudaError_t launch_f8_n(const CUtensorMap& mw, const CUtensorMap& mb, const CUtensorMap& mbb, const int32_t* plan, int E,
+                        int wave, int sub,
                         const Workspace& ws, int I, int H, const uint8_t* arena, size_t stride, int num_sms,
                         int32_t* err, cudaStream_t s) {
   static bool attr_set = false;
@@ -1144,17 +1137,18 @@ cudaError_t launch_f8_n(const CUtensorMap& mw, const CUtensorMap& mb, const int3
     attr_set = true;
   }
   tc_fp8_kernel<GATEUP><<<num_sms, F8Cfg::kThreads, F8Cfg::kSmemBytes, s>>>(
-      mw, mb, plan, E, wave, sub, ws, I, H, arena, stride, expert_layout(PMOE_FP8_BLOCK128, H, I), err);
+      mw, mb, mbb, plan, E, wave, sub, ws, I, H, arena, stride, expert_layout(PMOE_FP8_BLOCK128, H, I), err);
   return cudaGetLastError();
 }
 
 // block-FP8 with the small pair cap (tc_fp8_planes)
 template <bool GATEUP>
-cudaError_t launch_f8(const CUtensorMap& mw, const CUtensorMap& mb, const int32_t* plan, int E, int wave, int sub,
+cudaError_t launch_f8(const CUtensorMap& mw, const CUtensorMap& mb, const CUtensorMap& mbb, const int32_t* plan, int E,
+                      int wave, int sub,
                       const Workspace& ws, int I, int H, const uint8_t* arena, size_t stride, int num_sms,
                       int32_t* err, int tile_n, cudaStream_t s) {
   if (tile_n > F8Cfg::kN) return cudaErrorInvalidValue;
-  return launch_f8_n<GATEUP>(mw, mb, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, s);
+  return launch_f8_n<GATEUP>(mw, mb, mbb, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, s);
 }
 
 template <bool GATEUP, int FMT, int NMAX>
@@ -1219,10 +1213,11 @@ int tc_make_weight_maps(uint8_t* arena, size_t stride, int K, int H, int I, int 
   if (fmt == PMOE_FP8_BLOCK128) {
     // e4m3 rows as MMA operands: 128-byte boxes (128 K), 128-byte swizzle
     {
-      const cuuint64_t dims[3] = {(cuuint64_t)H, (cuuint64_t)(2 * I), (cuuint64_t)K};
-      const cuuint64_t strides[2] = {(cuuint64_t)H, (cuuint64_t)stride};
-      const cuuint32_t box[3] = {128, 64, 1};
-      if (encode(&out->gu8, arena + lay.gu_w, 3, dims, strides, box, kMapBytesSw128) != PMOE_OK) return PMOE_ECUDA;
+      // {H, I, 2 (gate, up), K}: one box holds a tile's 64 gate rows and the matching 64 up rows
+      const cuuint64_t dims[4] = {(cuuint64_t)H, (cuuint64_t)I, 2, (cuuint64_t)K};
+      const cuuint64_t strides[3] = {(cuuint64_t)H, (cuuint64_t)I * H, (cuuint64_t)stride};
+      const cuuint32_t box[4] = {128, 64, 2, 1};
+      if (encode(&out->gu8, arena + lay.gu_w, 4, dims, strides, box, kMapBytesSw128) != PMOE_OK) return PMOE_ECUDA;
     }
     const cuuint64_t dims[3] = {(cuuint64_t)I, (cuuint64_t)H, (cuuint64_t)K};
     const cuuint64_t strides[2] = {(cuuint64_t)I, (cuuint64_t)stride};
@@ -1248,17 +1243,22 @@ int tc_make_weight_maps(uint8_t* arena, size_t stride, int K, int H, int I, int 
 
 int tc_make_act_maps(int fmt, __nv_bfloat16* x_perm, __nv_bfloat16* h, size_t P, int H, int I, TcMaps* out) {
   if (fmt == PMOE_FP8_BLOCK128) {
-    // the two e4m3 planes of x and of h, [2][P][cols] bytes in the bf16 buffers' place
-    {
-      const cuuint64_t dims[3] = {(cuuint64_t)H, (cuuint64_t)P, 2};
-      const cuuint64_t strides[2] = {(cuuint64_t)H, (cuuint64_t)H * P};
-      const cuuint32_t box[3] = {128, 16, 1};
-      if (encode(&out->x8, x_perm, 3, dims, strides, box, kMapBytesSw128) != PMOE_OK) return PMOE_ECUDA;
+    // the two e4m3 planes of x and of h, [2][P][cols] bytes in the bf16 buffers' place; a box
+    // spans both planes (32 or 64 rows of each)
+    for (int big = 0; big < 2; ++big) {
+      const cuuint32_t rows = big ? 64 : 32;
+      {
+        const cuuint64_t dims[3] = {(cuuint64_t)H, (cuuint64_t)P, 2};
+        const cuuint64_t strides[2] = {(cuuint64_t)H, (cuuint64_t)H * P};
+        const cuuint32_t box[3] = {128, rows, 2};
+        if (encode(big ? &out->x8b : &out->x8, x_perm, 3, dims, strides, box, kMapBytesSw128) != PMOE_OK)
+          return PMOE_ECUDA;
+      }
+      const cuuint64_t dims[3] = {(cuuint64_t)I, (cuuint64_t)P, 2};
+      const cuuint64_t strides[2] = {(cuuint64_t)I, (cuuint64_t)I * P};
+      const cuuint32_t box[3] = {128, rows, 2};
+      if (encode(big ? &out->h8b : &out->h8, h, 3, dims, strides, box, kMapBytesSw128) != PMOE_OK) return PMOE_ECUDA;
     }
-    const cuuint64_t dims[3] = {(cuuint64_t)I, (cuuint64_t)P, 2};
-    const cuuint64_t strides[2] = {(cuuint64_t)I, (cuuint64_t)I * P};
-    const cuuint32_t box[3] = {128, (cuuint32_t)kTileRowsB, 1};
-    if (encode(&out->h8, h, 3, dims, strides, box, kMapBytesSw128) != PMOE_OK) return PMOE_ECUDA;
   }
   {
     const cuuint64_t dims[2] = {(cuuint64_t)H, (cuuint64_t)P};
@@ -1291,7 +1291,7 @@ cudaError_t tc_gateup(int fmt, const TcMaps& wm, const TcMaps& am, const int32_t
                       const Workspace& ws, int I, int H, const uint8_t* arena, size_t stride, int num_sms,
                       int32_t* err, int tile_n, cudaStream_t s) {
   if (tc_fp8_planes(fmt, tile_n))
-    return launch_f8<true>(wm.gu8, am.x8, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, tile_n, s);
+    return launch_f8<true>(wm.gu8, am.x8, am.x8b, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, tile_n, s);
   if (fmt == PMOE_FP8_BLOCK128)
     return launch_tc<true, PMOE_FP8_BLOCK128>(wm.gu, am.x, am.xb, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, tile_n, s);
   if (fmt == PMOE_INT4_GPTQ_G128)
@@ -1308,7 +1308,7 @@ cudaError_t tc_down(int fmt, const TcMaps& wm, const TcMaps& am, const int32_t* 
                     const Workspace& ws, int I, int H, const uint8_t* arena, size_t stride, int num_sms, int32_t* err,
                     int tile_n, cudaStream_t s) {
   if (tc_fp8_planes(fmt, tile_n))
-    return launch_f8<false>(wm.d8, am.h8, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, tile_n, s);
+    return launch_f8<false>(wm.d8, am.h8, am.h8b, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, tile_n, s);
   if (fmt == PMOE_FP8_BLOCK128)
     return launch_tc<false, PMOE_FP8_BLOCK128>(wm.d, am.h, am.hb, plan, E, wave, sub, ws, I, H, arena, stride, num_sms, err, tile_n, s);
   if (fmt == PMOE_INT4_GPTQ_G128)

@@ -19,8 +19,9 @@ struct TcMaps {
   // costs time of its own, so fewer and larger boxes stream a stage faster
   CUtensorMap xb, hb;
   // block-FP8 on the e4m3 MMAs: weight rows in 128-byte swizzled boxes, and the two
-  // e4m3 planes of x and h ({H or I, P, 2} bytes, in the bf16 buffers' place)
-  CUtensorMap gu8, d8, x8, h8;
+  // e4m3 planes of x and h ({H or I, P, 2} bytes, in the bf16 buffers' place; one box holds
+  // 32 (x8, h8) or 64 (x8b, h8b) rows of both planes, the lo rows after the hi rows)
+  CUtensorMap gu8, d8, x8, h8, x8b, h8b;
   // bf16 gate/up rows as {H, I, 2 (gate, up), K}: one box holds a tile's 64 gate rows and
   // the matching 64 up rows
   CUtensorMap gu4;
