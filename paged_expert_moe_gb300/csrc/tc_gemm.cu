@@ -14,7 +14,10 @@
 //   down     D[128 rows n][N pairs] = W_d[n0:n0+128, :] . h[pairs, :]^T; the epilogue
 //            writes the fp32 partial o_part[pair][n].          K = I, BK = 64
 // The two TMEM accumulator buffers (2 x 256 columns) let the epilogue of one item run
-// while the MMAs of the next fill the other buffer; 4 TMA stages of 48 KB.
+// while the MMAs of the next fill the other buffer; 4 TMA stages of 48 KB. Every TMA
+// instruction costs time of its own, so a bf16 stage is few boxes: gate/up's weight tile
+// as one 4-D box (64 gate rows, then the 64 up rows), a tile of more than 64 pairs in
+// 128-row boxes.
 // N = the tile's pair count rounded up to 16 (<= 256): the instruction descriptor is
 // built per tile, so no MMA work is spent on other experts' pairs beyond that.
 // Warp roles: warp 0 lane 0 issues TMA, warp 1 lane 0 issues tcgen05.mma (warp 1 owns
@@ -713,7 +716,9 @@ __global__ void __launch_bounds__(TcCfg<FMT, NMAX>::kThreads, 1)
 // at most kTcSmallN = 64 pairs. Two promotion groups of four warps take the items in turn,
 // each with its own ring of partial buffers, so one group's epilogue overlaps the other's
 // MMAs. The weight tiles (the HBM stream) and the activation planes (re-read by every
-// m-tile, from L2) have rings and producers of their own, the weights' the deeper one.
+// m-tile, from L2) have rings and producers of their own, the weights' the deeper one; a
+// stage is one TMA box in each (gate/up's weights as a 4-D box of gate and up rows; both
+// planes as one box of 32 or 64 rows each, the lo rows after the hi rows).
 // Warps: 0 TMA weights, 1 MMA issuer (owns the TMEM), 2-5 and 6-9 promotion groups 0 and 1
 // (TMEM lanes 32*(warp%4)..), 10 TMA activation planes.
 struct F8Cfg {
