@@ -725,8 +725,8 @@ struct F8Cfg {
   // TMEM partial buffers per group: gate/up stacks the hi and lo planes as one 2N-row
   // operand (one MMA per K step, 2 x 128 columns); down keeps them apart (two MMAs per
   // K step into 4 x 64 columns: it has two K units per stage)
-  template <bool GATEUP> static constexpr int kParts = GATEUP ? 2 : 4;
-  template <bool GATEUP> static constexpr int kPartCols = GATEUP ? 128 : 64;
+  static constexpr int parts(bool gateup) { return gateup ? 2 : 4; }
+  static constexpr int part_cols(bool gateup) { return gateup ? 128 : 64; }
   static constexpr int kN = 64;                   // pairs per tile (MMA N at most)
   static constexpr int kBK = 128;                 // K per stage (one byte each)
   static constexpr int kWBytes = 128 * kBK;       // weight tile, 128 rows
@@ -783,7 +783,7 @@ __global__ void __launch_bounds__(F8Cfg::kThreads, 1)
   constexpr int kN = C::kN;
   constexpr int kUnits = GATEUP ? 1 : 2;  // partial buffers per stage
   constexpr int kSteps = 4 / kUnits;      // K = 32 MMA steps per unit
-  constexpr int kParts = C::template kParts<GATEUP>, kPartCols = C::template kPartCols<GATEUP>;
+  constexpr int kParts = C::parts(GATEUP), kPartCols = C::part_cols(GATEUP);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* wring = smem;
