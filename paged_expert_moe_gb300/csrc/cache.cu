@@ -862,7 +862,8 @@ int moe_paged_forward(pmoe_cache* c, int layer, const void* x, int T, const int3
     // turned out to have one wave (the fused kernel then already wrote y)
     KernelMark km(c, PMOE_K_COMBINE, s);
     PMOE_CUDA(launch_combine(c->ws, w, (const __nv_bfloat16*)residual, (__nv_bfloat16*)y, T, k, H, s,
-                             (fused && !ce && !split0) ? c->plan_dev[layer] : nullptr));
+                             (fused && !ce && !split0) ? c->plan_dev[layer] : nullptr,
+                             tc && tc_o_part_bf16(c->d.format, tc_tile_n(T, k, E))));
   }
   // (under graph capture the graph's own order takes this event's place, and an event
   // recorded into a graph could not be waited on or queried outside it)

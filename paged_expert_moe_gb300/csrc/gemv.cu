@@ -143,7 +143,9 @@ __global__ void __launch_bounds__(256) gemv_down_kernel(int H, int I, const int3
 }
 
 // y[t][n] = bf16(residual[t][n] + sum_r w[t][r] * o_part[pos[t*k+r]][n]), ranks in order.
-__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ o_part, const int32_t* __restrict__ pos,
+// o_part rows are fp32 (decode kernels) or bf16 (tensor-core prefill kernels: BF16_PART).
+template <bool BF16_PART>
+__global__ void __launch_bounds__(256) combine_kernel(const void* __restrict__ o_part, const int32_t* __restrict__ pos,
                                                       const float* __restrict__ w,
                                                       const __nv_bfloat16* __restrict__ residual,
                                                       __nv_bfloat16* __restrict__ y, int T, int top_k, int H,
@@ -160,16 +162,24 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
       const int p = pos[t * top_k + r];
       if (p < 0) continue;
       const float wr = w[t * top_k + r];
-      const float4* op = reinterpret_cast<const float4*>(o_part + (size_t)p * H + (size_t)c * 8);
-      const float4 a = op[0], b = op[1];
-      acc[0] = fmaf(wr, a.x, acc[0]);
-      acc[1] = fmaf(wr, a.y, acc[1]);
-      acc[2] = fmaf(wr, a.z, acc[2]);
-      acc[3] = fmaf(wr, a.w, acc[3]);
-      acc[4] = fmaf(wr, b.x, acc[4]);
-      acc[5] = fmaf(wr, b.y, acc[5]);
-      acc[6] = fmaf(wr, b.z, acc[6]);
-      acc[7] = fmaf(wr, b.w, acc[7]);
+      float o[8];
+      if (BF16_PART) {
+        const uint4 q = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(o_part) +
+                                                        (size_t)p * H + (size_t)c * 8);
+        const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          o[2 * i] = bf_lo(qw[i]);
+          o[2 * i + 1] = bf_hi(qw[i]);
+        }
+      } else {
+        const float4* op = reinterpret_cast<const float4*>(static_cast<const float*>(o_part) + (size_t)p * H +
+                                                           (size_t)c * 8);
+        const float4 a = op[0], b = op[1];
+        o[0] = a.x, o[1] = a.y, o[2] = a.z, o[3] = a.w, o[4] = b.x, o[5] = b.y, o[6] = b.z, o[7] = b.w;
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = fmaf(wr, o[i], acc[i]);
     }
     if (residual != nullptr) {
       const uint4 rv = *reinterpret_cast<const uint4*>(residual + (size_t)t * H + (size_t)c * 8);
@@ -345,12 +355,15 @@ cudaError_t launch_gemv_down(int fmt, int H, int I, const int32_t* plan, int E, 
 }
 
 cudaError_t launch_combine(const Workspace& ws, const float* w, const __nv_bfloat16* residual, __nv_bfloat16* y,
-                           int T, int top_k, int H, cudaStream_t s, const int32_t* skip_plan) {
+                           int T, int top_k, int H, cudaStream_t s, const int32_t* skip_plan, bool bf16_part) {
   if (T == 0) return cudaSuccess;
   const int total = T * (H / 8);
   int blocks = (total + 255) / 256;
   if (blocks > 4096) blocks = 4096;
-  combine_kernel<<<blocks, 256, 0, s>>>(ws.o_part, ws.pos, w, residual, y, T, top_k, H, skip_plan);
+  if (bf16_part)
+    combine_kernel<true><<<blocks, 256, 0, s>>>(ws.o_part, ws.pos, w, residual, y, T, top_k, H, skip_plan);
+  else
+    combine_kernel<false><<<blocks, 256, 0, s>>>(ws.o_part, ws.pos, w, residual, y, T, top_k, H, skip_plan);
   return cudaGetLastError();
 }
 

@@ -67,7 +67,8 @@ struct Workspace {
   int32_t* tile_wave;   // [E + 2] tile range of each wave
   int32_t* tile_split;  // [E + 2] first tile of each wave's non-resident (just paged-in) experts
   __nv_bfloat16* h;     // [P][I] intermediate activations, grouped order
-  float* o_part;        // [P][H] per-pair down-projection outputs, grouped order
+  float* o_part;        // [P][H] per-pair down-projection outputs, grouped order: fp32, or
+                        // bf16 in the first half of the bytes where tc_o_part_bf16 says so
   __nv_bfloat16* x_perm;  // [P][H] tokens gathered in grouped order (tensor-core path)
   // Block-FP8 layers on the tensor path hold x_perm and h as two e4m3 planes each, in the
   // same bytes: x planes [2][p_cap][H], h planes [2][p_cap][I] (fp8_planes.cuh), with
@@ -118,7 +119,7 @@ cudaError_t launch_gemv_down(int fmt, int H, int I, const int32_t* plan, int E, 
                              cudaStream_t s);
 cudaError_t launch_combine(const Workspace& ws, const float* w, const __nv_bfloat16* residual,
                            __nv_bfloat16* y, int T, int top_k, int H, cudaStream_t s,
-                           const int32_t* skip_if_single_wave_plan = nullptr);
+                           const int32_t* skip_if_single_wave_plan = nullptr, bool bf16_part = false);
 bool decode_fused_supported(int fmt, int T, int top_k, int H, int I, int num_sms);
 // The fused decode kernels' chunking of one CTA's rows: chunks per gate/up part (cg) and
 // per down part (cd), and the ring bytes of the largest chunk.

@@ -12,7 +12,9 @@
 //            them through shared memory and writes h[pair][j0:j0+64] =
 //            bf16(silu(gate) * up) as 16-byte rows.           K = H, BK = 64
 //   down     D[128 rows n][N pairs] = W_d[n0:n0+128, :] . h[pairs, :]^T; the epilogue
-//            writes the fp32 partial o_part[pair][n].          K = I, BK = 64
+//            writes the pair's expert output o_part[pair][n]: bf16 weights as bf16
+//            rows through shared memory (half the bytes for the combine to read),
+//            quantised ones (converter warps) as fp32 rows.  K = I, BK = 64
 // The two TMEM accumulator buffers (2 x 256 columns) let the epilogue of one item run
 // while the MMAs of the next fill the other buffer; 4 TMA stages of 48 KB. Every TMA
 // instruction costs time of its own, so a bf16 stage is few boxes: gate/up's weight tile
@@ -215,6 +217,27 @@ struct TcCfg {
 };
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// Down epilogue: staging[row * 17 + i] holds the outputs of a tile's 128 weight rows for
+// its pairs c..c+15. Thread et (0..127 of the epilogue) writes pair c + (et & 15), rows
+// (et >> 4) * 16 .. +15 of m-tile mt, as bf16: two 16-byte stores, so a warp covers
+// whole 256-byte rows of o_part (the reads of staging hit 32 distinct banks).
+__device__ __forceinline__ void store_o_rows(const float* staging, int et, int c, int np, int pstart, int mt,
+                                             int H, float* o_part) {
+  const int pl = et & 15, js = (et >> 4) * 16;
+  if (c + pl >= np) return;
+  uint32_t w[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const __nv_bfloat162 b =
+        __floats2bfloat162_rn(staging[(js + 2 * j) * 17 + pl], staging[(js + 2 * j + 1) * 17 + pl]);
+    w[j] = *reinterpret_cast<const uint32_t*>(&b);
+  }
+  uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(o_part) + (size_t)(pstart + c + pl) * H +
+                                        mt * 128 + js);
+  dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+  dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+}
 
 // Named barrier over the 128 epilogue threads that also ORs a predicate across them,
 // so a failed wait in any epilogue thread makes all of them leave together.
@@ -678,7 +701,15 @@ __global__ void __launch_bounds__(TcCfg<FMT, NMAX>::kThreads, 1)
                 make_uint4(packed[0], packed[1], packed[2], packed[3]);
           }
           epi_bar();
+        } else if (!kQuant) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) staging[row * 17 + i] = __uint_as_float(v[i]);
+          epi_bar();
+          store_o_rows(staging, et, c, np, pstart, mt, H, ws.o_part);
+          epi_bar();
         } else {
+          // the converter warps bound this kernel on issue slots: fp32 rows straight from
+          // the registers cost the epilogue the fewest instructions
           const int n = mt * 128 + row;
 #pragma unroll
           for (int i = 0; i < 16; ++i)
@@ -711,7 +742,7 @@ __global__ void __launch_bounds__(TcCfg<FMT, NMAX>::kThreads, 1)
 //            x scale sx[pair], forms h = silu(gate) * up and writes h as two planes with
 //            one scale per (pair, 64 columns), hsc[m-tile][pair]
 //   down     acc += partial * s_w[row block][k block] * hsc[k unit][pair]; the epilogue
-//            writes the fp32 partial o_part[pair][n]
+//            writes o_part[pair][n] rounded to bf16, as the kernel above does
 // Tiles as in tc_grouped_kernel (swap-AB: 128 weight rows on M, the tile's pairs on N),
 // at most kTcSmallN = 64 pairs. Two promotion groups of four warps take the items in turn,
 // each with its own ring of partial buffers, so one group's epilogue overlaps the other's
@@ -1079,10 +1110,16 @@ __global__ void __launch_bounds__(F8Cfg::kThreads, 1)
           }
         }
       } else {
-        const int n = mt * 128 + row;
 #pragma unroll
-        for (int i = 0; i < kN; ++i)
-          if (i < np) ws.o_part[(size_t)(pstart + i) * H + n] = acc[i];
+        for (int cc = 0; cc < kN; cc += 16) {
+          if (cc < np) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) staging[row * 17 + i] = acc[cc + i];
+            grp_bar(g);
+            store_o_rows(staging, et, cc, np, pstart, mt, H, ws.o_part);
+            grp_bar(g);
+          }
+        }
       }
     }
   }

@@ -50,5 +50,8 @@ inline int tc_tile_n(int T, int top_k, int E) {
 // Block-FP8 forwards with small tiles run e4m3 MMAs on two-plane activations (x gathered
 // by launch_gather_rows_fp8x2); with large tiles the weights are dequantised to bf16.
 inline bool tc_fp8_planes(int fmt, int tile_n) { return fmt == PMOE_FP8_BLOCK128 && tile_n <= kTcSmallN; }
+// Whether the down GEMM writes o_part as bf16 rows (else fp32): the bf16 kernel and the
+// e4m3 kernel do; the kernels with converter warps do not.
+inline bool tc_o_part_bf16(int fmt, int tile_n) { return fmt == PMOE_BF16 || tc_fp8_planes(fmt, tile_n); }
 
 }  // namespace pmoe
