@@ -6,7 +6,7 @@
  * "What does Paged Experts actually do?"): each step a router sends every token
  * to top_k of E experts; a per-layer table of K GPU slots holds K of the E
  * experts, all E live in pinned host RAM, the routed experts that are not
- * resident are copied in (least recently used out), then the fused MoE runs over
+ * resident are copied in (the oldest-used evicted), then the fused MoE runs over
  * the slot table: gate/up projection, SiLU*mul, down projection and the
  * top_k-weighted combine. Paging never changes the result (section "Can paging
  * change the model's outputs?"): outputs are bitwise identical for every K.

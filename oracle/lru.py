@@ -5,10 +5,10 @@ Sources:
   layer are kept on the GPU, all E in pinned host RAM, and a step copies in only
   the routed experts that are not resident.
   Same article, "What does Paged Experts actually do?" item 3: missing experts
-  are copied into slots, least recently used out.
+  are copied into slots, evicting the expert whose last use is oldest.
   Same article, "What happens with more than one request?": a decode step is one
-  wave only if tokens x top_k <= K; larger steps run several waves, each with its
-  own page-in.
+  wave only if tokens x top_k <= K; larger steps run several waves, and every wave
+  copies its own missing experts in before it computes.
   "Locality of reference helped ...", section "The fix": a hit computes from
   VRAM with no bytes moved; a miss copies that one expert and evicts the least
   recently used one.

@@ -2,9 +2,9 @@
 //
 // Article "Running an MoE Model Larger Than Your VRAM": TL;DR (copy in only the
 // routed experts that are not resident), section "What does Paged Experts actually
-// do?" item 3 (least recently used out) and section "What happens with more than one
-// request?" (more distinct experts than slots -> several waves, each with its own
-// page-in). Post "Locality of reference helped ...", section "The fix": a hit moves
+// do?" item 3 (the oldest-used expert is evicted) and section "What happens with more than one
+// request?" (more distinct experts than slots -> several waves, every one
+// copying its own missing experts in). Post "Locality of reference helped ...", section "The fix": a hit moves
 // no bytes, a miss copies one expert and evicts the least recently used one.
 //
 // The planning itself is step::lru_plan_core (step_common.cuh, which states the rules

@@ -4,7 +4,7 @@
 //
 // Article "Running an MoE Model Larger Than Your VRAM": section "What does Paged Experts
 // actually do?" (the router picks top_k experts per token; routed experts that are not
-// resident are copied in, least recently used out) and section "What happens with more
+// resident are copied in, evicting the oldest-used) and section "What happens with more
 // than one request?" (more distinct experts than slots -> several waves).
 #pragma once
 

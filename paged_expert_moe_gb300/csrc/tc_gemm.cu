@@ -3,7 +3,8 @@
 //
 // Article "Running an MoE Model Larger Than Your VRAM", sections "What does Paged
 // Experts actually do?" (the fused MoE runs over the resident slots) and "Why do
-// short prompts get slower first tokens?" (a prefill touches nearly every expert).
+// short prompts get slower first tokens?" (a prompt's tokens route to almost all
+// of a layer's experts).
 // With ~128 pairs per expert the contraction is dense enough for the tensor cores.
 //
 // Tiles (swap-AB: the weight rows are the MMA's M side, the expert's pairs the N side):

@@ -213,7 +213,8 @@ def test_expert_sizes_match_the_layout_closed_forms():
     assert formats.expert_nbytes(0, H, I) == 9_437_184
     assert formats.expert_nbytes(1, H, I) == 4_719_744  # 3*2048*768 weights + 288 fp32 scales
     assert formats.expert_nbytes(2, H, I) == 2_506_752  # packed nibbles + 36,864 x (fp16 s, fp16 z)
-    # "FP8 is about 4.72 MB (3 x 2048 x 768 weights at one byte, scales ignored)"
+    # the article's FP8 expert size counts the weights only, one byte each (section "Why is
+    # it fast when experts keep crossing PCIe?")
     assert 3 * H * I == 4_718_592
     # NVFP4: packed codes, then per matrix 16 bytes (fp32 tensor scale + padding) and one
     # e4m3 byte per row and 16 inputs
