@@ -36,19 +36,44 @@ __global__ void __launch_bounds__(kChunk) group_chunk_hist(const int32_t* __rest
   for (int e = threadIdx.x; e < E; e += blockDim.x) chunk_cnt[(size_t)blockIdx.x * E + e] = s_cnt[e];
 }
 
-// Pass 2 (one thread per expert): counts[e] and, in place, the exclusive prefix of
-// chunk_cnt[.][e] over chunks (the pairs of e in earlier chunks).
+// Pass 2 (one warp per expert): counts[e] and, in place, the exclusive prefix of
+// chunk_cnt[.][e] over chunks (the pairs of e in earlier chunks). Lane l takes the
+// chunks [l * seg, (l + 1) * seg): their sum, a warp scan of the lane sums, then the
+// prefixes. Loads go 16 at a time, so a lane's segment costs a few L2 round trips
+// instead of one per chunk.
 __global__ void __launch_bounds__(256) group_chunk_scan(int n_chunks, int E, int32_t* __restrict__ chunk_cnt,
                                                         int32_t* __restrict__ counts) {
-  const int e = blockIdx.x * blockDim.x + threadIdx.x;
-  if (e >= E) return;
-  int run = 0;
-  for (int c = 0; c < n_chunks; ++c) {
-    const int v = chunk_cnt[(size_t)c * E + e];
-    chunk_cnt[(size_t)c * E + e] = run;
-    run += v;
+  constexpr int kBatch = 16;
+  const int e = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5), lane = threadIdx.x & 31;
+  if (e >= E) return;  // e is the same for the whole warp
+  const int seg = (n_chunks + 31) / 32;
+  const int c0 = min(n_chunks, lane * seg), c1 = min(n_chunks, c0 + seg);
+  int sum = 0;
+  for (int b = c0; b < c1; b += kBatch) {
+    int v[kBatch];
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) v[i] = (b + i < c1) ? chunk_cnt[(size_t)(b + i) * E + e] : 0;
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) sum += v[i];
   }
-  counts[e] = run;
+  int incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  if (lane == 31) counts[e] = incl;
+  int run = incl - sum;
+  for (int b = c0; b < c1; b += kBatch) {
+    int v[kBatch];
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) v[i] = (b + i < c1) ? chunk_cnt[(size_t)(b + i) * E + e] : 0;
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      if (b + i < c1) chunk_cnt[(size_t)(b + i) * E + e] = run;
+      run += v[i];
+    }
+  }
 }
 
 // Pass 4 (one CTA per chunk): stable position of every pair:
@@ -268,7 +293,16 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const __nv_bfloat16* _
     const int t = perm[j] / top_k;
     const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H);
     uint4* dst = reinterpret_cast<uint4*>(x_perm + (size_t)j * H);
-    for (int c = lane; c < nvec; c += 32) dst[c] = __ldg(src + c);
+    // eight 16-byte loads per lane before their stores: a 4 KB row in flight per warp
+    for (int c0 = lane; c0 < nvec; c0 += 32 * 8) {
+      uint4 v[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (c0 + 32 * i < nvec) v[i] = __ldg(src + c0 + 32 * i);
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (c0 + 32 * i < nvec) dst[c0 + 32 * i] = v[i];
+    }
   }
 }
 
@@ -342,7 +376,7 @@ cudaError_t launch_group(const int32_t* ids, int P, int E, const int32_t* plan, 
   const int n_chunks = (P + kChunk - 1) / kChunk;
   if ((size_t)n_chunks * E > (size_t)ws.chunk_cap) return cudaErrorInvalidValue;
   group_chunk_hist<<<n_chunks, kChunk, 0, s>>>(ids, P, E, ws.chunk_cnt, err);
-  group_chunk_scan<<<(E + 255) / 256, 256, 0, s>>>(n_chunks, E, ws.chunk_cnt, ws.counts);
+  group_chunk_scan<<<(32 * E + 255) / 256, 256, 0, s>>>(n_chunks, E, ws.chunk_cnt, ws.counts);
   group_scan_tiles<<<1, 1024, 0, s>>>(E, plan, ws, tile_n, err);
   group_chunk_place<<<n_chunks, kChunk, 0, s>>>(ids, P, E, ws.chunk_cnt, ws);
   return cudaGetLastError();
