@@ -47,12 +47,15 @@ def _expect(ids, E):
 @pytest.mark.parametrize("T,k,E,skew", [(1, 1, 1, False), (1, 8, 128, False), (33, 4, 16, True), (100, 3, 5, True),
                                         (129, 8, 128, False), (512, 8, 128, False), (1024, 8, 128, True),
                                         (640, 8, 1024, False), (1025, 8, 128, False), (2048, 8, 128, False),
-                                        (2048, 8, 128, True), (1152, 8, 1024, False), (4097, 8, 128, False)])
+                                        (2048, 8, 128, True), (1152, 8, 1024, False), (4097, 8, 128, False),
+                                        (16384, 8, 128, True), (20000, 8, 128, False)])
 def test_grouping_equals_oracle(pm, T, k, E, skew):
     """Uniform and skewed routing, through the kernels the forward uses: one CTA with every
     pair in shared memory up to 1024 pairs (decode), the one-CTA counting sort up to 8192,
-    and four launches over per-chunk histograms beyond (2048 x 8 is the prefill workload).
-    Ragged warp ranges, chunks and tails."""
+    and four launches over per-chunk histograms beyond (2048 x 8 is the prefill workload;
+    16384 x 8 = 512 chunks gives each lane of the chunk scan one full batch of 16 chunks,
+    20000 x 8 = 625 chunks two batches with a ragged tail). Ragged warp ranges, chunks and
+    tails."""
     rng = np.random.default_rng(7000 + T * 7 + E)
     if skew:
         p = np.arange(E, 0, -1, dtype=np.float64) ** 2

@@ -139,3 +139,37 @@ def test_prefill_quantised_512_tokens_k40(pm, fmt):
     sample = np.random.default_rng(501).choice(T, size=16, replace=False)
     ids, w = orouter.router_topk(logits[sample], k)
     hz.assert_layer_close(hz.bf16_to_f64(y40)[sample], L.oracle_y(x_bits[sample], ids, w), fmt)
+
+
+@pytest.mark.parametrize("T,fmt", [(300, 0), (300, 1), (64, 1), (300, 4)])
+def test_prefill_sm_pull_mode_is_bitwise_identical_to_copy_engine(pm, T, fmt):
+    """SM-pull page-in (plan kept on the device, a pull kernel per wave, GEMMs launched for
+    an upper bound of waves that skip the ones the plan does not have) against copy-engine
+    page-in, in one cache per mode carried over several steps: the same misses and waves
+    as the LRU simulator and the same output bits. bf16, block-FP8 on both of its tile
+    paths, NVFP4; K = 5 (several waves a step) and K = 16 (all resident after the first)."""
+    E, k, H, I = 16, 4, 256, 384
+    L = hz.SyntheticLayer(fmt, E, H, I, seed=400 + T + fmt)
+    rng = np.random.default_rng(400 + T + fmt)
+    steps = []
+    for _ in range(3):
+        sets = _skewed_sets(rng, T, E, k, hot=int(rng.integers(E)))
+        steps.append((sets,) + hz.step_inputs(rng, sets, E, H))
+    for K in (5, 16):
+        ys = {}
+        for mode in (0, 1):
+            cache = hz.make_cache([L], k, K, max_tokens=T, mode=mode)
+            sim = olru.LayerLRU(E, K)
+            ys[mode] = []
+            for sets, x_bits, logits in steps:
+                before = cache.expert_cache_stats(0)
+                ys[mode].append(_forward(cache, x_bits, logits, k))
+                st = cache.expert_cache_stats(0)
+                out = sim.step(np.asarray(sets).ravel().tolist())
+                assert st["misses"] - before["misses"] == out["n_misses"]
+                assert st["waves"] - before["waves"] == len(out["waves"])
+            cache.close()
+        for i, (a, b) in enumerate(zip(ys[0], ys[1])):
+            assert torch.equal(a.view(torch.int16), b.view(torch.int16)), f"K={K} step {i}"
+    ids, w = orouter.router_topk(steps[-1][2], k)
+    hz.assert_layer_close(hz.bf16_to_f64(ys[1][-1]), L.oracle_y(steps[-1][1], ids, w), fmt)
