@@ -219,25 +219,39 @@ struct TcCfg {
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
-// Down epilogue: staging[row * 17 + i] holds the outputs of a tile's 128 weight rows for
-// its pairs c..c+15. Thread et (0..127 of the epilogue) writes pair c + (et & 15), rows
-// (et >> 4) * 16 .. +15 of m-tile mt, as bf16: two 16-byte stores, so a warp covers
-// whole 256-byte rows of o_part (the reads of staging hit 32 distinct banks).
-__device__ __forceinline__ void store_o_rows(const float* staging, int et, int c, int np, int pstart, int mt,
-                                             int H, float* o_part) {
-  const int pl = et & 15, js = (et >> 4) * 16;
-  if (c + pl >= np) return;
-  uint32_t w[8];
+// Down epilogue, one chunk of 16 pairs c..c+15 of an item (m-tile mt). Thread `row` (the
+// TMEM lane: weight row n = mt * 128 + row) holds v[i] for pair c + i; it rounds them to
+// bf16 and stages them two pairs to a word, stg[row * 9 + j] = (pair 2j, pair 2j + 1).
+// After a barrier, thread et (0..127) reads the words of pairs 2 (et & 7) and + 1 for
+// rows (et >> 3) * 8 .. +7 and writes each pair's 8 outputs as one 16-byte store. Half
+// the shared-memory traffic of fp32 staging; both sides hit 32 distinct banks.
+__device__ __forceinline__ void stage_o_chunk(uint32_t* stg, int row, const float* v) {
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
-    const __nv_bfloat162 b =
-        __floats2bfloat162_rn(staging[(js + 2 * j) * 17 + pl], staging[(js + 2 * j + 1) * 17 + pl]);
-    w[j] = *reinterpret_cast<const uint32_t*>(&b);
+    const __nv_bfloat162 b = __floats2bfloat162_rn(v[2 * j], v[2 * j + 1]);
+    stg[row * 9 + j] = *reinterpret_cast<const uint32_t*>(&b);
   }
-  uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(o_part) + (size_t)(pstart + c + pl) * H +
-                                        mt * 128 + js);
-  dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-  dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
+__device__ __forceinline__ void store_o_rows(const uint32_t* stg, int et, int c, int np, int pstart, int mt,
+                                             int H, float* o_part) {
+  const int pp = et & 7, rb = et >> 3;
+  const int p0 = c + 2 * pp;
+  if (p0 >= np) return;
+  uint32_t w[8];
+#pragma unroll
+  for (int r = 0; r < 8; ++r) w[r] = stg[(rb * 8 + r) * 9 + pp];
+  uint32_t lo[4], hi[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    lo[k] = (w[2 * k] & 0xffffu) | (w[2 * k + 1] << 16);
+    hi[k] = (w[2 * k] >> 16) | (w[2 * k + 1] & 0xffff0000u);
+  }
+  __nv_bfloat16* o16 = reinterpret_cast<__nv_bfloat16*>(o_part);
+  const size_t col = (size_t)mt * 128 + rb * 8;
+  *reinterpret_cast<uint4*>(o16 + (size_t)(pstart + p0) * H + col) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+  if (p0 + 1 < np)
+    *reinterpret_cast<uint4*>(o16 + (size_t)(pstart + p0 + 1) * H + col) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
 }
 
 // Named barrier over the 128 epilogue threads that also ORs a predicate across them,
@@ -703,10 +717,12 @@ __global__ void __launch_bounds__(TcCfg<FMT, NMAX>::kThreads, 1)
           }
           epi_bar();
         } else if (!kQuant) {
+          float f[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) staging[row * 17 + i] = __uint_as_float(v[i]);
+          for (int i = 0; i < 16; ++i) f[i] = __uint_as_float(v[i]);
+          stage_o_chunk(reinterpret_cast<uint32_t*>(staging), row, f);
           epi_bar();
-          store_o_rows(staging, et, c, np, pstart, mt, H, ws.o_part);
+          store_o_rows(reinterpret_cast<const uint32_t*>(staging), et, c, np, pstart, mt, H, ws.o_part);
           epi_bar();
         } else {
           // the converter warps bound this kernel on issue slots: fp32 rows straight from
@@ -1114,10 +1130,9 @@ __global__ void __launch_bounds__(F8Cfg::kThreads, 1)
 #pragma unroll
         for (int cc = 0; cc < kN; cc += 16) {
           if (cc < np) {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) staging[row * 17 + i] = acc[cc + i];
+            stage_o_chunk(reinterpret_cast<uint32_t*>(staging), row, acc + cc);
             grp_bar(g);
-            store_o_rows(staging, et, cc, np, pstart, mt, H, ws.o_part);
+            store_o_rows(reinterpret_cast<const uint32_t*>(staging), et, cc, np, pstart, mt, H, ws.o_part);
             grp_bar(g);
           }
         }
