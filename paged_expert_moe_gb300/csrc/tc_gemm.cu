@@ -578,13 +578,27 @@ __global__ void __launch_bounds__(TcCfg<FMT, NMAX>::kThreads, 1)
         }
         const uint8_t* qt = qring + q * C::kQBytes;  // row r at qt + r * (kQBytes / 128)
         uint4* arow = reinterpret_cast<uint4*>(aring + s * C::kABytes + r * 128);
+        // this thread's 32 (e4m3) or 16 (4-bit) bytes of its row: 16-byte chunks at their
+        // swizzled places (64-byte rows: chunk k at k ^ ((r >> 1) & 3); 32-byte rows: chunk
+        // k at k ^ ((r >> 2) & 1)), conflict-free across the warp's 32 rows
+        uint32_t qw[8];
         if (FMT == PMOE_FP8_BLOCK128) {
-          const uint8_t* qr = qt + r * kBK;
+          const uint8_t* qrow = qt + r * kBK;
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            const uint4 v = *reinterpret_cast<const uint4*>(qrow + (((2 * hf + k) ^ ((r >> 1) & 3)) << 4));
+            qw[4 * k + 0] = v.x, qw[4 * k + 1] = v.y, qw[4 * k + 2] = v.z, qw[4 * k + 3] = v.w;
+          }
+        } else {
+          const uint4 v = *reinterpret_cast<const uint4*>(qt + r * (kBK / 2) + ((hf ^ ((r >> 2) & 1)) << 4));
+          qw[0] = v.x, qw[1] = v.y, qw[2] = v.z, qw[3] = v.w;
+        }
+        if (FMT == PMOE_FP8_BLOCK128) {
           const float sv = __uint_as_float(cached ? my_sc[(kb * kBK) >> 7] : __ldg(srow + ((kb * kBK) >> 7)));
 #pragma unroll
-          for (int c = 4 * hf; c < 4 * hf + 4; ++c) {
-            const uint2 v = *reinterpret_cast<const uint2*>(qr + c * 8);
-            const uint32_t wv[2] = {v.x, v.y};
+          for (int ci = 0; ci < 4; ++ci) {
+            const int c = 4 * hf + ci;
+            const uint32_t wv[2] = {qw[2 * ci], qw[2 * ci + 1]};
             uint32_t out[4];
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
@@ -602,11 +616,11 @@ __global__ void __launch_bounds__(TcCfg<FMT, NMAX>::kThreads, 1)
         } else if (FMT == PMOE_NVFP4) {
           // 64 codes = four blocks of 16, each with its own e4m3 byte; E2M1 times e4m3
           // is exact in bf16
-          const uint8_t* qr = qt + r * (kBK / 2);
           const uint32_t bw = cached ? my_sc[kb] : __ldg(srow + kb);
 #pragma unroll
-          for (int c = 4 * hf; c < 4 * hf + 4; ++c) {
-            const uint32_t word = *reinterpret_cast<const uint32_t*>(qr + c * 4);  // 8 codes, low nibble first
+          for (int ci = 0; ci < 4; ++ci) {
+            const int c = 4 * hf + ci;
+            const uint32_t word = qw[ci];  // 8 codes, low nibble first
             const __half_raw sh = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)((bw >> (8 * (c >> 1))) & 0xffu), __NV_E4M3);
             const float sv = __half2float(*reinterpret_cast<const __half*>(&sh));
             uint32_t out[4];
@@ -622,12 +636,12 @@ __global__ void __launch_bounds__(TcCfg<FMT, NMAX>::kThreads, 1)
           }
         } else if (FMT == PMOE_MXFP4) {
           // 64 codes = two blocks of 32, each with its own E8M0 byte
-          const uint8_t* qr = qt + r * (kBK / 2);
           const uint32_t xw = cached ? my_sc[(kb * kBK) >> 7] : __ldg(srow + ((kb * kBK) >> 7));
           const int xb = ((kb * kBK) >> 5) & 3;  // first of the stage's two scale bytes in the word
 #pragma unroll
-          for (int c = 4 * hf; c < 4 * hf + 4; ++c) {
-            const uint32_t word = *reinterpret_cast<const uint32_t*>(qr + c * 4);  // 8 codes, low nibble first
+          for (int ci = 0; ci < 4; ++ci) {
+            const int c = 4 * hf + ci;
+            const uint32_t word = qw[ci];  // 8 codes, low nibble first
             const uint32_t xbyte = (xw >> (8 * (xb + (c >> 2)))) & 0xffu;
             const float sv = xbyte ? __uint_as_float(xbyte << 23) : __uint_as_float(0x00400000u);
             uint32_t out[4];
@@ -642,12 +656,12 @@ __global__ void __launch_bounds__(TcCfg<FMT, NMAX>::kThreads, 1)
             arow[c ^ (r & 7)] = make_uint4(out[0], out[1], out[2], out[3]);
           }
         } else {
-          const uint8_t* qr = qt + r * (kBK / 2);
           const uint32_t szw = cached ? my_sc[(kb * kBK) >> 7] : __ldg(srow + ((kb * kBK) >> 7));
           const float2 sz = __half22float2(*reinterpret_cast<const __half2*>(&szw));
 #pragma unroll
-          for (int c = 4 * hf; c < 4 * hf + 4; ++c) {
-            const uint32_t word = *reinterpret_cast<const uint32_t*>(qr + c * 4);  // 8 nibbles, low first
+          for (int ci = 0; ci < 4; ++ci) {
+            const int c = 4 * hf + ci;
+            const uint32_t word = qw[ci];  // 8 nibbles, low first
             uint32_t out[4];
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
@@ -1166,9 +1180,11 @@ EncodeTiledFn get_encode() {
   return fn;
 }
 
-// bf16 elements with the 128-byte swizzle (MMA operands), raw bytes unswizzled (the
-// converters' input), or bytes with the 128-byte swizzle (e4m3 MMA operands)
-enum MapKind { kMapBf16Sw128, kMapBytes, kMapBytesSw128 };
+// bf16 elements with the 128-byte swizzle (MMA operands), bytes with the 128-byte
+// swizzle (e4m3 MMA operands), or raw quantised bytes with the 64- or 32-byte swizzle (the
+// converters' input: a tile row is 64 bytes of e4m3 or 32 of 4-bit codes, and the swizzle
+// spreads 32 consecutive rows' 16-byte chunks over all banks)
+enum MapKind { kMapBf16Sw128, kMapBytesSw128, kMapBytesSw64, kMapBytesSw32 };
 
 int encode(CUtensorMap* m, void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides_bytes,
            const cuuint32_t* box, MapKind kind = kMapBf16Sw128) {
@@ -1177,7 +1193,9 @@ int encode(CUtensorMap* m, void* base, int rank, const cuuint64_t* dims, const c
   cuuint32_t estr[5] = {1, 1, 1, 1, 1};  // element strides, one per dimension (rank <= 5)
   const CUresult r = fn(m, kind == kMapBf16Sw128 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8,
                         rank, base, dims, strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        kind == kMapBytes ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+                        kind == kMapBytesSw64   ? CU_TENSOR_MAP_SWIZZLE_64B
+                        : kind == kMapBytesSw32 ? CU_TENSOR_MAP_SWIZZLE_32B
+                                                : CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? PMOE_OK : PMOE_ECUDA;
 }
@@ -1282,8 +1300,9 @@ int tc_make_weight_maps(uint8_t* arena, size_t stride, int K, int H, int I, int 
     const cuuint32_t box[3] = {128, 128, 1};
     if (encode(&out->d8, arena + lay.d_w, 3, dims, strides, box, kMapBytesSw128) != PMOE_OK) return PMOE_ECUDA;
   }
-  // quantised weights are loaded as bytes (one e4m3, or two int4 / E2M1 codes, per byte), unswizzled
-  // (NVFP4's codes are laid out as MXFP4's)
+  // quantised weights are loaded as bytes (one e4m3, or two int4 / E2M1 codes, per byte), rows of
+  // 64 or 32 bytes with the swizzle of that width (NVFP4's codes are laid out as MXFP4's)
+  const MapKind qkind = fmt == PMOE_FP8_BLOCK128 ? kMapBytesSw64 : kMapBytesSw32;
   const cuuint64_t hb = fmt == PMOE_FP8_BLOCK128 ? (cuuint64_t)H : (cuuint64_t)H / 2;
   const cuuint64_t ib = fmt == PMOE_FP8_BLOCK128 ? (cuuint64_t)I : (cuuint64_t)I / 2;
   const cuuint32_t kbb = fmt == PMOE_FP8_BLOCK128 ? (cuuint32_t)kBK : (cuuint32_t)kBK / 2;
@@ -1291,12 +1310,12 @@ int tc_make_weight_maps(uint8_t* arena, size_t stride, int K, int H, int I, int 
     const cuuint64_t dims[3] = {hb, (cuuint64_t)(2 * I), (cuuint64_t)K};
     const cuuint64_t strides[2] = {hb, (cuuint64_t)stride};
     const cuuint32_t box[3] = {kbb, 64, 1};
-    if (encode(&out->gu, arena + lay.gu_w, 3, dims, strides, box, kMapBytes) != PMOE_OK) return PMOE_ECUDA;
+    if (encode(&out->gu, arena + lay.gu_w, 3, dims, strides, box, qkind) != PMOE_OK) return PMOE_ECUDA;
   }
   const cuuint64_t dims[3] = {ib, (cuuint64_t)H, (cuuint64_t)K};
   const cuuint64_t strides[2] = {ib, (cuuint64_t)stride};
   const cuuint32_t box[3] = {kbb, 128, 1};
-  return encode(&out->d, arena + lay.d_w, 3, dims, strides, box, kMapBytes) == PMOE_OK ? PMOE_OK : PMOE_ECUDA;
+  return encode(&out->d, arena + lay.d_w, 3, dims, strides, box, qkind) == PMOE_OK ? PMOE_OK : PMOE_ECUDA;
 }
 
 int tc_make_act_maps(int fmt, __nv_bfloat16* x_perm, __nv_bfloat16* h, size_t P, int H, int I, TcMaps* out) {
