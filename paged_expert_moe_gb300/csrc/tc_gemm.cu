@@ -14,8 +14,9 @@
 //            bf16(silu(gate) * up) as 16-byte rows.           K = H, BK = 64
 //   down     D[128 rows n][N pairs] = W_d[n0:n0+128, :] . h[pairs, :]^T; the epilogue
 //            writes the pair's expert output o_part[pair][n]: bf16 weights as bf16
-//            rows through shared memory (half the bytes for the combine to read),
-//            quantised ones (converter warps) as fp32 rows.  K = I, BK = 64
+//            rows (half the bytes for the combine to read), staged through shared
+//            memory two pairs to a word; quantised ones (converter warps) as fp32
+//            rows.                                             K = I, BK = 64
 // The two TMEM accumulator buffers (2 x 256 columns) let the epilogue of one item run
 // while the MMAs of the next fill the other buffer; 4 TMA stages of 48 KB. Every TMA
 // instruction costs time of its own, so a bf16 stage is few boxes: gate/up's weight tile
@@ -26,9 +27,10 @@
 // Warp roles: warp 0 lane 0 issues TMA, warp 1 lane 0 issues tcgen05.mma (warp 1 owns
 // the TMEM allocation), warps 2-5 drain TMEM (32 lanes each) in the epilogue. Quantised
 // weights: warp 0 streams the raw weight tiles into a deep ring of their own, warp 14
-// the activation tiles, and converter warps 6-13 dequantise each raw tile into a shallow
-// ring of bf16 operand tiles (the raw bytes, not the operand tiles, are what must be in
-// flight from HBM).
+// the activation tiles, and converter warps 6-13 dequantise each raw tile (loaded with the
+// TMA swizzle of its 64- or 32-byte rows, so that their reads are conflict-free) into a
+// shallow ring of bf16 operand tiles (the raw bytes, not the operand tiles, are what must
+// be in flight from HBM).
 // Every mbarrier wait is bounded; on expiry the CTA records kErrTcTimeout, stops,
 // waits (bounded) for its copies in flight, frees its TMEM and returns.
 #include "tc_gemm.h"
